@@ -1,0 +1,129 @@
+/*
+ * fa_api.h -- libfa_b200: FlashAttention forward pass on one GB300 (sm_103a).
+ *
+ * C ABI (extern "C"), plain pointers and sizes.  The library computes
+ *
+ *     O   = softmax(scale * Q K^T  [+ causal mask]) V
+ *     lse = log(sum_j exp(scale * Q K^T)_ij)            (natural log, per row)
+ *
+ * tile by tile with online-softmax rescaling: the S = QK^T and P = softmax(S)
+ * matrices never reach device memory.  The operation is the reference
+ * attention of "ops-transformer FlashAttention build and tuning" (section 4.3,
+ * compute_reference_attention: scaled QK^T, triu(diagonal=1) filled with -inf
+ * when causal, softmax, times V); the same page (section 1.2) describes the
+ * FlashAttention-2 form used here -- Q blocks in the outer loop, K/V blocks
+ * streamed in the inner loop, online normalisation of the softmax.  The
+ * argument list mirrors the torch_npu entry point traced on the page
+ * "npu_flash_attention, from ATen down to the Cube unit" (the
+ * npu_flash_attention(q, k, v, head_num, input_layout, scale, keep_prob) call):
+ * head count, layout string BNSD/BSND and scale become B, H, S_q, S_kv, D,
+ * fa_layout_t and `scale`; keep_prob is fixed at 1.0 (no dropout).
+ */
+#ifndef FA_API_H
+#define FA_API_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Tensor layouts.  Both are dense and contiguous, innermost dimension last:
+ *   FA_LAYOUT_BNSD: [B, H, S, D]   (batch, heads, sequence, head dim)
+ *   FA_LAYOUT_BSND: [B, S, H, D]   (the pages' [batch, seq, heads*head_dim])  */
+typedef enum { FA_LAYOUT_BNSD = 0, FA_LAYOUT_BSND = 1 } fa_layout_t;
+
+/* Element types of Q, K and V.
+ *   FA_DTYPE_F16      IEEE binary16; O is binary16.
+ *   FA_DTYPE_BF16     bfloat16; O is bfloat16.
+ *   FA_DTYPE_FP8E4M3  OCP FP8 E4M3 ("fn": max 448, no inf) with one fp32 descale
+ *                     per tensor (real value = code * descale); O is bfloat16.  */
+typedef enum { FA_DTYPE_F16 = 0, FA_DTYPE_BF16 = 1, FA_DTYPE_FP8E4M3 = 2 } fa_dtype_t;
+
+/* Status codes.  Errors are returned, never thrown or trapped. */
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,    /* null pointer, size < 1, non-finite or negative scale,
+                                descale given for a 16-bit dtype, bad enum              */
+  FA_ERR_UNSUPPORTED = 2,    /* D not in {64, 128}, or a size past the library's limits  */
+  FA_ERR_MISALIGNED = 3,     /* a tensor pointer not 16-byte aligned (TMA requirement)   */
+  FA_ERR_CUDA = 4,           /* a CUDA runtime/driver call or the launch failed          */
+  FA_ERR_DEVICE_TIMEOUT = 5  /* a bounded device-side wait expired (kernel gave up)      */
+} fa_status_t;
+
+/*
+ * fa_fwd -- one FlashAttention forward pass, asynchronous on `stream`.
+ *
+ * q    device, [B,H,S_q,D] or [B,S_q,H,D] per `layout`, element type `dtype`.
+ * k, v device, same layout with S_kv rows, element type `dtype`.  K and V get
+ *      separate descriptors (the Hygon retrospective, defect 13, is a backward
+ *      kernel that read V with K's stride).
+ * o    device, same layout and shape as q; element type: f16 for F16, bf16 for
+ *      BF16 and FP8E4M3.  Only rows < S_q are written.
+ * lse  device, fp32 [B, H, S_q] contiguous in every layout, natural log of the
+ *      row's softmax denominator including `scale` (and the descales).
+ * B, H, S_q, S_kv, D   sizes; all >= 1, D in {64, 128}.  Offsets are 64-bit:
+ *      a single tensor may exceed 4 GB (the Hygon retrospective, defect 1).
+ * scale  finite, >= 0; multiplies Q K^T before the softmax (commonly D^-0.5).
+ * layout FA_LAYOUT_BNSD or FA_LAYOUT_BSND (o follows q's layout).
+ * causal 0: every key visible.  Non-zero: query row i sees key j only if j <= i
+ *      (top-left aligned, the verifier's triu(diagonal=1) mask; with S_q == S_kv
+ *      this is the usual lower-triangular mask).
+ * dtype  see fa_dtype_t.
+ * descale_q/k/v  FP8 only: device pointers to one fp32 each, or NULL for 1.0.
+ *      Must all be NULL for the 16-bit dtypes.
+ * stream the CUDA stream to launch on (0 = legacy default stream).
+ *
+ * Pointers q, k, v, o must be 16-byte aligned; lse 4-byte aligned.  The caller
+ * owns every buffer; the library allocates nothing per call and keeps no
+ * per-call state.  Inputs may be NaN-poisoned past their last valid row: no
+ * element outside [0, S) is read.  The checks above run on the host before
+ * any launch and return an error without touching the device.
+ * Returns FA_OK once the kernel is enqueued; FA_ERR_CUDA if a CUDA call or
+ * the launch fails.  A bounded device-side wait that expires sets the
+ * library's device error word; fa_last_device_error() reports it.
+ */
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int64_t B, int64_t H, int64_t S_q, int64_t S_kv, int64_t D, float scale,
+                   fa_layout_t layout, int causal, fa_dtype_t dtype, const float* descale_q,
+                   const float* descale_k, const float* descale_v, cudaStream_t stream);
+
+/* A static, human-readable name for a status code (never NULL). */
+const char* fa_status_string(fa_status_t s);
+
+/*
+ * fa_last_device_error -- synchronises `stream`, then reads and clears the
+ * device error word of the current device.  Returns FA_OK if no kernel of this
+ * library on that device has reported an error since the last call,
+ * FA_ERR_DEVICE_TIMEOUT if a bounded wait expired, FA_ERR_CUDA if the
+ * synchronisation or the read failed.
+ */
+fa_status_t fa_last_device_error(cudaStream_t stream);
+
+/*
+ * fa_set_wait_limit_ns -- the time limit, in nanoseconds of the device's
+ * global timer, after which a device-side wait gives up and reports
+ * FA_ERR_DEVICE_TIMEOUT (default 2e9 = 2 s).  0 restores the default.  A
+ * process-wide host setting, read at each launch.
+ */
+void fa_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * fa_probe_wait_timeout -- launches one block whose thread waits on a
+ * shared-memory barrier that nothing ever arrives at, using the same bounded
+ * wait as fa_fwd, with the given limit (ns).  The wait must expire, set the
+ * device error word and return; the call then returns what
+ * fa_last_device_error() reports (FA_ERR_DEVICE_TIMEOUT when the mechanism
+ * works).  It exists so that the timeout path can be tested without a hang.
+ */
+fa_status_t fa_probe_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
+/* Library version, "major.minor.patch". */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_API_H */

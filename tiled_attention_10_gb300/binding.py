@@ -1,0 +1,129 @@
+"""ctypes binding of libfa_b200 (include/fa_api.h): argument marshalling only.
+
+Every step of the forward pass runs in the CUDA library.  There is no CPU or
+PyTorch fallback: if the library is missing, `load()` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_b200.so")
+
+FA_LAYOUT = {"BNSD": 0, "BSND": 1}
+FA_DTYPE = {"f16": 0, "bf16": 1, "e4m3": 2}
+FA_STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
+             3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
+
+# Symbols the header declares; the library must export all of them.
+EXPORTS = ("fa_fwd", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
+           "fa_probe_wait_timeout", "fa_version")
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {FA_STATUS.get(status, status)} ({fa_status_string(status)})")
+
+
+def load(path: str = LIB_PATH):
+    """Load libfa_b200.so (built by __graft_entry__.build()); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FileNotFoundError(
+            f"{path} is missing: build the CUDA library first (python -c "
+            "'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i64, f32, ip, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_uint64
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, ip, ip, ip,
+                           vp, vp, vp, vp]
+    lib.fa_fwd.restype = ip
+    lib.fa_status_string.argtypes = [ip]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_last_device_error.argtypes = [vp]
+    lib.fa_last_device_error.restype = ip
+    lib.fa_set_wait_limit_ns.argtypes = [u64]
+    lib.fa_set_wait_limit_ns.restype = None
+    lib.fa_probe_wait_timeout.argtypes = [u64, vp]
+    lib.fa_probe_wait_timeout.restype = ip
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def fa_status_string(status: int) -> str:
+    if _lib is None:
+        return FA_STATUS.get(status, "unknown status")
+    return _lib.fa_status_string(int(status)).decode()
+
+
+def fa_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, scale, layout, causal, dtype,
+           descale_q=None, descale_k=None, descale_v=None, stream=None) -> int:
+    """Same arguments as the C call; pointers as ints (or None), enums as names
+    or codes.  Returns the fa_status_t code."""
+    lib = load()
+    lay = FA_LAYOUT[layout] if isinstance(layout, str) else int(layout)
+    dt = FA_DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
+    return int(lib.fa_fwd(q, k, v, o, lse, int(B), int(H), int(S_q), int(S_kv), int(D),
+                          float(scale), lay, int(bool(causal)), dt, descale_q, descale_k,
+                          descale_v, stream))
+
+
+def fa_last_device_error(stream=None) -> int:
+    return int(load().fa_last_device_error(stream))
+
+
+def fa_set_wait_limit_ns(ns: int) -> None:
+    load().fa_set_wait_limit_ns(int(ns))
+
+
+def fa_probe_wait_timeout(limit_ns: int, stream=None) -> int:
+    return int(load().fa_probe_wait_timeout(int(limit_ns), stream))
+
+
+# --------------------------------------------------------------------------
+# Convenience wrapper over torch CUDA tensors (allocation only; the work is
+# the single fa_fwd call).
+# --------------------------------------------------------------------------
+def attention(q, k, v, *, causal=False, scale=None, layout="BNSD", descale=None,
+              out=None, lse=None, stream=None):
+    """O, lse = attention(q, k, v): q/k/v torch CUDA tensors in `layout`.
+
+    dtype follows q (float16, bfloat16 or float8_e4m3fn).  `descale` for FP8 is
+    a tuple of three 1-element fp32 CUDA tensors (or None for 1.0 each).
+    """
+    import torch
+    dmap = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float8_e4m3fn: "e4m3"}
+    if q.dtype not in dmap:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    dtype = dmap[q.dtype]
+    if layout == "BNSD":
+        B, H, S_q, D = q.shape
+        S_kv = k.shape[2]
+    else:
+        B, S_q, H, D = q.shape
+        S_kv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    odt = torch.float16 if dtype == "f16" else torch.bfloat16
+    if out is None:
+        out = torch.empty(q.shape, dtype=odt, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device)
+    ds = [None, None, None]
+    if descale is not None:
+        ds = [None if t is None else t.data_ptr() for t in descale]
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
+                S_q, S_kv, D, scale, layout, causal, dtype, ds[0], ds[1], ds[2], stream)
+    if st != 0:
+        raise FaError(st, "fa_fwd")
+    return out, lse
