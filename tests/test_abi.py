@@ -1,0 +1,77 @@
+"""The C-ABI library: it builds, loads, exports every symbol include/fa_api.h
+declares, and rejects bad arguments on the host before touching a device.
+No test here launches a kernel, so they all run without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tiled_attention_10_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "fa_api.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_what_binding_expects():
+    assert set(_declared_functions()) == set(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = binding.fa_status_string(code)
+        assert s and s != "unknown status"
+    assert binding.fa_status_string(99) == "unknown status"
+    assert lib.fa_version().decode().count(".") == 2
+
+
+GOOD = dict(q=16, k=32, v=48, o=64, lse=80, B=1, H=1, S_q=8, S_kv=8, D=128, scale=0.1,
+            layout="BNSD", causal=0, dtype="bf16")
+
+
+def _call(**over):
+    a = dict(GOOD)
+    a.update(over)
+    return binding.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["S_q"],
+                          a["S_kv"], a["D"], a["scale"], a["layout"], a["causal"], a["dtype"],
+                          a.get("dq"), a.get("dk"), a.get("dv"), None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1), (dict(lse=None), 1),
+    (dict(B=0), 1), (dict(H=0), 1), (dict(S_q=0), 1), (dict(S_kv=0), 1), (dict(D=0), 1),
+    (dict(S_kv=-5), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=-1.0), 1), (dict(layout=7), 1), (dict(dtype=9), 1),
+    (dict(dq=16), 1),                                   # descale with a 16-bit dtype
+    (dict(D=96), 2), (dict(D=256), 2), (dict(D=64, dtype="e4m3"), 2),
+    (dict(S_q=1 << 31), 2),
+    (dict(q=8), 3), (dict(o=24), 3), (dict(lse=82), 3),
+    (dict(dtype="e4m3", dq=18), 3),
+])
+def test_invalid_arguments_rejected_on_host(lib, over, code):
+    # Pointers are fake and never dereferenced: every case fails validation
+    # before any CUDA call.
+    assert _call(**over) == code
+
+
+def test_loads_without_gpu_and_does_not_fallback():
+    # The binding has no CPU path: the only compute entry point is the C call.
+    src = open(os.path.join(ROOT, "tiled_attention_10_gb300", "binding.py")).read()
+    assert "oracle" not in src
+    assert "scaled_dot_product_attention" not in src

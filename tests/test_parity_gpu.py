@@ -1,0 +1,73 @@
+"""GPU parity: the C-ABI call against the float64 oracle, element by element.
+
+Small shapes span several 128-row tiles and ragged tails; every output row is
+compared.  Tolerances are the max-abs bounds of the method's specification:
+O within 4e-3 (fp16), 1.6e-2 (bf16), 6e-2 (fp8 e4m3); lse within 1e-3.
+"""
+import pytest
+import torch
+
+from tiled_attention_10_gb300.inputs import Workload
+from tests.gpu_helpers import run_small
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    # B, H, S_q, S_kv
+    (1, 1, 128, 128),
+    (1, 2, 256, 256),
+    (2, 1, 384, 512),
+    (1, 1, 1, 1),
+    (1, 1, 2, 3),
+    (1, 3, 63, 64),
+    (2, 2, 127, 129),
+    (1, 2, 129, 127),
+    (1, 1, 255, 257),
+    (1, 1, 300, 700),
+    (2, 1, 640, 200),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D", [128, 64])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,S_q,S_kv", SHAPES)
+def test_parity_bnsd(B, H, S_q, S_kv, D, dtype, causal, cuda_lib):
+    w = Workload("t", B, H, S_q, S_kv, D, dtype, "BNSD", causal, seed=S_q * 7 + S_kv)
+    run_small(w)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,S_q,S_kv", [(2, 3, 200, 200), (1, 4, 129, 300), (2, 2, 513, 257)])
+def test_parity_bsnd_poisoned(B, H, S_q, S_kv, D, dtype, causal, cuda_lib):
+    """BSND with NaN bit patterns in the memory after the last valid row."""
+    w = Workload("t", B, H, S_q, S_kv, D, dtype, "BSND", causal, poison=True, seed=S_q + 3 * S_kv)
+    run_small(w)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("S_q,S_kv", [(128, 128), (200, 333), (1, 1), (512, 512)])
+def test_parity_fp8(S_q, S_kv, causal, cuda_lib):
+    w = Workload("t", 1, 3, S_q, S_kv, 128, "e4m3", "BNSD", causal, seed=S_q + S_kv)
+    run_small(w)
+
+
+@pytest.mark.parametrize("scale", [0.0, 0.02, 1.0])
+def test_parity_scales(scale, cuda_lib):
+    w = Workload("t", 1, 2, 200, 260, 128, "bf16", "BNSD", True, scale=scale, seed=4)
+    run_small(w)
+
+
+def test_large_logits_stay_finite(cuda_lib):
+    """The FP16 overflow trap of the Ascend page (section 6.2): logits far above
+    ln(65504) must not overflow -- scale 8 on N(0,1) data, D=64: scores ~ +-300."""
+    w = Workload("t", 1, 2, 256, 256, 64, "f16", "BNSD", False, scale=8.0, seed=5)
+    run_small(w)
+
+
+def test_many_units_persistent_schedule(cuda_lib):
+    """More units than SMs: every CTA walks several units."""
+    w = Workload("t", 4, 40, 256, 256, 64, "bf16", "BNSD", True, seed=6)
+    run_small(w)

@@ -1,0 +1,264 @@
+/*
+ * fa_api.cu -- host side of libfa_b200 (see include/fa_api.h).
+ *
+ * Argument checks (all before any CUDA call), TMA descriptor encoding with
+ * 64-bit strides and per-dimension bounds, schedule parameters, the launch,
+ * and the device error word that bounded waits report into.
+ *
+ * The page "npu_flash_attention, from ATen down to the Cube unit" walks the
+ * Ascend call through op registration, a tiling calculation that fails with
+ * "UB overflow", allocation and task submission; here the whole of that is
+ * one validation pass and one asynchronous kernel launch, and every failure
+ * is a returned status.
+ */
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa_api.h"
+#include "fa_kernel.cuh"
+
+namespace fa {
+// Explicit instantiations live in fa_inst_*.cu (compiled in parallel).
+extern template cudaError_t launch_fa_fwd<64, kDtF16>(const CUtensorMap&, const CUtensorMap&,
+                                                       const CUtensorMap&, const KernelParams&,
+                                                       int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<128, kDtF16>(const CUtensorMap&, const CUtensorMap&,
+                                                        const CUtensorMap&, const KernelParams&,
+                                                        int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<64, kDtBF16>(const CUtensorMap&, const CUtensorMap&,
+                                                        const CUtensorMap&, const KernelParams&,
+                                                        int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<128, kDtBF16>(const CUtensorMap&, const CUtensorMap&,
+                                                         const CUtensorMap&, const KernelParams&,
+                                                         int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<128, kDtE4M3>(const CUtensorMap&, const CUtensorMap&,
+                                                         const CUtensorMap&, const KernelParams&,
+                                                         int, cudaStream_t);
+}  // namespace fa
+
+// Device error word: bounded waits OR their error bits in here.
+__device__ uint32_t g_fa_device_error = 0;
+
+namespace {
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  uint32_t* err_word = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+// Per-device facts, looked up once with that device current.
+fa_status_t device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FA_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_device_error) != cudaSuccess) return FA_ERR_CUDA;
+    d.sm_count = sms;
+    d.err_word = static_cast<uint32_t*>(p);
+    d.ready = true;
+  }
+  *out = d;
+  return FA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 4-D tensor map over a [B,H,S,D] (BNSD) or [B,S,H,D] (BSND) tensor, boxes
+// of 128 rows x 128 bytes, 128-byte swizzle, zero fill out of bounds.  The
+// sequence dimension is its own map dimension, so rows >= S are never read
+// (in BSND the bytes after row S-1 of batch b are batch b+1's rows).
+bool make_map(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, fa_layout_t layout, int64_t B,
+              int64_t H, int64_t S, int64_t D) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const uint64_t eb = (dtype == FA_DTYPE_FP8E4M3) ? 1 : 2;
+  const CUtensorMapDataType t = dtype == FA_DTYPE_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                : dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+  const cuuint32_t inner = static_cast<cuuint32_t>(128 / eb);
+  if (layout == FA_LAYOUT_BNSD) {
+    dims[0] = D; dims[1] = S; dims[2] = H; dims[3] = B;
+    strides[0] = D * eb; strides[1] = S * D * eb; strides[2] = H * S * D * eb;
+    box[0] = inner; box[1] = 128; box[2] = 1; box[3] = 1;
+  } else {
+    dims[0] = D; dims[1] = H; dims[2] = S; dims[3] = B;
+    strides[0] = D * eb; strides[1] = H * D * eb; strides[2] = S * H * D * eb;
+    box[0] = inner; box[1] = 1; box[2] = 128; box[3] = 1;
+  }
+  CUresult r = enc(m, t, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+__global__ void fa_wait_probe_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t a = fa::smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    fa::mbar_init(a, 1);
+    abort_flag = 0;
+    fa::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const fa::WaitCtl wc{limit_ns, err, &abort_flag};
+    (void)fa::mbar_wait(a, 0u, wc);  // nothing ever arrives: must time out
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_version(void) { return "0.1.0"; }
+
+const char* fa_status_string(fa_status_t s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+void fa_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs);
+}
+
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                   int64_t H, int64_t S_q, int64_t S_kv, int64_t D, float scale,
+                   fa_layout_t layout, int causal, fa_dtype_t dtype, const float* descale_q,
+                   const float* descale_k, const float* descale_v, cudaStream_t stream) {
+  // ---- host-side checks: nothing below touches the device until they pass
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S_q < 1 || S_kv < 1 || D < 1) return FA_ERR_INVALID_ARG;
+  if (layout != FA_LAYOUT_BNSD && layout != FA_LAYOUT_BSND) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP8E4M3)
+    return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.0f) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_FP8E4M3 && (descale_q || descale_k || descale_v)) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_FP8E4M3 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  if (dtype == FA_DTYPE_FP8E4M3 &&
+      (!aligned(descale_q, 4) || !aligned(descale_k, 4) || !aligned(descale_v, 4)))
+    return FA_ERR_MISALIGNED;
+  // Limits: row coordinates are 32-bit in the TMA descriptors, the unit count
+  // is a 32-bit index, and TMA strides must stay below 2^40 bytes.
+  const int64_t kMaxSeq = (int64_t(1) << 31) - 256;
+  if (S_q > kMaxSeq || S_kv > kMaxSeq || B > INT32_MAX || H > INT32_MAX) return FA_ERR_UNSUPPORTED;
+  const int64_t eb = (dtype == FA_DTYPE_FP8E4M3) ? 1 : 2;
+  const int64_t n_qtiles = (S_q + 127) / 128;
+  const int64_t n_pairs = (n_qtiles + 1) / 2;
+  if (B * H > INT32_MAX / n_pairs) return FA_ERR_UNSUPPORTED;
+  const int64_t max_s = S_q > S_kv ? S_q : S_kv;
+  if ((double)H * (double)max_s * (double)D * (double)eb >= 1099511627776.0)
+    return FA_ERR_UNSUPPORTED;
+
+  DeviceInfo dev;
+  if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
+
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, dtype, layout, B, H, S_q, D) || !make_map(&mk, k, dtype, layout, B, H, S_kv, D) ||
+      !make_map(&mv, v, dtype, layout, B, H, S_kv, D))
+    return FA_ERR_CUDA;
+
+  fa::KernelParams p = {};
+  p.B = B; p.H = H; p.S_q = S_q; p.S_kv = S_kv;
+  p.n_kv_blocks = static_cast<int32_t>((S_kv + 127) / 128);
+  p.n_pairs = static_cast<int32_t>(n_pairs);
+  p.num_units = static_cast<int32_t>(B * H * n_pairs);
+  // Causal: group heads so that the K/V of the heads in flight together fit
+  // comfortably in L2 (about 48 MB); longest pairs first inside each group.
+  int64_t group = 1;
+  if (causal) {
+    const int64_t kv_bytes = 2 * S_kv * D * eb;
+    group = (48ll << 20) / (kv_bytes > 0 ? kv_bytes : 1);
+    if (group < 1) group = 1;
+    if (group > B * H) group = B * H;
+  }
+  p.group_heads = static_cast<int32_t>(group);
+  p.layout = static_cast<int32_t>(layout);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.descale_q = descale_q;
+  p.descale_k = descale_k;
+  p.descale_v = descale_v;
+  p.o = o;
+  p.lse = lse;
+  p.err = dev.err_word;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+
+  const int grid = static_cast<int>(p.num_units < dev.sm_count ? p.num_units : dev.sm_count);
+  cudaError_t e;
+  if (dtype == FA_DTYPE_F16)
+    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtF16>(mq, mk, mv, p, grid, stream)
+                  : fa::launch_fa_fwd<128, fa::kDtF16>(mq, mk, mv, p, grid, stream);
+  else if (dtype == FA_DTYPE_BF16)
+    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtBF16>(mq, mk, mv, p, grid, stream)
+                  : fa::launch_fa_fwd<128, fa::kDtBF16>(mq, mk, mv, p, grid, stream);
+  else
+    e = fa::launch_fa_fwd<128, fa::kDtE4M3>(mq, mk, mv, p, grid, stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t fa_last_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceInfo dev;
+  if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
+  uint32_t word = 0, zero = 0;
+  if (cudaMemcpy(&word, dev.err_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (cudaMemcpy(dev.err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (word & fa::kErrTimeout) return FA_ERR_DEVICE_TIMEOUT;
+  return word ? FA_ERR_CUDA : FA_OK;
+}
+
+fa_status_t fa_probe_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+  DeviceInfo dev;
+  if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
+  fa_wait_probe_kernel<<<1, 32, 0, stream>>>(dev.err_word, limit_ns ? limit_ns : 1000000ull);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  return fa_last_device_error(stream);
+}
+
+}  // extern "C"

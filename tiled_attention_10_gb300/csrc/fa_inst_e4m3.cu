@@ -1,0 +1,9 @@
+// Kernel instantiations for e4m3 inputs (one translation unit per element
+// type so the library builds in parallel).
+#include "fa_kernel.cuh"
+
+namespace fa {
+template cudaError_t launch_fa_fwd<128, kDtE4M3>(const CUtensorMap&, const CUtensorMap&,
+                                                const CUtensorMap&, const KernelParams&, int,
+                                                cudaStream_t);
+}  // namespace fa

@@ -1,0 +1,588 @@
+/*
+ * fa_kernel.cuh -- FlashAttention forward kernel for sm_103a.
+ *
+ * One persistent CTA per SM walks a static list of work units.  A unit is
+ * (batch*head, pair of 128-row query tiles): the two query tiles share every
+ * K/V tile that is streamed in, and their softmax work alternates with each
+ * other's matrix products on the tensor cores (the MatMul_n || Softmax_(n-1)
+ * overlap that "How the CANN runtime splits FlashAttention" describes in its
+ * scheduling layer, and the FA3 ping-pong of "ops-transformer FlashAttention
+ * build and tuning", section 1.2).
+ *
+ * Warp roles (12 warps = 3 warpgroups, 384 threads):
+ *   warps 0-3  softmax for query tile 0 (one query row per thread, TMEM lanes)
+ *   warps 4-7  softmax for query tile 1
+ *   warp  8    TMA producer: Q tiles, then K_j, V_j through an NS-slot ring
+ *   warp  9    TMEM owner and tcgen05.mma issuer (one thread)
+ *   warps 10-11 idle
+ * The launch gives every thread 168 registers (three warps share each SM
+ * sub-partition's register file); the control warpgroup then hands registers
+ * to the softmax warpgroups with setmaxnreg (56 / 224), so that a softmax
+ * thread can hold its whole 128-column score row in registers.
+ *
+ * Tensor memory (512 columns x 128 lanes, fp32):
+ *   [0,128)   S for tile 0   (P for tile 0 overwrites its first columns)
+ *   [128,256) S for tile 1
+ *   [256,384) O for tile 0   [384,512) O for tile 1
+ *
+ * Per K/V block j and tile t:
+ *   S_t = Q_t K_j^T                     (tcgen05.mma, operands from smem)
+ *   softmax warps: mask, running max, conditional O rescale, P = 2^(s*c - m),
+ *                  row sum, P -> TMEM as 16-bit (or e4m3 x 256)
+ *   O_t += P_t V_j                      (tcgen05.mma, A = P from TMEM)
+ * This is the FlashAttention-2 loop order of section 1.2 of the Ascend page
+ * (Q block outer, K/V inner) with the online normalisation of its section 6.2
+ * written in base 2.  The running max is only moved when the block max
+ * exceeds it by more than 2^8 (16-bit P) -- P then stays <= 256, which the
+ * 16-bit types and the fp32 accumulators hold exactly as well as <= 1, and
+ * O/l is unchanged because O and l share the same stale max.
+ *
+ * Tail and NaN safety (the Hygon retrospective, defects 2 and 3): TMA never
+ * reads outside [0, S) of a tensor -- rows past the end are zero-filled by the
+ * tensor map bounds -- and masked columns get P = 0 exactly, so stray NaNs
+ * in memory past the valid rows cannot reach the accumulators.
+ * 64-bit offsets everywhere a row index meets a stride (defect 1).  Masking
+ * uses explicit selects, and the library is built without fast-math
+ * (defect 8).  P and O are rounded to nearest-even (defect 9).
+ */
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+#include <cstdint>
+
+#include "fa_ptx.cuh"
+#include "fa_tmem_io.cuh"
+
+namespace fa {
+
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // key/value rows per tile
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsSoftmax = 224;  // 256 * 224 + 128 * 56 = 384 * 168
+constexpr uint32_t kRegsControl = 56;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kDtF16 = 0, kDtBF16 = 1, kDtE4M3 = 2;
+
+struct KernelParams {
+  int64_t B, H, S_q, S_kv;
+  int32_t n_kv_blocks;  // ceil(S_kv / 128)
+  int32_t n_pairs;      // ceil(ceil(S_q / 128) / 2)
+  int32_t num_units;    // B * H * n_pairs
+  int32_t group_heads;  // heads per scheduling group (1 = head-major order)
+  int32_t layout;       // 0 BNSD, 1 BSND
+  int32_t causal;
+  float scale_log2;     // scale * log2(e)
+  const float* descale_q;
+  const float* descale_k;
+  const float* descale_v;
+  void* o;
+  float* lse;
+  uint32_t* err;
+  uint64_t wait_limit_ns;
+};
+
+template <int D, int DT>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr bool kFp8 = (DT == kDtE4M3);
+  static constexpr int kElem = kFp8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElem;
+  static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte swizzle chunks");
+  static constexpr int kChunks = kRowBytes / 128;    // 128-byte column chunks per row
+  static constexpr int kBoxElems = 128 / kElem;       // elements in one TMA box row
+  static constexpr int kChunkBytes = 128 * 128;       // one box: 128 rows x 128 bytes
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kUK = kFp8 ? 32 : 16;          // K of one UMMA instruction
+  static constexpr int kQKSteps = D / kUK;
+  static constexpr int kPVSteps = kBN / kUK;
+  static constexpr int kSlots = (kTileBytes >= 32768) ? 5 : 8;
+  static constexpr int kQBytes = 2 * kTileBytes;
+  static constexpr int kBarOffset = kQBytes + kSlots * kTileBytes;
+  static constexpr int kNumBars = 2 * kSlots + 9;
+  static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;  // + align slack
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static constexpr uint32_t kFmt = kFp8 ? 0u : (DT == kDtBF16 ? 1u : 0u);
+  static constexpr uint32_t kIdescQK = umma_idesc(kFmt, false, kBM, kBN);
+  static constexpr uint32_t kIdescPV = umma_idesc(kFmt, true, kBM, D);
+  static constexpr float kRescaleThreshold = kFp8 ? 0.0f : 8.0f;
+  static constexpr uint32_t kTmemS = 0, kTmemO = 256;
+};
+
+// ---------------------------------------------------------------------------
+// Static schedule.  Units are grouped by `group_heads` heads; inside a group
+// the longest query-tile pairs come first when causal (LPT order) and heads
+// vary fastest, so CTAs running at the same time share K/V in L2.  CTA `bid`
+// takes unit w*grid + bid in even rounds and w*grid + grid-1-bid in odd
+// rounds (a snake that evens out the causal lengths).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int unit_of_round(int w, int grid, int bid) {
+  return w * grid + ((w & 1) ? (grid - 1 - bid) : bid);
+}
+
+__device__ __forceinline__ void decode_unit(const KernelParams& p, int u, int& bh, int& pair) {
+  const int per_group = p.group_heads * p.n_pairs;
+  const int g = u / per_group;
+  const int r = u - g * per_group;
+  const int BH = static_cast<int>(p.B * p.H);
+  const int heads = min(p.group_heads, BH - g * p.group_heads);
+  const int rank = r / heads;
+  bh = g * p.group_heads + (r - rank * heads);
+  pair = p.causal ? (p.n_pairs - 1 - rank) : rank;
+}
+
+// K/V blocks query tile `q_tile` needs (0 if the tile has no valid row).
+__device__ __forceinline__ int tile_kv_blocks(const KernelParams& p, int q_tile) {
+  const int64_t row0 = static_cast<int64_t>(q_tile) * kBM;
+  if (row0 >= p.S_q) return 0;
+  if (!p.causal) return p.n_kv_blocks;
+  const int64_t last_row = min(row0 + (kBM - 1), p.S_q - 1);
+  const int64_t max_col = min(last_row, p.S_kv - 1);
+  return static_cast<int>(max_col / kBN) + 1;
+}
+
+// TMA coordinates of (column c0, row s) of head (b, h): BNSD maps are
+// {D, S, H, B}, BSND maps are {D, H, S, B}.
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                         int layout, int32_t c0, int32_t s, int32_t h, int32_t b) {
+  if (layout == 0)
+    tma_load_4d(dst, map, bar, c0, s, h, b);
+  else
+    tma_load_4d(dst, map, bar, c0, h, s, b);
+}
+
+struct Bars {
+  uint32_t base;
+  int ns;
+  __device__ uint32_t full(int s) const { return base + 8u * s; }
+  __device__ uint32_t empty(int s) const { return base + 8u * (ns + s); }
+  __device__ uint32_t q_full() const { return base + 8u * (2 * ns); }
+  __device__ uint32_t q_empty() const { return base + 8u * (2 * ns + 1); }
+  __device__ uint32_t s_full(int t) const { return base + 8u * (2 * ns + 2 + t); }
+  __device__ uint32_t p_ready(int t) const { return base + 8u * (2 * ns + 4 + t); }
+  __device__ uint32_t o_done(int t) const { return base + 8u * (2 * ns + 6 + t); }
+  __device__ uint32_t drain() const { return base + 8u * (2 * ns + 8); }
+};
+
+// Short bounded wait used only while tearing down after an abort: it ignores
+// the abort flag and reports nothing.
+__device__ __forceinline__ void mbar_wait_teardown(uint32_t bar, uint32_t parity, uint64_t limit) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit) return;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Producer (one thread): Q pair, then K_0, V_0, K_1, V_1, ... into the ring.
+// ---------------------------------------------------------------------------
+template <int D, int DT>
+__device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
+                              const CUtensorMap* tmK, const CUtensorMap* tmV, uint32_t sQ,
+                              uint32_t sRing, const Bars& bars, const WaitCtl& wc) {
+  using C = Cfg<D, DT>;
+  uint32_t ring = 0, it = 0;
+  bool ok = true;
+  const int grid = gridDim.x, bid = blockIdx.x;
+  for (int w = 0; ok; ++w) {
+    const int u = unit_of_round(w, grid, bid);
+    if (u >= p.num_units) break;
+    int bh, pair;
+    decode_unit(p, u, bh, pair);
+    const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
+    const int n0 = tile_kv_blocks(p, 2 * pair), n1 = tile_kv_blocks(p, 2 * pair + 1);
+    const int nmax = max(n0, n1);
+    if (!mbar_wait(bars.q_empty(), (it & 1u) ^ 1u, wc)) { ok = false; break; }
+    mbar_arrive_expect_tx(bars.q_full(), (n0 > 0 ? C::kTileBytes : 0) + (n1 > 0 ? C::kTileBytes : 0));
+    for (int t = 0; t < 2; ++t) {
+      if ((t == 0 ? n0 : n1) == 0) continue;
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_tile(sQ + t * C::kTileBytes + c * C::kChunkBytes, tmQ, bars.q_full(), p.layout,
+                 c * C::kBoxElems, (2 * pair + t) * kBM, h, b);
+    }
+    ++it;
+    for (int j = 0; j < nmax && ok; ++j) {
+      for (int kv = 0; kv < 2; ++kv) {
+        const int slot = static_cast<int>(ring % C::kSlots);
+        if (!mbar_wait(bars.empty(slot), ((ring / C::kSlots) & 1u) ^ 1u, wc)) { ok = false; break; }
+        mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
+        const CUtensorMap* map = kv == 0 ? tmK : tmV;
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_tile(sRing + slot * C::kTileBytes + c * C::kChunkBytes, map, bars.full(slot),
+                   p.layout, c * C::kBoxElems, j * kBN, h, b);
+        ++ring;
+      }
+    }
+  }
+  if (!ok) {
+    // Let loads already in flight land before the CTA's shared memory goes away.
+    const uint32_t first = ring > static_cast<uint32_t>(C::kSlots) ? ring - C::kSlots : 0u;
+    for (uint32_t r = first; r < ring; ++r)
+      mbar_wait_teardown(bars.full(r % C::kSlots), (r / C::kSlots) & 1u, 20000000ull);
+    if (it > 0) mbar_wait_teardown(bars.q_full(), (it - 1) & 1u, 20000000ull);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one thread).
+// ---------------------------------------------------------------------------
+template <int D, int DT>
+__device__ __forceinline__ void issue_qk(uint32_t tmem, int t, uint32_t sQ, uint32_t sK) {
+  using C = Cfg<D, DT>;
+  const uint32_t a0 = sQ + t * C::kTileBytes;
+#pragma unroll 1
+  for (int kk = 0; kk < C::kQKSteps; ++kk) {
+    const uint32_t off = (kk * 32 / 128) * C::kChunkBytes + (kk * 32) % 128;  // 32 bytes of K per step
+    umma_ss<C::kFp8>(tmem + C::kTmemS + t * kBN, umma_desc_sw128(a0 + off, 16, 1024),
+                     umma_desc_sw128(sK + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D, int DT>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, int t, uint32_t sV, bool accumulate) {
+  using C = Cfg<D, DT>;
+#pragma unroll 1
+  for (int kk = 0; kk < C::kPVSteps; ++kk) {
+    // A = P_t from TMEM: kUK elements of K per step = 8 columns of 32 bits.
+    // B = V rows [kk*kUK, +kUK), MN-major: 128-byte rows, LBO = next column chunk.
+    umma_ts<C::kFp8>(tmem + C::kTmemO + t * 128, tmem + C::kTmemS + t * kBN + kk * 8,
+                     umma_desc_sw128(sV + kk * C::kUK * 128, C::kChunkBytes, 1024), C::kIdescPV,
+                     (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D, int DT>
+__device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint32_t sRing,
+                         const Bars& bars, const WaitCtl& wc) {
+  using C = Cfg<D, DT>;
+  uint32_t ring = 0, it = 0;
+  uint32_t p_phase[2] = {0u, 0u};
+  bool ok = true;
+  const int grid = gridDim.x, bid = blockIdx.x;
+  for (int w = 0; ok; ++w) {
+    const int u = unit_of_round(w, grid, bid);
+    if (u >= p.num_units) break;
+    int bh, pair;
+    decode_unit(p, u, bh, pair);
+    const int n[2] = {tile_kv_blocks(p, 2 * pair), tile_kv_blocks(p, 2 * pair + 1)};
+    const int nmax = max(n[0], n[1]);
+    if (!mbar_wait(bars.q_full(), it & 1u, wc)) { ok = false; break; }
+    ++it;
+    // Prologue: S_t = Q_t K_0^T for both tiles.
+    int slotK = static_cast<int>(ring % C::kSlots);
+    if (!mbar_wait(bars.full(slotK), (ring / C::kSlots) & 1u, wc)) { ok = false; break; }
+    ++ring;
+    tc_fence_after();
+    for (int t = 0; t < 2; ++t) {
+      if (n[t] == 0) continue;
+      issue_qk<D, DT>(tmem, t, sQ, sRing + slotK * C::kTileBytes);
+      umma_commit(bars.s_full(t));
+    }
+    umma_commit(bars.empty(slotK));
+    if (nmax == 1) umma_commit(bars.q_empty());
+    for (int j = 0; j < nmax; ++j) {
+      const int slotV = static_cast<int>(ring % C::kSlots);
+      if (!mbar_wait(bars.full(slotV), (ring / C::kSlots) & 1u, wc)) { ok = false; break; }
+      ++ring;
+      const bool has_next = j + 1 < nmax;
+      if (has_next) {
+        slotK = static_cast<int>(ring % C::kSlots);
+        if (!mbar_wait(bars.full(slotK), (ring / C::kSlots) & 1u, wc)) { ok = false; break; }
+        ++ring;
+      }
+      tc_fence_after();
+      for (int t = 0; t < 2; ++t) {
+        if (j >= n[t]) continue;
+        if (!mbar_wait(bars.p_ready(t), p_phase[t], wc)) { ok = false; break; }
+        p_phase[t] ^= 1u;
+        tc_fence_after();
+        issue_pv<D, DT>(tmem, t, sRing + slotV * C::kTileBytes, j > 0);
+        if (j + 1 < n[t]) {
+          issue_qk<D, DT>(tmem, t, sQ, sRing + slotK * C::kTileBytes);
+          umma_commit(bars.s_full(t));
+        } else {
+          umma_commit(bars.o_done(t));
+        }
+      }
+      if (!ok) break;
+      umma_commit(bars.empty(slotV));
+      if (has_next) {
+        umma_commit(bars.empty(slotK));
+        if (j + 2 == nmax) umma_commit(bars.q_empty());
+      }
+    }
+  }
+  // Drain: every MMA issued above completes before TMEM is released.
+  umma_commit(bars.drain());
+  mbar_wait_teardown(bars.drain(), 0u, ok ? 2000000000ull : 20000000ull);
+}
+
+// ---------------------------------------------------------------------------
+// Softmax / correction / epilogue (warps 0-7; one query row per thread).
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ void store_out_chunk(void* dst, const float (&x)[32], bool row_ok) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    w[i] = (DT == kDtF16) ? pack_f16x2(x[2 * i], x[2 * i + 1]) : pack_bf16x2(x[2 * i], x[2 * i + 1]);
+  if (row_ok) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
+}
+
+template <int D, int DT>
+__device__ void softmax_role(const KernelParams& p, uint32_t tmem, int warp, int lane,
+                             const Bars& bars, const WaitCtl& wc) {
+  using C = Cfg<D, DT>;
+  const int t = warp >> 2;            // query tile of this warpgroup
+  const int wq = warp & 3;            // TMEM lane quarter
+  const int r = wq * 32 + lane;       // row inside the tile
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_off + C::kTmemS + t * kBN;
+  const uint32_t tO = tmem + lane_off + C::kTmemO + t * 128;
+
+  float sl2 = p.scale_log2;
+  float o_mul = 1.0f;
+  if constexpr (C::kFp8) {
+    const float dq = p.descale_q ? *p.descale_q : 1.0f;
+    const float dk = p.descale_k ? *p.descale_k : 1.0f;
+    const float dv = p.descale_v ? *p.descale_v : 1.0f;
+    sl2 *= dq * dk;
+    o_mul = dv * (1.0f / 256.0f);  // P is stored as 256 * p in e4m3
+  }
+
+  uint32_t s_phase = 0u, o_phase = 0u;
+  const int grid = gridDim.x, bid = blockIdx.x;
+  for (int w = 0;; ++w) {
+    const int u = unit_of_round(w, grid, bid);
+    if (u >= p.num_units) break;
+    int bh, pair;
+    decode_unit(p, u, bh, pair);
+    const int q_tile = 2 * pair + t;
+    const int n = tile_kv_blocks(p, q_tile);
+    if (n == 0) continue;
+    const int64_t row = static_cast<int64_t>(q_tile) * kBM + r;
+    const int64_t col_end = p.causal ? min(row + 1, p.S_kv) : p.S_kv;  // columns < col_end visible
+    const int64_t tile_row0 = static_cast<int64_t>(q_tile) * kBM;
+
+    float m_run = -CUDART_INF_F, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait(bars.s_full(t), s_phase, wc)) { ok = false; break; }
+      s_phase ^= 1u;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_x32(tS + 32 * c, sr[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_dep_x32(sr[c]);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+      const int64_t col0 = static_cast<int64_t>(j) * kBN;
+      // Block-uniform: does any column of this block need a mask?
+      const bool masked = (col0 + kBN > p.S_kv) || (p.causal && col0 + (kBN - 1) > tile_row0);
+      const int lim = static_cast<int>(max(min(col_end - col0, static_cast<int64_t>(kBN)), int64_t(0)));
+
+      float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], c < lim ? s[c] : -CUDART_INF_F);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+      }
+      const float mxb = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float m_blk = (mxb == -CUDART_INF_F) ? -CUDART_INF_F : mxb * sl2;
+      const float m_new = fmaxf(m_run, m_blk);
+      // Decide the running max for this block.  On the first block O holds
+      // nothing yet (its first PV overwrites it); later the max only moves
+      // when it grew past the threshold, and then O and l are rescaled.
+      float alpha = 1.0f;
+      bool resc = false;
+      if (j == 0) {
+        m_run = m_new;
+      } else if (m_new > m_run + C::kRescaleThreshold) {
+        resc = true;
+        alpha = ex2(m_run - m_new);
+        l *= alpha;
+        m_run = m_new;
+      }
+      const float m_sub = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
+      const float neg_m = -m_sub;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          s[c] = (c < lim) ? ex2(fmaf(s[c], sl2, neg_m)) : 0.0f;
+          ps[c & 3] += s[c];
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          s[c] = ex2(fmaf(s[c], sl2, neg_m));
+          ps[c & 3] += s[c];
+        }
+      }
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+
+      if constexpr (C::kFp8) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          pk[i] = pack_e4m3x4(s[4 * i] * 256.f, s[4 * i + 1] * 256.f, s[4 * i + 2] * 256.f,
+                              s[4 * i + 3] * 256.f);
+        tmem_st_x32(tS, pk);
+      } else {
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          pk[i >> 5][i & 31] = (DT == kDtF16) ? pack_f16x2(s[2 * i], s[2 * i + 1])
+                                              : pack_bf16x2(s[2 * i], s[2 * i + 1]);
+        tmem_st_x32(tS, pk[0]);
+        tmem_st_x32(tS + 32, pk[1]);
+      }
+      // O_t *= alpha for the rows whose max moved (O is complete: the commit
+      // that signalled S_j covered the previous PV; the next PV waits for us).
+      if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld_x32(tO + 32 * c, ov);
+          tmem_wait_ld();
+          reg_dep_x32(ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st_x32(tO + 32 * c, ov);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bars.p_ready(t));
+    }
+    if (!ok) break;
+
+    // Epilogue: O / l -> output dtype, and lse, for rows < S_q.
+    if (!mbar_wait(bars.o_done(t), o_phase, wc)) break;
+    o_phase ^= 1u;
+    tc_fence_after();
+    const float inv = o_mul / l;
+    const bool row_ok = row < p.S_q;
+    const int64_t b = bh / p.H, h = bh % p.H;
+    const int64_t orow = (p.layout == 0) ? ((b * p.H + h) * p.S_q + row) : ((b * p.S_q + row) * p.H + h);
+    uint16_t* out = reinterpret_cast<uint16_t*>(p.o) + (row_ok ? orow * D : 0);
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t ov[32];
+      tmem_ld_x32(tO + 32 * c, ov);
+      tmem_wait_ld();
+      reg_dep_x32(ov);
+      float x[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(ov[i]) * inv;
+      store_out_chunk<DT>(out + 32 * c, x, row_ok);
+    }
+    if (row_ok) {
+      const float lse2 = m_run + log2f(l);
+      p.lse[static_cast<int64_t>(bh) * p.S_q + row] = lse2 * 0.69314718055994531f;
+    }
+    tc_fence_before();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// ---------------------------------------------------------------------------
+template <int D, int DT>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ KernelParams p) {
+  using C = Cfg<D, DT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sQ = base;
+  const uint32_t sRing = base + C::kQBytes;
+  const Bars bars{base + static_cast<uint32_t>(C::kBarOffset), C::kSlots};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOffset + C::kNumBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), 1);
+    }
+    mbar_init(bars.q_full(), 1);
+    mbar_init(bars.q_empty(), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars.s_full(t), 1);
+      mbar_init(bars.p_ready(t), 128);
+      mbar_init(bars.o_done(t), 1);
+    }
+    mbar_init(bars.drain(), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{p.wait_limit_ns, p.err, abort_flag};
+
+  if (warp < kProducerWarp) {
+    reg_alloc_inc<kRegsSoftmax>();
+    softmax_role<D, DT>(p, tmem, warp, lane, bars, wc);
+  } else {
+    reg_alloc_dec<kRegsControl>();
+    if (warp == kProducerWarp) {
+      if (lane == 0) producer_role<D, DT>(p, &tmQ, &tmK, &tmV, sQ, sRing, bars, wc);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) mma_role<D, DT>(p, tmem, sQ, sRing, bars, wc);
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Host-side launcher, one instantiation per (D, dtype).
+template <int D, int DT>
+cudaError_t launch_fa_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                          const KernelParams& p, int grid, cudaStream_t stream) {
+  using C = Cfg<D, DT>;
+  auto kern = fa_fwd_kernel<D, DT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, p);
+}
+
+}  // namespace fa
