@@ -229,8 +229,8 @@ int fa_oracle_rows(const void* q, const void* k, const void* v, int dtype, int l
 }
 
 /* Every row of every head.  O is [B, H, S_q, D] (BNSD, whatever the input
- * layout), lse is [B, H, S_q].  Heads run in parallel; each decodes its K
- * and V once. */
+ * layout), lse is [B, H, S_q].  Heads are taken one after another; inside a
+ * head the K/V decode and then the query rows run in parallel. */
 int fa_oracle_full(const void* q, const void* k, const void* v, int dtype, int layout,
                    int64_t B, int64_t H, int64_t S_q, int64_t S_kv, int64_t D,
                    double scale, int causal, double dq, double dk, double dv,
@@ -239,40 +239,47 @@ int fa_oracle_full(const void* q, const void* k, const void* v, int dtype, int l
   int rc = check_problem(&p);
   if (rc) return rc;
   if (!O || !lse) return 5;
+  double* kd = (double*)malloc(sizeof(double) * (size_t)(S_kv * D));
+  double* vd = (double*)malloc(sizeof(double) * (size_t)(S_kv * D));
+  if (!kd || !vd) { free(kd); free(vd); return 7; }
   int bad = 0;
 #ifdef _OPENMP
   if (n_threads > 0) omp_set_num_threads(n_threads);
+#endif
+  for (int64_t bh = 0; bh < B * H && !bad; ++bh) {
+    const int64_t b = bh / H, h = bh % H;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t j = 0; j < S_kv; ++j) {
+      load_row(&p, k, S_kv, dk, b, h, j, kd + j * D);
+      load_row(&p, v, S_kv, dv, b, h, j, vd + j * D);
+    }
+#ifdef _OPENMP
 #pragma omp parallel
 #endif
-  {
-    double* kd = (double*)malloc(sizeof(double) * (size_t)(S_kv * D));
-    double* vd = (double*)malloc(sizeof(double) * (size_t)(S_kv * D));
-    double* qrow = (double*)malloc(sizeof(double) * (size_t)D);
-    double* Srow = (double*)malloc(sizeof(double) * (size_t)S_kv);
-    double* Prow = (double*)malloc(sizeof(double) * (size_t)S_kv);
-    if (!kd || !vd || !qrow || !Srow || !Prow) {
+    {
+      double* qrow = (double*)malloc(sizeof(double) * (size_t)D);
+      double* Srow = (double*)malloc(sizeof(double) * (size_t)S_kv);
+      double* Prow = (double*)malloc(sizeof(double) * (size_t)S_kv);
+      if (!qrow || !Srow || !Prow) {
 #ifdef _OPENMP
 #pragma omp atomic write
 #endif
-      bad = 1;
-    } else {
+        bad = 1;
+      } else {
 #ifdef _OPENMP
-#pragma omp for schedule(dynamic, 1)
+#pragma omp for schedule(dynamic, 4)
 #endif
-      for (int64_t bh = 0; bh < B * H; ++bh) {
-        int64_t b = bh / H, h = bh % H;
-        for (int64_t j = 0; j < S_kv; ++j) {
-          load_row(&p, k, S_kv, dk, b, h, j, kd + j * D);
-          load_row(&p, v, S_kv, dv, b, h, j, vd + j * D);
-        }
         for (int64_t i = 0; i < S_q; ++i) {
           load_row(&p, q, S_q, dq, b, h, i, qrow);
           attend_row(&p, qrow, kd, vd, i, Srow, Prow, O + (bh * S_q + i) * D, lse + bh * S_q + i);
         }
       }
+      free(qrow); free(Srow); free(Prow);
     }
-    free(kd); free(vd); free(qrow); free(Srow); free(Prow);
   }
+  free(kd); free(vd);
   return bad ? 7 : 0;
 }
 

@@ -1,0 +1,80 @@
+"""Runtime behaviour on the GPU: determinism, streams, the bounded-wait
+timeout path, and that a call with bad arguments launches nothing."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tiled_attention_10_gb300 import binding
+from tiled_attention_10_gb300.inputs import Workload, make_inputs
+from tests.gpu_helpers import Run, check, compare_full, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bitwise_deterministic(cuda_lib):
+    """Static schedule, no atomics: two calls give identical bits."""
+    w = Workload("t", 2, 8, 1000, 1000, 128, "bf16", "BNSD", True, seed=21)
+    x = make_inputs(w, device="cuda")
+    a = Run(w, x.q, x.k, x.v)
+    b = Run(w, x.q, x.k, x.v)
+    torch.cuda.synchronize()
+    assert a.status == 0 and b.status == 0
+    assert torch.equal(a.o.view(torch.int16), b.o.view(torch.int16))
+    assert torch.equal(a.lse.view(torch.int32), b.lse.view(torch.int32))
+
+
+def test_side_stream(cuda_lib):
+    w = Workload("t", 1, 4, 300, 300, 64, "f16", "BSND", False, seed=22)
+    x = make_inputs(w)
+    q, k, v = to_device(x)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        r = Run(w, q, k, v, stream=s.cuda_stream)
+    s.synchronize()
+    eo, el, og, lg = compare_full(w, r, x)
+    check(w, r, eo, el, og, lg)
+
+
+def test_wait_timeout_reports_and_context_survives(cuda_lib):
+    """A wait on a barrier nothing arrives at must expire after its limit,
+    report FA_ERR_DEVICE_TIMEOUT, and leave the context usable."""
+    st = binding.fa_probe_wait_timeout(2_000_000)   # 2 ms limit
+    assert st == 5, binding.FA_STATUS.get(st)
+    assert binding.fa_last_device_error() == 0       # the word was cleared
+    w = Workload("t", 1, 2, 256, 256, 128, "bf16", "BNSD", True, seed=23)
+    x = make_inputs(w)
+    q, k, v = to_device(x)
+    r = Run(w, q, k, v)
+    torch.cuda.synchronize()
+    eo, el, og, lg = compare_full(w, r, x)
+    check(w, r, eo, el, og, lg)
+
+
+def test_bad_arguments_launch_nothing(cuda_lib):
+    w = Workload("t", 1, 1, 128, 128, 128, "bf16", "BNSD", False, seed=24)
+    x = make_inputs(w, device="cuda")
+    o = torch.full_like(x.q, 7.0)
+    lse = torch.full((1, 1, 128), 7.0, device="cuda")
+    st = binding.fa_fwd(x.q.data_ptr(), x.k.data_ptr(), x.v.data_ptr(), o.data_ptr(),
+                        lse.data_ptr(), 1, 1, 128, 128, 96, 0.1, "BNSD", 0, "bf16")
+    assert st == 2
+    st = binding.fa_fwd(x.q.data_ptr() + 2, x.k.data_ptr(), x.v.data_ptr(), o.data_ptr(),
+                        lse.data_ptr(), 1, 1, 128, 128, 128, 0.1, "BNSD", 0, "bf16")
+    assert st == 3
+    torch.cuda.synchronize()
+    assert bool((o == 7.0).all()) and bool((lse == 7.0).all())
+
+
+def test_torch_tensor_wrapper(cuda_lib):
+    w = Workload("t", 2, 2, 200, 300, 128, "bf16", "BSND", True, seed=25)
+    x = make_inputs(w)
+    q, k, v = to_device(x)
+    out, lse = binding.attention(q, k, v, causal=True, layout="BSND")
+    torch.cuda.synchronize()
+    O, L = oracle.attention_full(x.q, x.k, x.v, dtype="bf16", layout="BSND", B=2, H=2, S_q=200,
+                                 S_kv=300, D=128, scale=w.softmax_scale, causal=True)
+    og = out.float().cpu().double().permute(0, 2, 1, 3).numpy()
+    assert np.abs(og - O).max() <= 1.6e-2
+    assert np.abs(lse.cpu().double().numpy() - L).max() <= 1e-3
