@@ -17,7 +17,7 @@
  *   warps 10-11 idle
  * The launch gives every thread 168 registers (three warps share each SM
  * sub-partition's register file); the control warpgroup then hands registers
- * to the softmax warpgroups with setmaxnreg (56 / 224), so that a softmax
+ * to the softmax warpgroups with setmaxnreg (72 / 216), so that a softmax
  * thread can hold its whole 128-column score row in registers.
  *
  * Tensor memory (512 columns x 128 lanes, fp32):
@@ -61,8 +61,8 @@ namespace fa {
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // key/value rows per tile
 constexpr int kThreads = 384;
-constexpr uint32_t kRegsSoftmax = 224;  // 256 * 224 + 128 * 56 = 384 * 168
-constexpr uint32_t kRegsControl = 56;
+constexpr uint32_t kRegsSoftmax = 216;  // 256 * 216 + 128 * 72 = 384 * 168
+constexpr uint32_t kRegsControl = 72;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -230,36 +230,62 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
 // ---------------------------------------------------------------------------
 // MMA issuer (one thread).
 // ---------------------------------------------------------------------------
+// S_t = Q_t K^T: K = D in kQKSteps instructions, 32 bytes of K each (inside
+// a 128-byte swizzle chunk, then the next 16 KB chunk).  qlo / klo are the low
+// descriptor words of the Q tile and the K slot.
 template <int D, int DT>
-__device__ __forceinline__ void issue_qk(uint32_t tmem, int t, uint32_t sQ, uint32_t sK) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t qlo, uint32_t klo) {
   using C = Cfg<D, DT>;
-  const uint32_t a0 = sQ + t * C::kTileBytes;
-#pragma unroll 1
+  constexpr uint32_t hi = umma_desc_hi_sw128(1024);
+#pragma unroll
   for (int kk = 0; kk < C::kQKSteps; ++kk) {
-    const uint32_t off = (kk * 32 / 128) * C::kChunkBytes + (kk * 32) % 128;  // 32 bytes of K per step
-    umma_ss<C::kFp8>(tmem + C::kTmemS + t * kBN, umma_desc_sw128(a0 + off, 16, 1024),
-                     umma_desc_sw128(sK + off, 16, 1024), C::kIdescQK, kk > 0 ? 1u : 0u);
+    constexpr int kStepBytes = 32;
+    const uint32_t off = static_cast<uint32_t>(((kk * kStepBytes / 128) * C::kChunkBytes +
+                                                (kk * kStepBytes) % 128) >> 4);
+    umma_ss_w<C::kFp8>(d_tmem, qlo + off, hi, klo + off, hi, C::kIdescQK, kk > 0 ? 1u : 0u);
   }
 }
 
+// O_t (+)= P_t V: A = P_t from TMEM (kUK elements of K = 8 columns per step),
+// B = V rows [kk*kUK, +kUK) MN-major (128-byte rows; LBO = next column chunk).
 template <int D, int DT>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, int t, uint32_t sV, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t vlo,
+                                         uint32_t accumulate) {
   using C = Cfg<D, DT>;
-#pragma unroll 1
+  constexpr uint32_t hi = umma_desc_hi_sw128(1024);
+#pragma unroll
   for (int kk = 0; kk < C::kPVSteps; ++kk) {
-    // A = P_t from TMEM: kUK elements of K per step = 8 columns of 32 bits.
-    // B = V rows [kk*kUK, +kUK), MN-major: 128-byte rows, LBO = next column chunk.
-    umma_ts<C::kFp8>(tmem + C::kTmemO + t * 128, tmem + C::kTmemS + t * kBN + kk * 8,
-                     umma_desc_sw128(sV + kk * C::kUK * 128, C::kChunkBytes, 1024), C::kIdescPV,
-                     (accumulate || kk > 0) ? 1u : 0u);
+    const uint32_t off = static_cast<uint32_t>((kk * C::kUK * 128) >> 4);
+    umma_ts_w<C::kFp8>(o_tmem, p_tmem + kk * 8, vlo + off, hi, C::kIdescPV,
+                       kk > 0 ? 1u : accumulate);
   }
 }
+
+// Ring position: slot index and the parity of its current use.
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  template <int NS>
+  __device__ __forceinline__ void advance() {
+    if (++slot == NS) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
 
 template <int D, int DT>
 __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint32_t sRing,
                          const Bars& bars, const WaitCtl& wc) {
   using C = Cfg<D, DT>;
-  uint32_t ring = 0, it = 0;
+  constexpr uint32_t kTileW = C::kTileBytes >> 4;  // one tile, in descriptor units
+  const uint32_t q_lo[2] = {umma_desc_lo(sQ, 16), umma_desc_lo(sQ, 16) + kTileW};
+  const uint32_t k_lo0 = umma_desc_lo(sRing, 16);               // K-major view of slot 0
+  const uint32_t v_lo0 = umma_desc_lo(sRing, C::kChunkBytes);   // MN-major view of slot 0
+  const uint32_t tS[2] = {tmem + C::kTmemS, tmem + C::kTmemS + kBN};
+  const uint32_t tO[2] = {tmem + C::kTmemO, tmem + C::kTmemO + 128};
+  RingPos rp;
+  uint32_t it = 0;
   uint32_t p_phase[2] = {0u, 0u};
   bool ok = true;
   const int grid = gridDim.x, bid = blockIdx.x;
@@ -273,36 +299,35 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
     if (!mbar_wait(bars.q_full(), it & 1u, wc)) { ok = false; break; }
     ++it;
     // Prologue: S_t = Q_t K_0^T for both tiles.
-    int slotK = static_cast<int>(ring % C::kSlots);
-    if (!mbar_wait(bars.full(slotK), (ring / C::kSlots) & 1u, wc)) { ok = false; break; }
-    ++ring;
+    int slotK = rp.slot;
+    if (!mbar_wait(bars.full(slotK), rp.phase, wc)) { ok = false; break; }
+    rp.advance<C::kSlots>();
     tc_fence_after();
     for (int t = 0; t < 2; ++t) {
       if (n[t] == 0) continue;
-      issue_qk<D, DT>(tmem, t, sQ, sRing + slotK * C::kTileBytes);
+      issue_qk<D, DT>(tS[t], q_lo[t], k_lo0 + slotK * kTileW);
       umma_commit(bars.s_full(t));
     }
     umma_commit(bars.empty(slotK));
     if (nmax == 1) umma_commit(bars.q_empty());
     for (int j = 0; j < nmax; ++j) {
-      const int slotV = static_cast<int>(ring % C::kSlots);
-      if (!mbar_wait(bars.full(slotV), (ring / C::kSlots) & 1u, wc)) { ok = false; break; }
-      ++ring;
+      const int slotV = rp.slot;
+      if (!mbar_wait(bars.full(slotV), rp.phase, wc)) { ok = false; break; }
+      rp.advance<C::kSlots>();
       const bool has_next = j + 1 < nmax;
       if (has_next) {
-        slotK = static_cast<int>(ring % C::kSlots);
-        if (!mbar_wait(bars.full(slotK), (ring / C::kSlots) & 1u, wc)) { ok = false; break; }
-        ++ring;
+        slotK = rp.slot;
+        if (!mbar_wait(bars.full(slotK), rp.phase, wc)) { ok = false; break; }
+        rp.advance<C::kSlots>();
       }
-      tc_fence_after();
       for (int t = 0; t < 2; ++t) {
         if (j >= n[t]) continue;
         if (!mbar_wait(bars.p_ready(t), p_phase[t], wc)) { ok = false; break; }
         p_phase[t] ^= 1u;
         tc_fence_after();
-        issue_pv<D, DT>(tmem, t, sRing + slotV * C::kTileBytes, j > 0);
+        issue_pv<D, DT>(tO[t], tS[t], v_lo0 + slotV * kTileW, j > 0 ? 1u : 0u);
         if (j + 1 < n[t]) {
-          issue_qk<D, DT>(tmem, t, sQ, sRing + slotK * C::kTileBytes);
+          issue_qk<D, DT>(tS[t], q_lo[t], k_lo0 + slotK * kTileW);
           umma_commit(bars.s_full(t));
         } else {
           umma_commit(bars.o_done(t));
@@ -393,15 +418,21 @@ __device__ void softmax_role(const KernelParams& p, uint32_t tmem, int warp, int
       const bool masked = (col0 + kBN > p.S_kv) || (p.causal && col0 + (kBN - 1) > tile_row0);
       const int lim = static_cast<int>(max(min(col_end - col0, static_cast<int64_t>(kBN)), int64_t(0)));
 
-      float mx[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+      // Row max of the block: masked columns become -inf first (block-uniform
+      // branch; only tail and diagonal blocks take it).
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], c < lim ? s[c] : -CUDART_INF_F);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+        for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -CUDART_INF_F;
       }
-      const float mxb = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < 128; c += 8) {
+        mx0 = max3(mx0, s[c], s[c + 1]);
+        mx1 = max3(mx1, s[c + 2], s[c + 3]);
+        mx2 = max3(mx2, s[c + 4], s[c + 5]);
+        mx3 = max3(mx3, s[c + 6], s[c + 7]);
+      }
+      const float mxb = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       const float m_blk = (mxb == -CUDART_INF_F) ? -CUDART_INF_F : mxb * sl2;
       const float m_new = fmaxf(m_run, m_blk);
       // Decide the running max for this block.  On the first block O holds
@@ -418,22 +449,32 @@ __device__ void softmax_role(const KernelParams& p, uint32_t tmem, int warp, int
         m_run = m_new;
       }
       const float m_sub = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
-      const float neg_m = -m_sub;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      if (masked) {
+      // p = 2^(s * sl2 - m): pairs through one packed FMA, then ex2 each; a
+      // masked column gets exactly 0 (a select, so no NaN can survive).
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_sub, -m_sub);
+      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          s[c] = (c < lim) ? ex2(fmaf(s[c], sl2, neg_m)) : 0.0f;
-          ps[c & 3] += s[c];
+      for (int i = 0; i < 64; ++i) {
+        float a, b;
+        f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negm2), a, b);
+        a = ex2(a);
+        b = ex2(b);
+        if (masked) {
+          a = (2 * i < lim) ? a : 0.0f;
+          b = (2 * i + 1 < lim) ? b : 0.0f;
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          s[c] = ex2(fmaf(s[c], sl2, neg_m));
-          ps[c & 3] += s[c];
-        }
+        s[2 * i] = a;
+        s[2 * i + 1] = b;
+        if (i & 1)
+          acc1 = f2_add(acc1, f2_pack(a, b));
+        else
+          acc0 = f2_add(acc0, f2_pack(a, b));
       }
-      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      {
+        float x0, x1;
+        f2_unpack(f2_add(acc0, acc1), x0, x1);
+        l += x0 + x1;
+      }
 
       if constexpr (C::kFp8) {
         uint32_t pk[32];
