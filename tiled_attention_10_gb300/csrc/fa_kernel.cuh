@@ -312,22 +312,34 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
     if (nmax == 1) umma_commit(bars.q_empty());
     for (int j = 0; j < nmax; ++j) {
       const int slotV = rp.slot;
-      if (!mbar_wait(bars.full(slotV), rp.phase, wc)) { ok = false; break; }
+      const uint32_t phV = rp.phase;
       rp.advance<C::kSlots>();
       const bool has_next = j + 1 < nmax;
+      int slotKn = slotK;
+      uint32_t phK = 0;
       if (has_next) {
-        slotK = rp.slot;
-        if (!mbar_wait(bars.full(slotK), rp.phase, wc)) { ok = false; break; }
+        slotKn = rp.slot;
+        phK = rp.phase;
         rp.advance<C::kSlots>();
       }
+      bool v_ready = false, k_ready = !has_next;
       for (int t = 0; t < 2; ++t) {
         if (j >= n[t]) continue;
         if (!mbar_wait(bars.p_ready(t), p_phase[t], wc)) { ok = false; break; }
         p_phase[t] ^= 1u;
+        if (!v_ready) {
+          if (!mbar_wait(bars.full(slotV), phV, wc)) { ok = false; break; }
+          v_ready = true;
+        }
         tc_fence_after();
         issue_pv<D, DT>(tO[t], tS[t], v_lo0 + slotV * kTileW, j > 0 ? 1u : 0u);
         if (j + 1 < n[t]) {
-          issue_qk<D, DT>(tS[t], q_lo[t], k_lo0 + slotK * kTileW);
+          if (!k_ready) {
+            if (!mbar_wait(bars.full(slotKn), phK, wc)) { ok = false; break; }
+            k_ready = true;
+            tc_fence_after();
+          }
+          issue_qk<D, DT>(tS[t], q_lo[t], k_lo0 + slotKn * kTileW);
           umma_commit(bars.s_full(t));
         } else {
           umma_commit(bars.o_done(t));
@@ -336,9 +348,14 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
       if (!ok) break;
       umma_commit(bars.empty(slotV));
       if (has_next) {
-        umma_commit(bars.empty(slotK));
+        // Every tile that uses K_{j+1} has issued its S by now (a tile with
+        // n_t = j + 1 never does), but K_{j+1} may still be unread if no tile
+        // needed it: wait for it before handing its slot back.
+        if (!k_ready && !mbar_wait(bars.full(slotKn), phK, wc)) { ok = false; break; }
+        umma_commit(bars.empty(slotKn));
         if (j + 2 == nmax) umma_commit(bars.q_empty());
       }
+      slotK = slotKn;
     }
   }
   // Drain: every MMA issued above completes before TMEM is released.
@@ -424,15 +441,19 @@ __device__ void softmax_role(const KernelParams& p, uint32_t tmem, int warp, int
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -CUDART_INF_F;
       }
-      float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F, mx2 = -CUDART_INF_F, mx3 = -CUDART_INF_F;
+      // 3-input max tree over the 128 scores (depth 5, ~64 instructions).
+      float t43[43];
 #pragma unroll
-      for (int c = 0; c < 128; c += 8) {
-        mx0 = max3(mx0, s[c], s[c + 1]);
-        mx1 = max3(mx1, s[c + 2], s[c + 3]);
-        mx2 = max3(mx2, s[c + 4], s[c + 5]);
-        mx3 = max3(mx3, s[c + 6], s[c + 7]);
-      }
-      const float mxb = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      for (int i = 0; i < 42; ++i) t43[i] = max3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+      t43[42] = fmaxf(s[126], s[127]);
+      float t15[15];
+#pragma unroll
+      for (int i = 0; i < 14; ++i) t15[i] = max3(t43[3 * i], t43[3 * i + 1], t43[3 * i + 2]);
+      t15[14] = t43[42];
+      const float t5a = max3(t15[0], t15[1], t15[2]), t5b = max3(t15[3], t15[4], t15[5]);
+      const float t5c = max3(t15[6], t15[7], t15[8]), t5d = max3(t15[9], t15[10], t15[11]);
+      const float t5e = max3(t15[12], t15[13], t15[14]);
+      const float mxb = max3(max3(t5a, t5b, t5c), t5d, t5e);
       const float m_blk = (mxb == -CUDART_INF_F) ? -CUDART_INF_F : mxb * sl2;
       const float m_new = fmaxf(m_run, m_blk);
       // Decide the running max for this block.  On the first block O holds
@@ -449,32 +470,34 @@ __device__ void softmax_role(const KernelParams& p, uint32_t tmem, int warp, int
         m_run = m_new;
       }
       const float m_sub = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
-      // p = 2^(s * sl2 - m): pairs through one packed FMA, then ex2 each; a
-      // masked column gets exactly 0 (a select, so no NaN can survive).
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_sub, -m_sub);
-      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+      // p = 2^(s * sl2 - m); a masked column gets exactly 0 (a select, so no
+      // NaN can survive).  The block-uniform branch sits outside the unrolled
+      // loops so each loop is one straight-line block the scheduler can
+      // interleave (MUFU latency hidden across columns).
+      const float neg_m = -m_sub;
+      float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+      if (masked) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        float a, b;
-        f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negm2), a, b);
-        a = ex2(a);
-        b = ex2(b);
-        if (masked) {
-          a = (2 * i < lim) ? a : 0.0f;
-          b = (2 * i + 1 < lim) ? b : 0.0f;
+        for (int c = 0; c < 128; c += 4) {
+          const float p0 = ex2(fmaf(s[c], sl2, neg_m)), p1 = ex2(fmaf(s[c + 1], sl2, neg_m));
+          const float p2 = ex2(fmaf(s[c + 2], sl2, neg_m)), p3 = ex2(fmaf(s[c + 3], sl2, neg_m));
+          s[c] = (c < lim) ? p0 : 0.0f;
+          s[c + 1] = (c + 1 < lim) ? p1 : 0.0f;
+          s[c + 2] = (c + 2 < lim) ? p2 : 0.0f;
+          s[c + 3] = (c + 3 < lim) ? p3 : 0.0f;
+          ps0 += s[c]; ps1 += s[c + 1]; ps2 += s[c + 2]; ps3 += s[c + 3];
         }
-        s[2 * i] = a;
-        s[2 * i + 1] = b;
-        if (i & 1)
-          acc1 = f2_add(acc1, f2_pack(a, b));
-        else
-          acc0 = f2_add(acc0, f2_pack(a, b));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          s[c] = ex2(fmaf(s[c], sl2, neg_m));
+          s[c + 1] = ex2(fmaf(s[c + 1], sl2, neg_m));
+          s[c + 2] = ex2(fmaf(s[c + 2], sl2, neg_m));
+          s[c + 3] = ex2(fmaf(s[c + 3], sl2, neg_m));
+          ps0 += s[c]; ps1 += s[c + 1]; ps2 += s[c + 2]; ps3 += s[c + 3];
+        }
       }
-      {
-        float x0, x1;
-        f2_unpack(f2_add(acc0, acc1), x0, x1);
-        l += x0 + x1;
-      }
+      l += (ps0 + ps1) + (ps2 + ps3);
 
       if constexpr (C::kFp8) {
         uint32_t pk[32];
