@@ -26,19 +26,19 @@
 namespace fa {
 // Explicit instantiations live in fa_inst_*.cu (compiled in parallel).
 extern template cudaError_t launch_fa_fwd<64, kDtF16>(const CUtensorMap&, const CUtensorMap&,
-                                                       const CUtensorMap&, const KernelParams&,
+                                                       const CUtensorMap&, const CUtensorMap&, const KernelParams&,
                                                        int, cudaStream_t);
 extern template cudaError_t launch_fa_fwd<128, kDtF16>(const CUtensorMap&, const CUtensorMap&,
-                                                        const CUtensorMap&, const KernelParams&,
+                                                        const CUtensorMap&, const CUtensorMap&, const KernelParams&,
                                                         int, cudaStream_t);
 extern template cudaError_t launch_fa_fwd<64, kDtBF16>(const CUtensorMap&, const CUtensorMap&,
-                                                        const CUtensorMap&, const KernelParams&,
+                                                        const CUtensorMap&, const CUtensorMap&, const KernelParams&,
                                                         int, cudaStream_t);
 extern template cudaError_t launch_fa_fwd<128, kDtBF16>(const CUtensorMap&, const CUtensorMap&,
-                                                         const CUtensorMap&, const KernelParams&,
+                                                         const CUtensorMap&, const CUtensorMap&, const KernelParams&,
                                                          int, cudaStream_t);
 extern template cudaError_t launch_fa_fwd<128, kDtE4M3>(const CUtensorMap&, const CUtensorMap&,
-                                                         const CUtensorMap&, const KernelParams&,
+                                                         const CUtensorMap&, const CUtensorMap&, const KernelParams&,
                                                          int, cudaStream_t);
 }  // namespace fa
 
@@ -97,7 +97,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // sequence dimension is its own map dimension, so rows >= S are never read
 // (in BSND the bytes after row S-1 of batch b are batch b+1's rows).
 bool make_map(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, fa_layout_t layout, int64_t B,
-              int64_t H, int64_t S, int64_t D) {
+              int64_t H, int64_t S, int64_t D, cuuint32_t box_rows = 128) {
   auto enc = encode_fn();
   if (!enc) return false;
   const uint64_t eb = (dtype == FA_DTYPE_FP8E4M3) ? 1 : 2;
@@ -110,11 +110,11 @@ bool make_map(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, fa_layout_t lay
   if (layout == FA_LAYOUT_BNSD) {
     dims[0] = D; dims[1] = S; dims[2] = H; dims[3] = B;
     strides[0] = D * eb; strides[1] = S * D * eb; strides[2] = H * S * D * eb;
-    box[0] = inner; box[1] = 128; box[2] = 1; box[3] = 1;
+    box[0] = inner; box[1] = box_rows; box[2] = 1; box[3] = 1;
   } else {
     dims[0] = D; dims[1] = H; dims[2] = S; dims[3] = B;
     strides[0] = D * eb; strides[1] = H * D * eb; strides[2] = S * H * D * eb;
-    box[0] = inner; box[1] = 1; box[2] = 128; box[3] = 1;
+    box[0] = inner; box[1] = 1; box[2] = box_rows; box[3] = 1;
   }
   CUresult r = enc(m, t, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -196,9 +196,13 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
   DeviceInfo dev;
   if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
 
-  CUtensorMap mq, mk, mv;
+  // O: the output dtype (16-bit; bf16 for fp8 inputs), boxes of 32 rows (one
+  // warp's rows) x 128 bytes, written by TMA stores.
+  CUtensorMap mq, mk, mv, mo;
+  const fa_dtype_t odt = (dtype == FA_DTYPE_F16) ? FA_DTYPE_F16 : FA_DTYPE_BF16;
   if (!make_map(&mq, q, dtype, layout, B, H, S_q, D) || !make_map(&mk, k, dtype, layout, B, H, S_kv, D) ||
-      !make_map(&mv, v, dtype, layout, B, H, S_kv, D))
+      !make_map(&mv, v, dtype, layout, B, H, S_kv, D) ||
+      !make_map(&mo, o, odt, layout, B, H, S_q, D, 32))
     return FA_ERR_CUDA;
 
   fa::KernelParams p = {};
@@ -230,13 +234,13 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
   const int grid = static_cast<int>(p.num_units < dev.sm_count ? p.num_units : dev.sm_count);
   cudaError_t e;
   if (dtype == FA_DTYPE_F16)
-    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtF16>(mq, mk, mv, p, grid, stream)
-                  : fa::launch_fa_fwd<128, fa::kDtF16>(mq, mk, mv, p, grid, stream);
+    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtF16>(mq, mk, mv, mo, p, grid, stream)
+                  : fa::launch_fa_fwd<128, fa::kDtF16>(mq, mk, mv, mo, p, grid, stream);
   else if (dtype == FA_DTYPE_BF16)
-    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtBF16>(mq, mk, mv, p, grid, stream)
-                  : fa::launch_fa_fwd<128, fa::kDtBF16>(mq, mk, mv, p, grid, stream);
+    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtBF16>(mq, mk, mv, mo, p, grid, stream)
+                  : fa::launch_fa_fwd<128, fa::kDtBF16>(mq, mk, mv, mo, p, grid, stream);
   else
-    e = fa::launch_fa_fwd<128, fa::kDtE4M3>(mq, mk, mv, p, grid, stream);
+    e = fa::launch_fa_fwd<128, fa::kDtE4M3>(mq, mk, mv, mo, p, grid, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

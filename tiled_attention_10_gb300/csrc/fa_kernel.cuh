@@ -100,10 +100,14 @@ struct Cfg {
   static constexpr int kUK = kFp8 ? 32 : 16;          // K of one UMMA instruction
   static constexpr int kQKSteps = D / kUK;
   static constexpr int kPVSteps = kBN / kUK;
-  static constexpr int kSlots = (kTileBytes >= 32768) ? 5 : 8;
+  static constexpr int kSlots = (kTileBytes >= 32768) ? 4 : 8;
   static constexpr int kQBytes = 2 * kTileBytes;
-  static constexpr int kBarOffset = kQBytes + kSlots * kTileBytes;
-  static constexpr int kNumBars = 2 * kSlots + 9;
+  // Epilogue staging: per warp one 32-row x 128-byte box of O (64 columns),
+  // written by the warp and drained by a TMA store: 8 warps x 4 KB.
+  static constexpr int kEpiBoxBytes = 32 * 128;
+  static constexpr int kEpiOffset = kQBytes + kSlots * kTileBytes;
+  static constexpr int kBarOffset = kEpiOffset + 8 * kEpiBoxBytes;
+  static constexpr int kNumBars = 2 * kSlots + 11;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;  // + align slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr uint32_t kFmt = kFp8 ? 0u : (DT == kDtBF16 ? 1u : 0u);
@@ -163,9 +167,9 @@ struct Bars {
   __device__ uint32_t q_full() const { return base + 8u * (2 * ns); }
   __device__ uint32_t q_empty() const { return base + 8u * (2 * ns + 1); }
   __device__ uint32_t s_full(int t) const { return base + 8u * (2 * ns + 2 + t); }
-  __device__ uint32_t p_ready(int t) const { return base + 8u * (2 * ns + 4 + t); }
-  __device__ uint32_t o_done(int t) const { return base + 8u * (2 * ns + 6 + t); }
-  __device__ uint32_t drain() const { return base + 8u * (2 * ns + 8); }
+  __device__ uint32_t p_half(int t, int h) const { return base + 8u * (2 * ns + 4 + 2 * t + h); }
+  __device__ uint32_t o_done(int t) const { return base + 8u * (2 * ns + 8 + t); }
+  __device__ uint32_t drain() const { return base + 8u * (2 * ns + 10); }
 };
 
 // Short bounded wait used only while tearing down after an abort: it ignores
@@ -246,15 +250,17 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t qlo, uint32_t
   }
 }
 
-// O_t (+)= P_t V: A = P_t from TMEM (kUK elements of K = 8 columns per step),
-// B = V rows [kk*kUK, +kUK) MN-major (128-byte rows; LBO = next column chunk).
-template <int D, int DT>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t vlo,
-                                         uint32_t accumulate) {
+// O_t (+)= P_t V for keys [64h, 64h+64) (half h of the block): A = P_t from
+// TMEM (kUK elements of K = 8 columns per step), B = V rows [kk*kUK, +kUK),
+// MN-major (128-byte rows; LBO = next column chunk).
+template <int D, int DT, int H>
+__device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, uint32_t vlo,
+                                              uint32_t accumulate) {
   using C = Cfg<D, DT>;
   constexpr uint32_t hi = umma_desc_hi_sw128(1024);
+  constexpr int kHalf = C::kPVSteps / 2;
 #pragma unroll
-  for (int kk = 0; kk < C::kPVSteps; ++kk) {
+  for (int kk = H * kHalf; kk < (H + 1) * kHalf; ++kk) {
     const uint32_t off = static_cast<uint32_t>((kk * C::kUK * 128) >> 4);
     umma_ts_w<C::kFp8>(o_tmem, p_tmem + kk * 8, vlo + off, hi, C::kIdescPV,
                        kk > 0 ? 1u : accumulate);
@@ -325,14 +331,17 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
       bool v_ready = false, k_ready = !has_next;
       for (int t = 0; t < 2; ++t) {
         if (j >= n[t]) continue;
-        if (!mbar_wait(bars.p_ready(t), p_phase[t], wc)) { ok = false; break; }
-        p_phase[t] ^= 1u;
+        if (!mbar_wait(bars.p_half(t, 0), p_phase[t], wc)) { ok = false; break; }
         if (!v_ready) {
           if (!mbar_wait(bars.full(slotV), phV, wc)) { ok = false; break; }
           v_ready = true;
         }
         tc_fence_after();
-        issue_pv<D, DT>(tO[t], tS[t], v_lo0 + slotV * kTileW, j > 0 ? 1u : 0u);
+        issue_pv_half<D, DT, 0>(tO[t], tS[t], v_lo0 + slotV * kTileW, j > 0 ? 1u : 0u);
+        if (!mbar_wait(bars.p_half(t, 1), p_phase[t], wc)) { ok = false; break; }
+        p_phase[t] ^= 1u;
+        tc_fence_after();
+        issue_pv_half<D, DT, 1>(tO[t], tS[t], v_lo0 + slotV * kTileW, 1u);
         if (j + 1 < n[t]) {
           if (!k_ready) {
             if (!mbar_wait(bars.full(slotKn), phK, wc)) { ok = false; break; }
@@ -366,22 +375,17 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
 // ---------------------------------------------------------------------------
 // Softmax / correction / epilogue (warps 0-7; one query row per thread).
 // ---------------------------------------------------------------------------
-template <int DT>
-__device__ __forceinline__ void store_out_chunk(void* dst, const float (&x)[32], bool row_ok) {
-  uint32_t w[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    w[i] = (DT == kDtF16) ? pack_f16x2(x[2 * i], x[2 * i + 1]) : pack_bf16x2(x[2 * i], x[2 * i + 1]);
-  if (row_ok) {
-    uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-  }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 
 template <int D, int DT>
-__device__ void softmax_role(const KernelParams& p, uint32_t tmem, int warp, int lane,
-                             const Bars& bars, const WaitCtl& wc) {
+__device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, uint32_t tmem,
+                             uint32_t sEpi, int warp, int lane, const Bars& bars,
+                             const WaitCtl& wc) {
   using C = Cfg<D, DT>;
   const int t = warp >> 2;            // query tile of this warpgroup
   const int wq = warp & 3;            // TMEM lane quarter
@@ -470,53 +474,9 @@ __device__ void softmax_role(const KernelParams& p, uint32_t tmem, int warp, int
         m_run = m_new;
       }
       const float m_sub = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
-      // p = 2^(s * sl2 - m); a masked column gets exactly 0 (a select, so no
-      // NaN can survive).  The block-uniform branch sits outside the unrolled
-      // loops so each loop is one straight-line block the scheduler can
-      // interleave (MUFU latency hidden across columns).
-      const float neg_m = -m_sub;
-      float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
-      if (masked) {
-#pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          const float p0 = ex2(fmaf(s[c], sl2, neg_m)), p1 = ex2(fmaf(s[c + 1], sl2, neg_m));
-          const float p2 = ex2(fmaf(s[c + 2], sl2, neg_m)), p3 = ex2(fmaf(s[c + 3], sl2, neg_m));
-          s[c] = (c < lim) ? p0 : 0.0f;
-          s[c + 1] = (c + 1 < lim) ? p1 : 0.0f;
-          s[c + 2] = (c + 2 < lim) ? p2 : 0.0f;
-          s[c + 3] = (c + 3 < lim) ? p3 : 0.0f;
-          ps0 += s[c]; ps1 += s[c + 1]; ps2 += s[c + 2]; ps3 += s[c + 3];
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          s[c] = ex2(fmaf(s[c], sl2, neg_m));
-          s[c + 1] = ex2(fmaf(s[c + 1], sl2, neg_m));
-          s[c + 2] = ex2(fmaf(s[c + 2], sl2, neg_m));
-          s[c + 3] = ex2(fmaf(s[c + 3], sl2, neg_m));
-          ps0 += s[c]; ps1 += s[c + 1]; ps2 += s[c + 2]; ps3 += s[c + 3];
-        }
-      }
-      l += (ps0 + ps1) + (ps2 + ps3);
-
-      if constexpr (C::kFp8) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          pk[i] = pack_e4m3x4(s[4 * i] * 256.f, s[4 * i + 1] * 256.f, s[4 * i + 2] * 256.f,
-                              s[4 * i + 3] * 256.f);
-        tmem_st_x32(tS, pk);
-      } else {
-        uint32_t pk[2][32];
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          pk[i >> 5][i & 31] = (DT == kDtF16) ? pack_f16x2(s[2 * i], s[2 * i + 1])
-                                              : pack_bf16x2(s[2 * i], s[2 * i + 1]);
-        tmem_st_x32(tS, pk[0]);
-        tmem_st_x32(tS + 32, pk[1]);
-      }
-      // O_t *= alpha for the rows whose max moved (O is complete: the commit
-      // that signalled S_j covered the previous PV; the next PV waits for us).
+      // O_t *= alpha for the rows whose max moved, before any PV of this block
+      // accumulates into O (O is complete: the commit that signalled S_j
+      // covered the previous PV; this block's PV waits for P below).
       if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -528,39 +488,122 @@ __device__ void softmax_role(const KernelParams& p, uint32_t tmem, int warp, int
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
           tmem_st_x32(tO + 32 * c, ov);
         }
+        tmem_wait_st();
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bars.p_ready(t));
+      // p = 2^(s * sl2 - m), in two halves of 64 columns.  After each half its
+      // P (16-bit, or e4m3 x 256) goes to TMEM and is signalled, so the PV
+      // product of the first 64 keys runs while the second half is computed.
+      // A masked column gets exactly 0 (a select: no NaN can survive).  The
+      // block-uniform mask branch sits outside the unrolled loops so each loop
+      // is straight-line code and MUFU latency hides across columns.
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_sub, -m_sub);
+      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (masked) {
+#pragma unroll
+          for (int i = 32 * h; i < 32 * h + 32; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negm2), x0, x1);
+            x0 = (2 * i < lim) ? ex2(x0) : 0.0f;
+            x1 = (2 * i + 1 < lim) ? ex2(x1) : 0.0f;
+            s[2 * i] = x0;
+            s[2 * i + 1] = x1;
+            if (i & 1) acc1 = f2_add(acc1, f2_pack(x0, x1)); else acc0 = f2_add(acc0, f2_pack(x0, x1));
+          }
+        } else {
+#pragma unroll
+          for (int i = 32 * h; i < 32 * h + 32; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negm2), x0, x1);
+            x0 = ex2(x0);
+            x1 = ex2(x1);
+            s[2 * i] = x0;
+            s[2 * i + 1] = x1;
+            if (i & 1) acc1 = f2_add(acc1, f2_pack(x0, x1)); else acc0 = f2_add(acc0, f2_pack(x0, x1));
+          }
+        }
+        if constexpr (C::kFp8) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = 64 * h + 4 * i;
+            pk[i] = pack_e4m3x4(s[c] * 256.f, s[c + 1] * 256.f, s[c + 2] * 256.f, s[c + 3] * 256.f);
+          }
+          tmem_st_x16(tS + 16 * h, pk);
+        } else {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = 64 * h + 2 * i;
+            pk[i] = (DT == kDtF16) ? pack_f16x2(s[c], s[c + 1]) : pack_bf16x2(s[c], s[c + 1]);
+          }
+          tmem_st_x32(tS + 32 * h, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bars.p_half(t, h));
+      }
+      {
+        float x0, x1;
+        f2_unpack(f2_add(acc0, acc1), x0, x1);
+        l += x0 + x1;
+      }
     }
     if (!ok) break;
 
-    // Epilogue: O / l -> output dtype, and lse, for rows < S_q.
+    // Epilogue: O / l -> output dtype, staged per warp (32 rows x 64 columns,
+    // 128-byte swizzle) and written by a TMA store whose tensor map clips rows
+    // >= S_q; then lse for rows < S_q.
     if (!mbar_wait(bars.o_done(t), o_phase, wc)) break;
     o_phase ^= 1u;
     tc_fence_after();
     const float inv = o_mul / l;
-    const bool row_ok = row < p.S_q;
-    const int64_t b = bh / p.H, h = bh % p.H;
-    const int64_t orow = (p.layout == 0) ? ((b * p.H + h) * p.S_q + row) : ((b * p.S_q + row) * p.H + h);
-    uint16_t* out = reinterpret_cast<uint16_t*>(p.o) + (row_ok ? orow * D : 0);
+    const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
+    const int32_t box_row0 = q_tile * kBM + wq * 32;
+    const uint32_t stage = sEpi + static_cast<uint32_t>(warp) * C::kEpiBoxBytes;
 #pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t ov[32];
-      tmem_ld_x32(tO + 32 * c, ov);
+    for (int hh = 0; hh < D / 64; ++hh) {
+      uint32_t o0[32], o1[32];
+      tmem_ld_x32(tO + 64 * hh, o0);
+      tmem_ld_x32(tO + 64 * hh + 32, o1);
       tmem_wait_ld();
-      reg_dep_x32(ov);
-      float x[32];
+      reg_dep_x32(o0);
+      reg_dep_x32(o1);
+      uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(ov[i]) * inv;
-      store_out_chunk<DT>(out + 32 * c, x, row_ok);
+      for (int i = 0; i < 16; ++i) {
+        const float a0 = __uint_as_float(o0[2 * i]) * inv, a1 = __uint_as_float(o0[2 * i + 1]) * inv;
+        const float c0 = __uint_as_float(o1[2 * i]) * inv, c1 = __uint_as_float(o1[2 * i + 1]) * inv;
+        pk[i] = (DT == kDtF16) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
+        pk[16 + i] = (DT == kDtF16) ? pack_f16x2(c0, c1) : pack_bf16x2(c0, c1);
+      }
+      // The previous TMA store from this staging box must have read it.
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(stage + lane * 128 + ((u ^ (lane & 7)) << 4), pk[4 * u], pk[4 * u + 1],
+                     pk[4 * u + 2], pk[4 * u + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && box_row0 < p.S_q) {  // rows past S_q are clipped by the map
+        if (p.layout == 0)
+          tma_store_4d(tmO, stage, 64 * hh, box_row0, h, b);
+        else
+          tma_store_4d(tmO, stage, 64 * hh, h, box_row0, b);
+        bulk_commit_group();
+      }
     }
-    if (row_ok) {
+    if (row < p.S_q) {
       const float lse2 = m_run + log2f(l);
       p.lse[static_cast<int64_t>(bh) * p.S_q + row] = lse2 * 0.69314718055994531f;
     }
     tc_fence_before();
   }
+  // Every TMA store of this warp has completed before the CTA exits.
+  if (lane == 0) bulk_wait_group0();
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -569,7 +612,8 @@ __device__ void softmax_role(const KernelParams& p, uint32_t tmem, int warp, int
 template <int D, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ KernelParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const __grid_constant__ KernelParams p) {
   using C = Cfg<D, DT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -577,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sQ = base;
   const uint32_t sRing = base + C::kQBytes;
+  const uint32_t sEpi = base + C::kEpiOffset;
   const Bars bars{base + static_cast<uint32_t>(C::kBarOffset), C::kSlots};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOffset + C::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -591,7 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bars.q_empty(), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(bars.s_full(t), 1);
-      mbar_init(bars.p_ready(t), 128);
+      mbar_init(bars.p_half(t, 0), 128);
+      mbar_init(bars.p_half(t, 1), 128);
       mbar_init(bars.o_done(t), 1);
     }
     mbar_init(bars.drain(), 1);
@@ -602,6 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -615,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kProducerWarp) {
     reg_alloc_inc<kRegsSoftmax>();
-    softmax_role<D, DT>(p, tmem, warp, lane, bars, wc);
+    softmax_role<D, DT>(p, &tmO, tmem, sEpi, warp, lane, bars, wc);
   } else {
     reg_alloc_dec<kRegsControl>();
     if (warp == kProducerWarp) {
@@ -636,7 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Host-side launcher, one instantiation per (D, dtype).
 template <int D, int DT>
 cudaError_t launch_fa_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const KernelParams& p, int grid, cudaStream_t stream) {
+                          const CUtensorMap& o, const KernelParams& p, int grid,
+                          cudaStream_t stream) {
   using C = Cfg<D, DT>;
   auto kern = fa_fwd_kernel<D, DT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -646,7 +694,7 @@ cudaError_t launch_fa_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, p);
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, p);
 }
 
 }  // namespace fa
