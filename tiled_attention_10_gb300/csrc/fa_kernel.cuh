@@ -382,10 +382,118 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// One K/V block of the softmax for one query row (the thread's TMEM lane):
+// row max, running-max update with conditional O rescale, P = 2^(s*sl2 - m)
+// in two signalled halves, row sum.  Instantiated twice -- with and without
+// the tail/causal mask -- so the unmasked copy, which almost every block
+// runs, is one contiguous straight-line body.
+template <int D, int DT, bool kMasked>
+__device__ __forceinline__ void softmax_block(float (&s)[128], int lim, int j, float sl2,
+                                              float& m_run, float& l, uint32_t tS, uint32_t tO,
+                                              const Bars& bars, int t) {
+  using C = Cfg<D, DT>;
+  // Masked columns become -inf: they drop out of the max and give p = 0.
+  if constexpr (kMasked) {
+#pragma unroll
+    for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -CUDART_INF_F;
+  }
+  // 3-input max tree over the 128 scores (depth 5, ~64 instructions).
+  float t43[43];
+#pragma unroll
+  for (int i = 0; i < 42; ++i) t43[i] = max3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+  t43[42] = fmaxf(s[126], s[127]);
+  float t15[15];
+#pragma unroll
+  for (int i = 0; i < 14; ++i) t15[i] = max3(t43[3 * i], t43[3 * i + 1], t43[3 * i + 2]);
+  t15[14] = t43[42];
+  const float t5a = max3(t15[0], t15[1], t15[2]), t5b = max3(t15[3], t15[4], t15[5]);
+  const float t5c = max3(t15[6], t15[7], t15[8]), t5d = max3(t15[9], t15[10], t15[11]);
+  const float t5e = max3(t15[12], t15[13], t15[14]);
+  const float mxb = max3(max3(t5a, t5b, t5c), t5d, t5e);
+  const float m_blk = (mxb == -CUDART_INF_F) ? -CUDART_INF_F : mxb * sl2;
+  const float m_new = fmaxf(m_run, m_blk);
+  // Decide the running max for this block.  On the first block O holds
+  // nothing yet (its first PV overwrites it); later the max only moves
+  // when it grew past the threshold, and then O and l are rescaled.
+  float alpha = 1.0f;
+  bool resc = false;
+  if (j == 0) {
+    m_run = m_new;
+  } else if (m_new > m_run + C::kRescaleThreshold) {
+    resc = true;
+    alpha = ex2(m_run - m_new);
+    l *= alpha;
+    m_run = m_new;
+  }
+  const float m_sub = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
+  // O_t *= alpha for the rows whose max moved, before any PV of this block
+  // accumulates into O (O is complete: the commit that signalled S_j
+  // covered the previous PV; this block's PV waits for P below).
+  if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t ov[32];
+      tmem_ld_x32(tO + 32 * c, ov);
+      tmem_wait_ld();
+      reg_dep_x32(ov);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+      tmem_st_x32(tO + 32 * c, ov);
+    }
+    tmem_wait_st();
+  }
+  // p = 2^(s * sl2 - m), in two halves of 64 columns.  After each half its
+  // P (16-bit, or e4m3 x 256) goes to TMEM and is signalled, so the PV
+  // product of the first 64 keys runs while the second half is computed.
+  // The loops are straight-line code (no branch inside) so the scheduler
+  // can hide MUFU latency across columns.
+  const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_sub, -m_sub);
+  uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    // Masked columns already hold -inf (set before the max), and sl2 > 0,
+    // so they come out as exactly 0; one loop serves every block.
+#pragma unroll
+    for (int i = 32 * h; i < 32 * h + 32; ++i) {
+      float x0, x1;
+      f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negm2), x0, x1);
+      x0 = ex2(x0);
+      x1 = ex2(x1);
+      s[2 * i] = x0;
+      s[2 * i + 1] = x1;
+      if (i & 1) acc1 = f2_add(acc1, f2_pack(x0, x1)); else acc0 = f2_add(acc0, f2_pack(x0, x1));
+    }
+    if constexpr (C::kFp8) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int c = 64 * h + 4 * i;
+        pk[i] = pack_e4m3x4(s[c] * 256.f, s[c + 1] * 256.f, s[c + 2] * 256.f, s[c + 3] * 256.f);
+      }
+      tmem_st_x16(tS + 16 * h, pk);
+    } else {
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int c = 64 * h + 2 * i;
+        pk[i] = (DT == kDtF16) ? pack_f16x2(s[c], s[c + 1]) : pack_bf16x2(s[c], s[c + 1]);
+      }
+      tmem_st_x32(tS + 32 * h, pk);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bars.p_half(t, h));
+  }
+  {
+    float x0, x1;
+    f2_unpack(f2_add(acc0, acc1), x0, x1);
+    l += x0 + x1;
+  }}
+
 template <int D, int DT>
 __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, uint32_t tmem,
-                             uint32_t sEpi, int warp, int lane, const Bars& bars,
-                             const WaitCtl& wc) {
+                           uint32_t sEpi, int warp, int lane, const Bars& bars,
+                           const WaitCtl& wc) {
   using C = Cfg<D, DT>;
   const int t = warp >> 2;            // query tile of this warpgroup
   const int wq = warp & 3;            // TMEM lane quarter
@@ -397,209 +505,107 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, uint
   float sl2 = p.scale_log2;
   float o_mul = 1.0f;
   if constexpr (C::kFp8) {
-    const float dq = p.descale_q ? *p.descale_q : 1.0f;
-    const float dk = p.descale_k ? *p.descale_k : 1.0f;
-    const float dv = p.descale_v ? *p.descale_v : 1.0f;
-    sl2 *= dq * dk;
-    o_mul = dv * (1.0f / 256.0f);  // P is stored as 256 * p in e4m3
+  const float dq = p.descale_q ? *p.descale_q : 1.0f;
+  const float dk = p.descale_k ? *p.descale_k : 1.0f;
+  const float dv = p.descale_v ? *p.descale_v : 1.0f;
+  sl2 *= dq * dk;
+  o_mul = dv * (1.0f / 256.0f);  // P is stored as 256 * p in e4m3
   }
+  // A masked score is -inf and must give p = 0: keep the base-2 scale
+  // strictly positive (a zero scale or descale becomes 1e-30, which changes
+  // no unmasked exponent by more than ~1e-29 relative).
+  sl2 = fmaxf(sl2, 1e-30f);
 
   uint32_t s_phase = 0u, o_phase = 0u;
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0;; ++w) {
-    const int u = unit_of_round(w, grid, bid);
-    if (u >= p.num_units) break;
-    int bh, pair;
-    decode_unit(p, u, bh, pair);
-    const int q_tile = 2 * pair + t;
-    const int n = tile_kv_blocks(p, q_tile);
-    if (n == 0) continue;
-    const int64_t row = static_cast<int64_t>(q_tile) * kBM + r;
-    const int64_t col_end = p.causal ? min(row + 1, p.S_kv) : p.S_kv;  // columns < col_end visible
-    const int64_t tile_row0 = static_cast<int64_t>(q_tile) * kBM;
+  const int u = unit_of_round(w, grid, bid);
+  if (u >= p.num_units) break;
+  int bh, pair;
+  decode_unit(p, u, bh, pair);
+  const int q_tile = 2 * pair + t;
+  const int n = tile_kv_blocks(p, q_tile);
+  if (n == 0) continue;
+  const int64_t row = static_cast<int64_t>(q_tile) * kBM + r;
+  const int64_t col_end = p.causal ? min(row + 1, p.S_kv) : p.S_kv;  // columns < col_end visible
+  const int64_t tile_row0 = static_cast<int64_t>(q_tile) * kBM;
 
-    float m_run = -CUDART_INF_F, l = 0.0f;
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      if (!mbar_wait(bars.s_full(t), s_phase, wc)) { ok = false; break; }
-      s_phase ^= 1u;
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_x32(tS + 32 * c, sr[c]);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) reg_dep_x32(sr[c]);
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
-
-      const int64_t col0 = static_cast<int64_t>(j) * kBN;
-      // Block-uniform: does any column of this block need a mask?
-      const bool masked = (col0 + kBN > p.S_kv) || (p.causal && col0 + (kBN - 1) > tile_row0);
-      const int lim = static_cast<int>(max(min(col_end - col0, static_cast<int64_t>(kBN)), int64_t(0)));
-
-      // Row max of the block: masked columns become -inf first (block-uniform
-      // branch; only tail and diagonal blocks take it).
-      if (masked) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -CUDART_INF_F;
-      }
-      // 3-input max tree over the 128 scores (depth 5, ~64 instructions).
-      float t43[43];
-#pragma unroll
-      for (int i = 0; i < 42; ++i) t43[i] = max3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
-      t43[42] = fmaxf(s[126], s[127]);
-      float t15[15];
-#pragma unroll
-      for (int i = 0; i < 14; ++i) t15[i] = max3(t43[3 * i], t43[3 * i + 1], t43[3 * i + 2]);
-      t15[14] = t43[42];
-      const float t5a = max3(t15[0], t15[1], t15[2]), t5b = max3(t15[3], t15[4], t15[5]);
-      const float t5c = max3(t15[6], t15[7], t15[8]), t5d = max3(t15[9], t15[10], t15[11]);
-      const float t5e = max3(t15[12], t15[13], t15[14]);
-      const float mxb = max3(max3(t5a, t5b, t5c), t5d, t5e);
-      const float m_blk = (mxb == -CUDART_INF_F) ? -CUDART_INF_F : mxb * sl2;
-      const float m_new = fmaxf(m_run, m_blk);
-      // Decide the running max for this block.  On the first block O holds
-      // nothing yet (its first PV overwrites it); later the max only moves
-      // when it grew past the threshold, and then O and l are rescaled.
-      float alpha = 1.0f;
-      bool resc = false;
-      if (j == 0) {
-        m_run = m_new;
-      } else if (m_new > m_run + C::kRescaleThreshold) {
-        resc = true;
-        alpha = ex2(m_run - m_new);
-        l *= alpha;
-        m_run = m_new;
-      }
-      const float m_sub = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
-      // O_t *= alpha for the rows whose max moved, before any PV of this block
-      // accumulates into O (O is complete: the commit that signalled S_j
-      // covered the previous PV; this block's PV waits for P below).
-      if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld_x32(tO + 32 * c, ov);
-          tmem_wait_ld();
-          reg_dep_x32(ov);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st_x32(tO + 32 * c, ov);
-        }
-        tmem_wait_st();
-      }
-      // p = 2^(s * sl2 - m), in two halves of 64 columns.  After each half its
-      // P (16-bit, or e4m3 x 256) goes to TMEM and is signalled, so the PV
-      // product of the first 64 keys runs while the second half is computed.
-      // A masked column gets exactly 0 (a select: no NaN can survive).  The
-      // block-uniform mask branch sits outside the unrolled loops so each loop
-      // is straight-line code and MUFU latency hides across columns.
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_sub, -m_sub);
-      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (masked) {
-#pragma unroll
-          for (int i = 32 * h; i < 32 * h + 32; ++i) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negm2), x0, x1);
-            x0 = (2 * i < lim) ? ex2(x0) : 0.0f;
-            x1 = (2 * i + 1 < lim) ? ex2(x1) : 0.0f;
-            s[2 * i] = x0;
-            s[2 * i + 1] = x1;
-            if (i & 1) acc1 = f2_add(acc1, f2_pack(x0, x1)); else acc0 = f2_add(acc0, f2_pack(x0, x1));
-          }
-        } else {
-#pragma unroll
-          for (int i = 32 * h; i < 32 * h + 32; ++i) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sl2x2, negm2), x0, x1);
-            x0 = ex2(x0);
-            x1 = ex2(x1);
-            s[2 * i] = x0;
-            s[2 * i + 1] = x1;
-            if (i & 1) acc1 = f2_add(acc1, f2_pack(x0, x1)); else acc0 = f2_add(acc0, f2_pack(x0, x1));
-          }
-        }
-        if constexpr (C::kFp8) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c = 64 * h + 4 * i;
-            pk[i] = pack_e4m3x4(s[c] * 256.f, s[c + 1] * 256.f, s[c + 2] * 256.f, s[c + 3] * 256.f);
-          }
-          tmem_st_x16(tS + 16 * h, pk);
-        } else {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c = 64 * h + 2 * i;
-            pk[i] = (DT == kDtF16) ? pack_f16x2(s[c], s[c + 1]) : pack_bf16x2(s[c], s[c + 1]);
-          }
-          tmem_st_x32(tS + 32 * h, pk);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bars.p_half(t, h));
-      }
-      {
-        float x0, x1;
-        f2_unpack(f2_add(acc0, acc1), x0, x1);
-        l += x0 + x1;
-      }
-    }
-    if (!ok) break;
-
-    // Epilogue: O / l -> output dtype, staged per warp (32 rows x 64 columns,
-    // 128-byte swizzle) and written by a TMA store whose tensor map clips rows
-    // >= S_q; then lse for rows < S_q.
-    if (!mbar_wait(bars.o_done(t), o_phase, wc)) break;
-    o_phase ^= 1u;
+  float m_run = -CUDART_INF_F, l = 0.0f;
+  bool ok = true;
+  for (int j = 0; j < n; ++j) {
+    if (!mbar_wait(bars.s_full(t), s_phase, wc)) { ok = false; break; }
+    s_phase ^= 1u;
     tc_fence_after();
-    const float inv = o_mul / l;
-    const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
-    const int32_t box_row0 = q_tile * kBM + wq * 32;
-    const uint32_t stage = sEpi + static_cast<uint32_t>(warp) * C::kEpiBoxBytes;
+    uint32_t sr[4][32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld_x32(tS + 32 * c, sr[c]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < 4; ++c) reg_dep_x32(sr[c]);
+    float s[128];
+#pragma unroll
+    for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+    const int64_t col0 = static_cast<int64_t>(j) * kBN;
+    // Block-uniform: does any column of this block need a mask?
+    const bool masked = (col0 + kBN > p.S_kv) || (p.causal && col0 + (kBN - 1) > tile_row0);
+    const int lim = static_cast<int>(max(min(col_end - col0, static_cast<int64_t>(kBN)), int64_t(0)));
+
+    if (masked)
+      softmax_block<D, DT, true>(s, lim, j, sl2, m_run, l, tS, tO, bars, t);
+    else
+      softmax_block<D, DT, false>(s, kBN, j, sl2, m_run, l, tS, tO, bars, t);
+  }
+  if (!ok) break;
+
+  // Epilogue: O / l -> output dtype, staged per warp (32 rows x 64 columns,
+  // 128-byte swizzle) and written by a TMA store whose tensor map clips rows
+  // >= S_q; then lse for rows < S_q.
+  if (!mbar_wait(bars.o_done(t), o_phase, wc)) break;
+  o_phase ^= 1u;
+  tc_fence_after();
+  const float inv = o_mul / l;
+  const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
+  const int32_t box_row0 = q_tile * kBM + wq * 32;
+  const uint32_t stage = sEpi + static_cast<uint32_t>(warp) * C::kEpiBoxBytes;
 #pragma unroll 1
-    for (int hh = 0; hh < D / 64; ++hh) {
-      uint32_t o0[32], o1[32];
-      tmem_ld_x32(tO + 64 * hh, o0);
-      tmem_ld_x32(tO + 64 * hh + 32, o1);
-      tmem_wait_ld();
-      reg_dep_x32(o0);
-      reg_dep_x32(o1);
-      uint32_t pk[32];
+  for (int hh = 0; hh < D / 64; ++hh) {
+    uint32_t o0[32], o1[32];
+    tmem_ld_x32(tO + 64 * hh, o0);
+    tmem_ld_x32(tO + 64 * hh + 32, o1);
+    tmem_wait_ld();
+    reg_dep_x32(o0);
+    reg_dep_x32(o1);
+    uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float a0 = __uint_as_float(o0[2 * i]) * inv, a1 = __uint_as_float(o0[2 * i + 1]) * inv;
-        const float c0 = __uint_as_float(o1[2 * i]) * inv, c1 = __uint_as_float(o1[2 * i + 1]) * inv;
-        pk[i] = (DT == kDtF16) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
-        pk[16 + i] = (DT == kDtF16) ? pack_f16x2(c0, c1) : pack_bf16x2(c0, c1);
-      }
-      // The previous TMA store from this staging box must have read it.
-      if (lane == 0) bulk_wait_group_read0();
-      __syncwarp();
+    for (int i = 0; i < 16; ++i) {
+      const float a0 = __uint_as_float(o0[2 * i]) * inv, a1 = __uint_as_float(o0[2 * i + 1]) * inv;
+      const float c0 = __uint_as_float(o1[2 * i]) * inv, c1 = __uint_as_float(o1[2 * i + 1]) * inv;
+      pk[i] = (DT == kDtF16) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
+      pk[16 + i] = (DT == kDtF16) ? pack_f16x2(c0, c1) : pack_bf16x2(c0, c1);
+    }
+    // The previous TMA store from this staging box must have read it.
+    if (lane == 0) bulk_wait_group_read0();
+    __syncwarp();
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_shared_v4(stage + lane * 128 + ((u ^ (lane & 7)) << 4), pk[4 * u], pk[4 * u + 1],
-                     pk[4 * u + 2], pk[4 * u + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0 && box_row0 < p.S_q) {  // rows past S_q are clipped by the map
-        if (p.layout == 0)
-          tma_store_4d(tmO, stage, 64 * hh, box_row0, h, b);
-        else
-          tma_store_4d(tmO, stage, 64 * hh, h, box_row0, b);
-        bulk_commit_group();
-      }
+    for (int u = 0; u < 8; ++u)
+      st_shared_v4(stage + lane * 128 + ((u ^ (lane & 7)) << 4), pk[4 * u], pk[4 * u + 1],
+                   pk[4 * u + 2], pk[4 * u + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && box_row0 < p.S_q) {  // rows past S_q are clipped by the map
+      if (p.layout == 0)
+        tma_store_4d(tmO, stage, 64 * hh, box_row0, h, b);
+      else
+        tma_store_4d(tmO, stage, 64 * hh, h, box_row0, b);
+      bulk_commit_group();
     }
-    if (row < p.S_q) {
-      const float lse2 = m_run + log2f(l);
-      p.lse[static_cast<int64_t>(bh) * p.S_q + row] = lse2 * 0.69314718055994531f;
-    }
-    tc_fence_before();
+  }
+  if (row < p.S_q) {
+    const float lse2 = m_run + log2f(l);
+    p.lse[static_cast<int64_t>(bh) * p.S_q + row] = lse2 * 0.69314718055994531f;
+  }
+  tc_fence_before();
   }
   // Every TMA store of this warp has completed before the CTA exits.
   if (lane == 0) bulk_wait_group0();
