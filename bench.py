@@ -183,12 +183,13 @@ def oracle_sample(w, x, n_heads: int, rows: int, threads: int = 0) -> float:
     import oracle
     import torch
     heads = []
+    g = w.H // w.kv_heads
     for bh in range(n_heads):
         b, h = divmod(bh, w.H)
         if w.layout == "BNSD":
-            heads.append((x.q[b, h, :rows], x.k[b, h], x.v[b, h]))
+            heads.append((x.q[b, h, :rows], x.k[b, h // g], x.v[b, h // g]))
         else:
-            heads.append((x.q[b, :rows, h], x.k[b, :, h], x.v[b, :, h]))
+            heads.append((x.q[b, :rows, h], x.k[b, :, h // g], x.v[b, :, h // g]))
     q = torch.stack([t[0] for t in heads]).unsqueeze(0).cpu()
     k = torch.stack([t[1] for t in heads]).unsqueeze(0).cpu()
     v = torch.stack([t[2] for t in heads]).unsqueeze(0).cpu()
@@ -224,7 +225,7 @@ def run_reference(args, w, world, rank):
     import oracle
     from tiled_attention_10_gb300.inputs import make_inputs
     oracle.build()
-    one = type(w)(**{**w.__dict__, "B": 1, "H": 1})
+    one = type(w)(**{**w.__dict__, "B": 1, "H": 1, "H_kv": None})
     x = make_inputs(one)
     cores = oracle.max_threads()
     rows = min(w.S_q, 256)
@@ -268,9 +269,10 @@ def run_ours(args, w, world, rank, local):
     sp = stream.cuda_stream
 
     def step(qq=q, kk=k, vv=v):
-        st = binding.fa_fwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
-                            lse.data_ptr(), w.B, w.H, w.S_q, w.S_kv, w.D, w.softmax_scale,
-                            w.layout, w.causal, w.dtype, ds[0], ds[1], ds[2], sp)
+        st = binding.fa_fwd_gqa(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
+                                lse.data_ptr(), w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D,
+                                w.softmax_scale, w.layout, w.causal, w.dtype, ds[0], ds[1],
+                                ds[2], sp)
         if st != 0:
             raise RuntimeError(f"fa_fwd: {binding.fa_status_string(st)}")
 
@@ -373,8 +375,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    from tiled_attention_10_gb300.inputs import HEADLINE, WORKLOADS
-    w = WORKLOADS[args.workload or HEADLINE]
+    from tiled_attention_10_gb300.inputs import ALL_WORKLOADS, HEADLINE
+    w = ALL_WORKLOADS[args.workload or HEADLINE]
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":

@@ -89,6 +89,24 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
                    fa_layout_t layout, int causal, fa_dtype_t dtype, const float* descale_q,
                    const float* descale_k, const float* descale_v, cudaStream_t stream);
 
+/*
+ * fa_fwd_gqa -- the same forward pass with grouped-query attention: q and o
+ * have H heads, k and v have H_kv heads, H a multiple of H_kv.  With
+ * ngroups = H / H_kv, query head h attends with key/value head h / ngroups:
+ * the query heads are taken in their own flat order, i.e. q viewed as
+ * [.., H_kv, ngroups, D] -- no regrouping or transposition of q by the
+ * caller.  (The Hygon retrospective, defect 12, is a GQA bug caused by glue
+ * code and kernel disagreeing on exactly this head order.)  lse is
+ * [B, H, S_q].  Every other argument, check and status is as for fa_fwd;
+ * additionally H_kv < 1 or H % H_kv != 0 gives FA_ERR_INVALID_ARG.
+ * fa_fwd(...) is fa_fwd_gqa(...) with H_kv = H.
+ */
+fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv, int64_t D,
+                       float scale, fa_layout_t layout, int causal, fa_dtype_t dtype,
+                       const float* descale_q, const float* descale_k, const float* descale_v,
+                       cudaStream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* fa_status_string(fa_status_t s);
 

@@ -52,9 +52,13 @@ def _load():
                                        dbl, ip, dbl, dbl, dbl, i64, vp, vp, vp, vp, ip]
         lib.fa_oracle_full.argtypes = [vp, vp, vp, ip, ip, i64, i64, i64, i64, i64,
                                        dbl, ip, dbl, dbl, dbl, vp, vp, ip]
+        lib.fa_oracle_rows_gqa.argtypes = [vp, vp, vp, ip, ip, i64, i64, i64, i64, i64, i64,
+                                           dbl, ip, dbl, dbl, dbl, i64, vp, vp, vp, vp, ip]
+        lib.fa_oracle_full_gqa.argtypes = [vp, vp, vp, ip, ip, i64, i64, i64, i64, i64, i64,
+                                           dbl, ip, dbl, dbl, dbl, vp, vp, ip]
         lib.fa_oracle_max_threads.argtypes = []
         for f in (lib.fa_oracle_decode, lib.fa_oracle_rows, lib.fa_oracle_full,
-                  lib.fa_oracle_max_threads):
+                  lib.fa_oracle_rows_gqa, lib.fa_oracle_full_gqa, lib.fa_oracle_max_threads):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -86,11 +90,12 @@ def decode(x, dtype: str) -> np.ndarray:
 
 
 def attention_rows(q, k, v, *, dtype, layout, B, H, S_q, S_kv, D, scale, causal,
-                   rows, descale=(1.0, 1.0, 1.0), want_p=False, threads=0):
+                   rows, descale=(1.0, 1.0, 1.0), want_p=False, threads=0, H_kv=None):
     """Oracle output for selected rows.
 
     rows: int64 array [n, 3] of (b, h, i).  Returns (O [n, D], lse [n]) and,
-    with want_p, P [n, S_kv].  Inputs are raw buffers in the given layout.
+    with want_p, P [n, S_kv].  Inputs are raw buffers in the given layout;
+    K and V have H_kv heads (default H; query head h reads head h // (H // H_kv)).
     """
     qa, ka, va = _raw(q), _raw(k), _raw(v)
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
@@ -98,8 +103,9 @@ def attention_rows(q, k, v, *, dtype, layout, B, H, S_q, S_kv, D, scale, causal,
     O = np.empty((n, D), dtype=np.float64)
     lse = np.empty(n, dtype=np.float64)
     P = np.empty((n, S_kv), dtype=np.float64) if want_p else None
-    rc = _load().fa_oracle_rows(qa.ctypes.data, ka.ctypes.data, va.ctypes.data,
-                                DTYPE_CODES[dtype], LAYOUT_CODES[layout], B, H, S_q, S_kv, D,
+    rc = _load().fa_oracle_rows_gqa(qa.ctypes.data, ka.ctypes.data, va.ctypes.data,
+                                DTYPE_CODES[dtype], LAYOUT_CODES[layout], B, H,
+                                H if H_kv is None else H_kv, S_q, S_kv, D,
                                 float(scale), int(bool(causal)), float(descale[0]),
                                 float(descale[1]), float(descale[2]), n, r.ctypes.data,
                                 O.ctypes.data, lse.ctypes.data,
@@ -110,13 +116,15 @@ def attention_rows(q, k, v, *, dtype, layout, B, H, S_q, S_kv, D, scale, causal,
 
 
 def attention_full(q, k, v, *, dtype, layout, B, H, S_q, S_kv, D, scale, causal,
-                   descale=(1.0, 1.0, 1.0), threads=0):
-    """Oracle output for every row: O [B, H, S_q, D] (BNSD order), lse [B, H, S_q]."""
+                   descale=(1.0, 1.0, 1.0), threads=0, H_kv=None):
+    """Oracle output for every row: O [B, H, S_q, D] (BNSD order), lse [B, H, S_q].
+    K and V have H_kv heads (default H)."""
     qa, ka, va = _raw(q), _raw(k), _raw(v)
     O = np.empty((B, H, S_q, D), dtype=np.float64)
     lse = np.empty((B, H, S_q), dtype=np.float64)
-    rc = _load().fa_oracle_full(qa.ctypes.data, ka.ctypes.data, va.ctypes.data,
-                                DTYPE_CODES[dtype], LAYOUT_CODES[layout], B, H, S_q, S_kv, D,
+    rc = _load().fa_oracle_full_gqa(qa.ctypes.data, ka.ctypes.data, va.ctypes.data,
+                                DTYPE_CODES[dtype], LAYOUT_CODES[layout], B, H,
+                                H if H_kv is None else H_kv, S_q, S_kv, D,
                                 float(scale), int(bool(causal)), float(descale[0]),
                                 float(descale[1]), float(descale[2]), O.ctypes.data,
                                 lse.ctypes.data, int(threads))

@@ -37,6 +37,12 @@
  *
  * Layouts: BNSD = [B, H, S, D] and BSND = [B, S, H, D], both contiguous;
  * element offsets are 64-bit throughout.
+ *
+ * Grouped-query attention (the Hygon retrospective, defect 12): Q has H heads,
+ * K and V have H_kv heads with H a multiple of H_kv, ngroups = H / H_kv, and
+ * query head h reads key/value head h / ngroups (Q viewed as
+ * [.., H_kv, ngroups, D] in its own flat head order).  H_kv = H is plain
+ * multi-head attention.
  */
 #include <math.h>
 #include <stdint.h>
@@ -119,13 +125,14 @@ typedef struct {
   int64_t B, H, S_q, S_kv, D;
   double scale, dq, dk, dv;
   int causal;
+  int64_t H_kv;
 } problem_t;
 
-/* Decode row s of head (b, h) of one tensor into out[0..D). */
-static void load_row(const problem_t* p, const void* t, int64_t S, double ds,
+/* Decode row s of head (b, h) of one tensor with `heads` heads into out[0..D). */
+static void load_row(const problem_t* p, const void* t, int64_t heads, int64_t S, double ds,
                      int64_t b, int64_t h, int64_t s, double* out) {
   for (int64_t d = 0; d < p->D; ++d) {
-    double x = decode_one(t, p->dtype, elem_offset(p->layout, p->H, S, p->D, b, h, s, d));
+    double x = decode_one(t, p->dtype, elem_offset(p->layout, heads, S, p->D, b, h, s, d));
     out[d] = (p->dtype == ORC_E4M3) ? x * ds : x;
   }
 }
@@ -165,6 +172,7 @@ static int check_problem(const problem_t* p) {
   if (p->B < 1 || p->H < 1 || p->S_q < 1 || p->S_kv < 1 || p->D < 1) return 2;
   if (p->dtype < ORC_F16 || p->dtype > ORC_E4M3) return 3;
   if (p->layout != ORC_BNSD && p->layout != ORC_BSND) return 4;
+  if (p->H_kv < 1 || p->H % p->H_kv != 0) return 8;
   return 0;
 }
 
@@ -178,12 +186,12 @@ int fa_oracle_decode(const void* x, int dtype, int64_t n, double* out) {
 /* Selected rows: rows holds n_rows triples (b, h, i).  O is [n_rows, D],
  * lse is [n_rows], P (optional, may be NULL) is [n_rows, S_kv].  Each row
  * decodes its own head's K and V, so this suits sparse samples. */
-int fa_oracle_rows(const void* q, const void* k, const void* v, int dtype, int layout,
-                   int64_t B, int64_t H, int64_t S_q, int64_t S_kv, int64_t D,
-                   double scale, int causal, double dq, double dk, double dv,
-                   int64_t n_rows, const int64_t* rows, double* O, double* lse,
-                   double* P, int n_threads) {
-  problem_t p = {q, k, v, dtype, layout, B, H, S_q, S_kv, D, scale, dq, dk, dv, causal};
+int fa_oracle_rows_gqa(const void* q, const void* k, const void* v, int dtype, int layout,
+                       int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv,
+                       int64_t D, double scale, int causal, double dq, double dk, double dv,
+                       int64_t n_rows, const int64_t* rows, double* O, double* lse,
+                       double* P, int n_threads) {
+  problem_t p = {q, k, v, dtype, layout, B, H, S_q, S_kv, D, scale, dq, dk, dv, causal, H_kv};
   int rc = check_problem(&p);
   if (rc) return rc;
   if (!rows || !O || !lse || n_rows < 0) return 5;
@@ -214,11 +222,12 @@ int fa_oracle_rows(const void* q, const void* k, const void* v, int dtype, int l
 #endif
       for (int64_t r = 0; r < n_rows; ++r) {
         int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+        int64_t hk = h / (H / H_kv);
         for (int64_t j = 0; j < S_kv; ++j) {
-          load_row(&p, k, S_kv, dk, b, h, j, kd + j * D);
-          load_row(&p, v, S_kv, dv, b, h, j, vd + j * D);
+          load_row(&p, k, H_kv, S_kv, dk, b, hk, j, kd + j * D);
+          load_row(&p, v, H_kv, S_kv, dv, b, hk, j, vd + j * D);
         }
-        load_row(&p, q, S_q, dq, b, h, i, qrow);
+        load_row(&p, q, H, S_q, dq, b, h, i, qrow);
         attend_row(&p, qrow, kd, vd, i, Srow, Prow, O + r * D, lse + r);
         if (P) memcpy(P + r * S_kv, Prow, sizeof(double) * (size_t)S_kv);
       }
@@ -231,11 +240,11 @@ int fa_oracle_rows(const void* q, const void* k, const void* v, int dtype, int l
 /* Every row of every head.  O is [B, H, S_q, D] (BNSD, whatever the input
  * layout), lse is [B, H, S_q].  Heads are taken one after another; inside a
  * head the K/V decode and then the query rows run in parallel. */
-int fa_oracle_full(const void* q, const void* k, const void* v, int dtype, int layout,
-                   int64_t B, int64_t H, int64_t S_q, int64_t S_kv, int64_t D,
-                   double scale, int causal, double dq, double dk, double dv,
-                   double* O, double* lse, int n_threads) {
-  problem_t p = {q, k, v, dtype, layout, B, H, S_q, S_kv, D, scale, dq, dk, dv, causal};
+int fa_oracle_full_gqa(const void* q, const void* k, const void* v, int dtype, int layout,
+                       int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv,
+                       int64_t D, double scale, int causal, double dq, double dk, double dv,
+                       double* O, double* lse, int n_threads) {
+  problem_t p = {q, k, v, dtype, layout, B, H, S_q, S_kv, D, scale, dq, dk, dv, causal, H_kv};
   int rc = check_problem(&p);
   if (rc) return rc;
   if (!O || !lse) return 5;
@@ -247,13 +256,13 @@ int fa_oracle_full(const void* q, const void* k, const void* v, int dtype, int l
   if (n_threads > 0) omp_set_num_threads(n_threads);
 #endif
   for (int64_t bh = 0; bh < B * H && !bad; ++bh) {
-    const int64_t b = bh / H, h = bh % H;
+    const int64_t b = bh / H, h = bh % H, hk = h / (H / H_kv);
 #ifdef _OPENMP
 #pragma omp parallel for schedule(static)
 #endif
     for (int64_t j = 0; j < S_kv; ++j) {
-      load_row(&p, k, S_kv, dk, b, h, j, kd + j * D);
-      load_row(&p, v, S_kv, dv, b, h, j, vd + j * D);
+      load_row(&p, k, H_kv, S_kv, dk, b, hk, j, kd + j * D);
+      load_row(&p, v, H_kv, S_kv, dv, b, hk, j, vd + j * D);
     }
 #ifdef _OPENMP
 #pragma omp parallel
@@ -272,7 +281,7 @@ int fa_oracle_full(const void* q, const void* k, const void* v, int dtype, int l
 #pragma omp for schedule(dynamic, 4)
 #endif
         for (int64_t i = 0; i < S_q; ++i) {
-          load_row(&p, q, S_q, dq, b, h, i, qrow);
+          load_row(&p, q, H, S_q, dq, b, h, i, qrow);
           attend_row(&p, qrow, kd, vd, i, Srow, Prow, O + (bh * S_q + i) * D, lse + bh * S_q + i);
         }
       }
@@ -281,6 +290,24 @@ int fa_oracle_full(const void* q, const void* k, const void* v, int dtype, int l
   }
   free(kd); free(vd);
   return bad ? 7 : 0;
+}
+
+/* Multi-head attention: the grouped entry points with H_kv = H. */
+int fa_oracle_rows(const void* q, const void* k, const void* v, int dtype, int layout,
+                   int64_t B, int64_t H, int64_t S_q, int64_t S_kv, int64_t D,
+                   double scale, int causal, double dq, double dk, double dv,
+                   int64_t n_rows, const int64_t* rows, double* O, double* lse,
+                   double* P, int n_threads) {
+  return fa_oracle_rows_gqa(q, k, v, dtype, layout, B, H, H, S_q, S_kv, D, scale, causal, dq, dk,
+                            dv, n_rows, rows, O, lse, P, n_threads);
+}
+
+int fa_oracle_full(const void* q, const void* k, const void* v, int dtype, int layout,
+                   int64_t B, int64_t H, int64_t S_q, int64_t S_kv, int64_t D,
+                   double scale, int causal, double dq, double dk, double dv,
+                   double* O, double* lse, int n_threads) {
+  return fa_oracle_full_gqa(q, k, v, dtype, layout, B, H, H, S_q, S_kv, D, scale, causal, dq, dk,
+                            dv, O, lse, n_threads);
 }
 
 /* Threads an OpenMP region would use (1 without OpenMP). */

@@ -47,10 +47,17 @@ class Run:
         if w.dtype == "e4m3" and descale is not None:
             self._ds = [torch.tensor([d], dtype=torch.float32, device=dev) for d in descale]
             ds = [t.data_ptr() for t in self._ds]
-        self.status = binding.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), self.o.data_ptr(),
-                                     self.lse.data_ptr(), w.B, w.H, w.S_q, w.S_kv, w.D,
-                                     w.softmax_scale, w.layout, w.causal, w.dtype, ds[0], ds[1],
-                                     ds[2], stream)
+        if w.kv_heads == w.H:
+            self.status = binding.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                         self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H, w.S_q,
+                                         w.S_kv, w.D, w.softmax_scale, w.layout, w.causal, w.dtype,
+                                         ds[0], ds[1], ds[2], stream)
+        else:
+            self.status = binding.fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                             self.o.data_ptr(), self.lse.data_ptr(), w.B, w.H,
+                                             w.kv_heads, w.S_q, w.S_kv, w.D, w.softmax_scale,
+                                             w.layout, w.causal, w.dtype, ds[0], ds[1], ds[2],
+                                             stream)
         self.device_status = binding.fa_last_device_error(stream)
 
     def guards_intact(self) -> bool:
@@ -69,7 +76,7 @@ def compare_full(w: Workload, r: Run, x):
     """Every row against the oracle; returns (max err O, max err lse)."""
     O, lse = oracle.attention_full(x.q, x.k, x.v, dtype=w.dtype, layout=w.layout, B=w.B, H=w.H,
                                    S_q=w.S_q, S_kv=w.S_kv, D=w.D, scale=w.softmax_scale,
-                                   causal=w.causal, descale=x.descale)
+                                   causal=w.causal, descale=x.descale, H_kv=w.kv_heads)
     og = r.o_bnsd64()
     lg = r.lse.cpu().double().numpy()
     return float(np.abs(og - O).max()), float(np.abs(lg - lse).max()), og, lg
@@ -99,12 +106,14 @@ def sampled_rows_check(w: Workload, r: Run, q, k, v, descale, rows):
     """Oracle on selected (b, h, i) rows using host copies of that head only."""
     err_o = err_l = 0.0
     og_all = []
+    g = w.H // w.kv_heads
     for (b, h, i) in rows:
+        hk = h // g   # key/value head of query head h
         if w.layout == "BNSD":
-            qh, kh, vh = q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu()
+            qh, kh, vh = q[b, h].cpu(), k[b, hk].cpu(), v[b, hk].cpu()
             o_row = r.o[b, h, i].float().cpu().double().numpy()
         else:
-            qh, kh, vh = q[b, :, h].cpu(), k[b, :, h].cpu(), v[b, :, h].cpu()
+            qh, kh, vh = q[b, :, h].cpu(), k[b, :, hk].cpu(), v[b, :, hk].cpu()
             o_row = r.o[b, i, h].float().cpu().double().numpy()
         O, lse = oracle.attention_rows(qh, kh, vh, dtype=w.dtype, layout="BNSD", B=1, H=1,
                                        S_q=w.S_q, S_kv=w.S_kv, D=w.D, scale=w.softmax_scale,

@@ -75,3 +75,19 @@ def test_loads_without_gpu_and_does_not_fallback():
     src = open(os.path.join(ROOT, "tiled_attention_10_gb300", "binding.py")).read()
     assert "oracle" not in src
     assert "scaled_dot_product_attention" not in src
+
+
+def _call_gqa(**over):
+    a = dict(GOOD, H=4, H_kv=2)
+    a.update(over)
+    return binding.fa_fwd_gqa(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["H_kv"],
+                              a["S_q"], a["S_kv"], a["D"], a["scale"], a["layout"], a["causal"],
+                              a["dtype"], None, None, None, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(H_kv=0), 1), (dict(H_kv=3), 1), (dict(H=4, H_kv=8), 1), (dict(q=None), 1),
+    (dict(D=80), 2), (dict(k=40), 3),
+])
+def test_gqa_invalid_arguments_rejected_on_host(lib, over, code):
+    assert _call_gqa(**over) == code

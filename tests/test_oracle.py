@@ -326,3 +326,54 @@ def test_argument_errors():
     with pytest.raises(ValueError):
         oracle.attention_rows(z, z, z, dtype="bf16", layout="BNSD", B=1, H=1, S_q=2, S_kv=2,
                               D=4, scale=1.0, causal=False, rows=[(0, 0, 2)])
+
+
+# ---------------------------------------------------------------------------
+# Grouped-query attention: query head h reads key/value head h // (H // H_kv)
+# (Q viewed as [.., H_kv, ngroups, D], the Hygon retrospective, defect 12).
+# ---------------------------------------------------------------------------
+GQA_CASES = [
+    # B, H, H_kv, S_q, S_kv, D, dtype, layout, causal
+    (1, 4, 2, 7, 9, 8, "bf16", "BNSD", False),
+    (2, 6, 3, 11, 11, 16, "f16", "BSND", True),
+    (1, 8, 1, 5, 13, 4, "bf16", "BSND", False),
+    (2, 4, 4, 9, 6, 8, "bf16", "BNSD", True),
+]
+
+
+@pytest.mark.parametrize("B,H,H_kv,S_q,S_kv,D,dtype,layout,causal", GQA_CASES)
+def test_gqa_matches_torch_sdpa_enable_gqa(B, H, H_kv, S_q, S_kv, D, dtype, layout, causal):
+    w = Workload("t", B, H, S_q, S_kv, D, dtype, layout, causal, seed=H * 10 + H_kv, H_kv=H_kv)
+    x = make_inputs(w)
+    O, lse = oracle.attention_full(x.q, x.k, x.v, dtype=dtype, layout=layout, B=B, H=H,
+                                   H_kv=H_kv, S_q=S_q, S_kv=S_kv, D=D, scale=w.softmax_scale,
+                                   causal=causal)
+    q, k, v = (_bnsd64(t, layout) for t in (x.q, x.k, x.v))
+    ref = F.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=w.softmax_scale,
+                                         enable_gqa=True).numpy()
+    np.testing.assert_allclose(O, ref, rtol=0, atol=1e-12)
+    kr = k.repeat_interleave(H // H_kv, dim=1)
+    s = w.softmax_scale * (q @ kr.transpose(-1, -2))
+    if causal:
+        s = s.masked_fill(torch.ones(S_q, S_kv, dtype=torch.bool).triu(1), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_gqa_head_mapping_is_floor_division():
+    # K/V heads with constant, distinct values: query head h must see value h // 3.
+    B, H, H_kv, S, D = 1, 6, 2, 4, 4
+    q = torch.zeros(B, H, S, D, dtype=torch.bfloat16)
+    k = torch.zeros(B, H_kv, S, D, dtype=torch.bfloat16)
+    v = torch.stack([torch.full((S, D), float(c + 1)) for c in range(H_kv)]).unsqueeze(0)
+    v = v.to(torch.bfloat16)
+    O, _ = oracle.attention_full(q, k, v, dtype="bf16", layout="BNSD", B=B, H=H, H_kv=H_kv,
+                                 S_q=S, S_kv=S, D=D, scale=1.0, causal=False)
+    for h in range(H):
+        assert (O[0, h] == float(h // 3 + 1)).all()
+
+
+def test_gqa_rejects_non_multiple_heads():
+    z = np.zeros(64, np.uint16)
+    with pytest.raises(ValueError):
+        oracle.attention_rows(z, z, z, dtype="bf16", layout="BNSD", B=1, H=3, H_kv=2, S_q=1,
+                              S_kv=1, D=4, scale=1.0, causal=False, rows=[(0, 0, 0)])

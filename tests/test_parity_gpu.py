@@ -71,3 +71,15 @@ def test_many_units_persistent_schedule(cuda_lib):
     """More units than SMs: every CTA walks several units."""
     w = Workload("t", 4, 40, 256, 256, 64, "bf16", "BNSD", True, seed=6)
     run_small(w)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "e4m3"])
+@pytest.mark.parametrize("layout", ["BNSD", "BSND"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,H_kv", [(4, 2), (8, 1), (6, 3), (4, 4)])
+def test_parity_gqa(H, H_kv, causal, layout, dtype, cuda_lib):
+    """Grouped-query attention: query head h reads key/value head h // (H // H_kv)."""
+    D = 128 if dtype == "e4m3" else 64
+    w = Workload("t", 2, H, 300, 257, D, dtype, layout, causal, seed=H * 7 + H_kv, H_kv=H_kv,
+                 poison=(layout == "BSND"))
+    run_small(w)

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from tiled_attention_10_gb300.inputs import WORKLOADS, make_inputs, sample_rows
+from tiled_attention_10_gb300.inputs import EXTRA_WORKLOADS, WORKLOADS, make_inputs, sample_rows
 from tests.gpu_helpers import TOL_LSE, TOL_O, Run, check, compare_full, sampled_rows_check, to_device
 
 pytestmark = pytest.mark.gpu
@@ -97,4 +97,17 @@ def test_workload_over_4gb_causal(cuda_lib):
     # the last head's last rows live beyond byte offset 2^32 of every tensor
     tail = [(w.B - 1, w.H - 1, i) for i in (w.S_q - 1, w.S_q - 128, w.S_q - 129)]
     eo, el = sampled_rows_check(w, r, x.q, x.k, x.v, x.descale, tail)
+    assert eo <= TOL_O[w.dtype] and el <= TOL_LSE, (eo, el)
+
+
+@pytest.mark.parametrize("name", sorted(EXTRA_WORKLOADS))
+def test_gqa_workloads_sampled(name, cuda_lib):
+    w = EXTRA_WORKLOADS[name]
+    x = make_inputs(w, device="cuda")
+    r = Run(w, x.q, x.k, x.v)
+    torch.cuda.synchronize()
+    assert r.status == 0 and r.device_status == 0 and r.guards_intact()
+    assert _whole_output_finite(r)
+    eo, el = sampled_rows_check(w, r, x.q, x.k, x.v, x.descale, _edge_rows(w, 96, seed=2))
+    print(f"{name}: max|dO|={eo:.3g} max|dlse|={el:.3g}")
     assert eo <= TOL_O[w.dtype] and el <= TOL_LSE, (eo, el)

@@ -18,7 +18,7 @@ FA_STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
              3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
 # Symbols the header declares; the library must export all of them.
-EXPORTS = ("fa_fwd", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
+EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
            "fa_probe_wait_timeout", "fa_version")
 
 _lib = None
@@ -44,6 +44,9 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, ip, ip, ip,
                            vp, vp, vp, vp]
     lib.fa_fwd.restype = ip
+    lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, ip, ip, ip,
+                               vp, vp, vp, vp]
+    lib.fa_fwd_gqa.restype = ip
     lib.fa_status_string.argtypes = [ip]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_device_error.argtypes = [vp]
@@ -76,6 +79,18 @@ def fa_fwd(q, k, v, o, lse, B, H, S_q, S_kv, D, scale, layout, causal, dtype,
                           descale_v, stream))
 
 
+def fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout, causal, dtype,
+               descale_q=None, descale_k=None, descale_v=None, stream=None) -> int:
+    """Grouped-query variant: k and v have H_kv heads (query head h reads
+    key/value head h // (H // H_kv)).  Returns the fa_status_t code."""
+    lib = load()
+    lay = FA_LAYOUT[layout] if isinstance(layout, str) else int(layout)
+    dt = FA_DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
+    return int(lib.fa_fwd_gqa(q, k, v, o, lse, int(B), int(H), int(H_kv), int(S_q), int(S_kv),
+                              int(D), float(scale), lay, int(bool(causal)), dt, descale_q,
+                              descale_k, descale_v, stream))
+
+
 def fa_last_device_error(stream=None) -> int:
     return int(load().fa_last_device_error(stream))
 
@@ -94,7 +109,8 @@ def fa_probe_wait_timeout(limit_ns: int, stream=None) -> int:
 # --------------------------------------------------------------------------
 def attention(q, k, v, *, causal=False, scale=None, layout="BNSD", descale=None,
               out=None, lse=None, stream=None):
-    """O, lse = attention(q, k, v): q/k/v torch CUDA tensors in `layout`.
+    """O, lse = attention(q, k, v): q/k/v torch CUDA tensors in `layout`
+    (k and v may have fewer heads than q: grouped-query attention).
 
     dtype follows q (float16, bfloat16 or float8_e4m3fn).  `descale` for FP8 is
     a tuple of three 1-element fp32 CUDA tensors (or None for 1.0 each).
@@ -106,10 +122,10 @@ def attention(q, k, v, *, causal=False, scale=None, layout="BNSD", descale=None,
     dtype = dmap[q.dtype]
     if layout == "BNSD":
         B, H, S_q, D = q.shape
-        S_kv = k.shape[2]
+        H_kv, S_kv = k.shape[1], k.shape[2]
     else:
         B, S_q, H, D = q.shape
-        S_kv = k.shape[1]
+        S_kv, H_kv = k.shape[1], k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     odt = torch.float16 if dtype == "f16" else torch.bfloat16
@@ -122,8 +138,9 @@ def attention(q, k, v, *, causal=False, scale=None, layout="BNSD", descale=None,
         ds = [None if t is None else t.data_ptr() for t in descale]
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
-    st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
-                S_q, S_kv, D, scale, layout, causal, dtype, ds[0], ds[1], ds[2], stream)
+    st = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B,
+                    H, H_kv, S_q, S_kv, D, scale, layout, causal, dtype, ds[0], ds[1], ds[2],
+                    stream)
     if st != 0:
         raise FaError(st, "fa_fwd")
     return out, lse

@@ -162,13 +162,15 @@ void fa_set_wait_limit_ns(uint64_t ns) {
   g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs);
 }
 
-fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
-                   int64_t H, int64_t S_q, int64_t S_kv, int64_t D, float scale,
-                   fa_layout_t layout, int causal, fa_dtype_t dtype, const float* descale_q,
-                   const float* descale_k, const float* descale_v, cudaStream_t stream) {
+fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv, int64_t D,
+                       float scale, fa_layout_t layout, int causal, fa_dtype_t dtype,
+                       const float* descale_q, const float* descale_k, const float* descale_v,
+                       cudaStream_t stream) {
   // ---- host-side checks: nothing below touches the device until they pass
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || S_q < 1 || S_kv < 1 || D < 1) return FA_ERR_INVALID_ARG;
+  if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
   if (layout != FA_LAYOUT_BNSD && layout != FA_LAYOUT_BSND) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP8E4M3)
     return FA_ERR_INVALID_ARG;
@@ -200,13 +202,14 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
   // warp's rows) x 128 bytes, written by TMA stores.
   CUtensorMap mq, mk, mv, mo;
   const fa_dtype_t odt = (dtype == FA_DTYPE_F16) ? FA_DTYPE_F16 : FA_DTYPE_BF16;
-  if (!make_map(&mq, q, dtype, layout, B, H, S_q, D) || !make_map(&mk, k, dtype, layout, B, H, S_kv, D) ||
-      !make_map(&mv, v, dtype, layout, B, H, S_kv, D) ||
+  if (!make_map(&mq, q, dtype, layout, B, H, S_q, D) || !make_map(&mk, k, dtype, layout, B, H_kv, S_kv, D) ||
+      !make_map(&mv, v, dtype, layout, B, H_kv, S_kv, D) ||
       !make_map(&mo, o, odt, layout, B, H, S_q, D, 32))
     return FA_ERR_CUDA;
 
   fa::KernelParams p = {};
   p.B = B; p.H = H; p.S_q = S_q; p.S_kv = S_kv;
+  p.kv_group = static_cast<int32_t>(H / H_kv);
   p.n_kv_blocks = static_cast<int32_t>((S_kv + 127) / 128);
   p.n_pairs = static_cast<int32_t>(n_pairs);
   p.num_units = static_cast<int32_t>(B * H * n_pairs);
@@ -214,7 +217,9 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
   // comfortably in L2 (about 48 MB); longest pairs first inside each group.
   int64_t group = 1;
   if (causal) {
-    const int64_t kv_bytes = 2 * S_kv * D * eb;
+    // K/V bytes one query head brings into L2 (a key/value head is shared
+    // by H / H_kv consecutive query heads).
+    const int64_t kv_bytes = 2 * S_kv * D * eb * H_kv / H;
     group = (48ll << 20) / (kv_bytes > 0 ? kv_bytes : 1);
     if (group < 1) group = 1;
     if (group > B * H) group = B * H;
@@ -242,6 +247,14 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
   else
     e = fa::launch_fa_fwd<128, fa::kDtE4M3>(mq, mk, mv, mo, p, grid, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                   int64_t H, int64_t S_q, int64_t S_kv, int64_t D, float scale,
+                   fa_layout_t layout, int causal, fa_dtype_t dtype, const float* descale_q,
+                   const float* descale_k, const float* descale_v, cudaStream_t stream) {
+  return fa_fwd_gqa(q, k, v, o, lse, B, H, H, S_q, S_kv, D, scale, layout, causal, dtype,
+                    descale_q, descale_k, descale_v, stream);
 }
 
 fa_status_t fa_last_device_error(cudaStream_t stream) {

@@ -70,6 +70,7 @@ constexpr int kDtF16 = 0, kDtBF16 = 1, kDtE4M3 = 2;
 
 struct KernelParams {
   int64_t B, H, S_q, S_kv;
+  int32_t kv_group;     // query heads per key/value head (1 = multi-head)
   int32_t n_kv_blocks;  // ceil(S_kv / 128)
   int32_t n_pairs;      // ceil(ceil(S_q / 128) / 2)
   int32_t num_units;    // B * H * n_pairs
@@ -198,6 +199,7 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
     int bh, pair;
     decode_unit(p, u, bh, pair);
     const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
+    const int32_t hk = h / p.kv_group;  // key/value head of query head h
     const int n0 = tile_kv_blocks(p, 2 * pair), n1 = tile_kv_blocks(p, 2 * pair + 1);
     const int nmax = max(n0, n1);
     if (!mbar_wait(bars.q_empty(), (it & 1u) ^ 1u, wc)) { ok = false; break; }
@@ -217,7 +219,7 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
         const CUtensorMap* map = kv == 0 ? tmK : tmV;
         for (int c = 0; c < C::kChunks; ++c)
           tma_tile(sRing + slot * C::kTileBytes + c * C::kChunkBytes, map, bars.full(slot),
-                   p.layout, c * C::kBoxElems, j * kBN, h, b);
+                   p.layout, c * C::kBoxElems, j * kBN, hk, b);
         ++ring;
       }
     }

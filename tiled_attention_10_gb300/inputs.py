@@ -44,6 +44,11 @@ class Workload:
     scale: Optional[float] = None   # default 1/sqrt(D)
     poison: bool = False            # NaN-poisoned memory past the valid rows
     seed: int = 0
+    H_kv: Optional[int] = None      # key/value heads (grouped-query attention); default H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.H_kv is None else self.H_kv
 
     @property
     def softmax_scale(self) -> float:
@@ -56,7 +61,8 @@ class Workload:
         return f / 2 if self.causal else f
 
     def describe(self) -> dict:
-        return {"workload": self.name, "B": self.B, "H": self.H, "S_q": self.S_q,
+        return {"workload": self.name, "B": self.B, "H": self.H, "H_kv": self.kv_heads,
+                "S_q": self.S_q,
                 "S_kv": self.S_kv, "D": self.D, "dtype": self.dtype, "layout": self.layout,
                 "causal": self.causal, "scale": self.softmax_scale,
                 "values": f"iid N(0,{self.std}^2), seed {self.seed}"
@@ -79,6 +85,16 @@ WORKLOADS = {
                                             16384, 128, "bf16", "BNSD", True, std=0.5),
 }
 HEADLINE = "bf16_4x32x4096x128"
+
+# Further workloads for the steps beyond the measured five (same recipe).
+EXTRA_WORKLOADS = {
+    # grouped-query attention: 32 query heads on 8 key/value heads
+    "bf16_gqa_4x32kv8x4096x128": Workload("bf16_gqa_4x32kv8x4096x128", 4, 32, 4096, 4096, 128,
+                                          "bf16", "BNSD", False, H_kv=8),
+    "bf16_gqa_causal_1x64kv8x8192x128": Workload("bf16_gqa_causal_1x64kv8x8192x128", 1, 64, 8192,
+                                                 8192, 128, "bf16", "BSND", True, H_kv=8),
+}
+ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
 
 
 def shape_of(layout: str, B: int, H: int, S: int, D: int):
@@ -132,14 +148,14 @@ class Inputs:
 def make_inputs(w: Workload, device="cpu", pad_rows: int = 128) -> Inputs:
     """Draw Q, K, V for workload `w` (seeds 3*seed + 0/1/2) on `device`."""
     qs = shape_of(w.layout, w.B, w.H, w.S_q, w.D)
-    ks = shape_of(w.layout, w.B, w.H, w.S_kv, w.D)
+    ks = shape_of(w.layout, w.B, w.kv_heads, w.S_kv, w.D)
     tensors, descales, bufs = [], [], []
     for i, shp in enumerate((qs, ks, ks)):
         x32 = _draw(shp, w.std, 3 * w.seed + i, device)
         x, ds = _cast(x32, w.dtype)
         del x32
         if w.poison:
-            pad = pad_rows * w.H * w.D
+            pad = pad_rows * (w.H if i == 0 else w.kv_heads) * w.D
             buf, view = poisoned_like(shp, w.dtype, device, pad)
             view.copy_(x)
             x = view
