@@ -267,12 +267,25 @@ def run_ours(args, w, world, rank, local):
         ds = [t.data_ptr() for t in dst]
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
+    n_splits, ws, ws_bytes = 1, None, 0
+    if w.split:   # split-KV: plan once, workspace allocated outside the timed region
+        st, n_splits, ws_bytes = binding.fa_fwd_splitkv_plan(w.B, w.H, w.S_q, w.S_kv, w.D)
+        if st != 0:
+            raise RuntimeError("fa_fwd_splitkv_plan failed")
+        ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    launches_per_step = 2 if n_splits > 1 else 1
 
     def step(qq=q, kk=k, vv=v):
-        st = binding.fa_fwd_gqa(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
-                                lse.data_ptr(), w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D,
-                                w.softmax_scale, w.layout, w.causal, w.dtype, ds[0], ds[1],
-                                ds[2], sp)
+        if w.split:
+            st = binding.fa_fwd_splitkv(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
+                                        lse.data_ptr(), w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D,
+                                        w.softmax_scale, w.layout, w.causal, w.dtype, ds[0],
+                                        ds[1], ds[2], n_splits, ws.data_ptr(), ws_bytes, sp)
+        else:
+            st = binding.fa_fwd_gqa(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D,
+                                    w.softmax_scale, w.layout, w.causal, w.dtype, ds[0], ds[1],
+                                    ds[2], sp)
         if st != 0:
             raise RuntimeError(f"fa_fwd: {binding.fa_status_string(st)}")
 
@@ -347,7 +360,8 @@ def run_ours(args, w, world, rank, local):
         "config": {**w.describe(),
                    "l2": ("no flush: inputs (Q+K+V) exceed the 129 MB L2" if in_bytes > (129 << 20)
                           else "no flush: inputs fit in L2 (launch-bound workload)"),
-                   "parallelism": f"{world} independent shard(s) of B*H, one per GPU"},
+                   "parallelism": f"{world} independent shard(s) of B*H, one per GPU",
+                   **({"n_splits": n_splits} if w.split else {})},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(w.name),
@@ -355,7 +369,7 @@ def run_ours(args, w, world, rank, local):
                                     f"{' x2 (fp8 nominal ratio)' if w.dtype == 'e4m3' else ''}"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

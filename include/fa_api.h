@@ -22,6 +22,7 @@
 #ifndef FA_API_H
 #define FA_API_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -106,6 +107,42 @@ fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
                        float scale, fa_layout_t layout, int causal, fa_dtype_t dtype,
                        const float* descale_q, const float* descale_k, const float* descale_v,
                        cudaStream_t stream);
+
+/*
+ * Split-KV ("flash-decoding") forward pass, for problems whose
+ * batch x heads x query tiles cannot fill the GPU (few heads, short queries,
+ * long keys).  Each query tile's keys are cut into n_splits chunks processed
+ * in parallel; every chunk writes its normalised fp32 partial O and partial
+ * log-sum-exp to `workspace`, and a second kernel merges them:
+ *     lse = log sum_s exp(lse_s),   O = sum_s exp(lse_s - lse) O_s.
+ * This is the partition-and-reduce of the paged-decode kernels in the Hygon
+ * retrospective (defect 7: per-partition exp_sums / max_logits, then a reduce
+ * kernel); the result is the same attention as fa_fwd_gqa.
+ *
+ * fa_fwd_splitkv_plan -- picks n_splits for the current device (about two
+ *   waves of work items, at least two 128-key blocks per split, at most 32;
+ *   1 when the problem already fills the GPU) and the workspace it needs
+ *   (0 when n_splits == 1).  Host only; FA_ERR_INVALID_ARG on bad sizes or
+ *   NULL outputs, FA_ERR_CUDA if the device cannot be queried.
+ *
+ * fa_fwd_splitkv -- arguments as fa_fwd_gqa, plus n_splits (1..32; 1 runs
+ *   fa_fwd_gqa and ignores the workspace) and a caller-owned device
+ *   workspace of at least the planned bytes, 256-byte aligned (fp32 partial
+ *   O [n_splits, B, H, S_q, D], then fp32 partial lse [n_splits, B, H, S_q]).
+ *   FA_ERR_INVALID_ARG: n_splits < 1, workspace NULL or too small;
+ *   FA_ERR_MISALIGNED: workspace not 256-byte aligned; FA_ERR_UNSUPPORTED:
+ *   n_splits > 32.  Two launches on `stream`; the workspace is read and
+ *   written by both, so calls sharing one workspace must not overlap.
+ */
+fa_status_t fa_fwd_splitkv_plan(int64_t B, int64_t H, int64_t S_q, int64_t S_kv, int64_t D,
+                                int* n_splits, size_t* workspace_bytes);
+
+fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv,
+                           int64_t D, float scale, fa_layout_t layout, int causal,
+                           fa_dtype_t dtype, const float* descale_q, const float* descale_k,
+                           const float* descale_v, int n_splits, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
 
 /* A static, human-readable name for a status code (never NULL). */
 const char* fa_status_string(fa_status_t s);

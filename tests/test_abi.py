@@ -91,3 +91,15 @@ def _call_gqa(**over):
 ])
 def test_gqa_invalid_arguments_rejected_on_host(lib, over, code):
     assert _call_gqa(**over) == code
+
+
+def test_splitkv_host_checks(lib):
+    # fake pointers, never dereferenced: each case fails before any CUDA call
+    base = (16, 32, 48, 64, 80, 1, 2, 2, 8, 512, 128, 0.1, "BNSD", 0, "bf16", None, None, None)
+    assert binding.fa_fwd_splitkv(*base, 0, 4096, 1 << 20) == 1        # n_splits < 1
+    assert binding.fa_fwd_splitkv(*base, 64, 4096, 1 << 20) == 2       # too many splits
+    assert binding.fa_fwd_splitkv(*base, 4, None, 1 << 20) == 1        # no workspace
+    assert binding.fa_fwd_splitkv(*base, 4, 4096, 8) == 1              # too small
+    assert binding.fa_fwd_splitkv(*base, 4, 4112, 1 << 20) == 3        # not 256-aligned
+    bad = (16, 32, 48, 64, 80, 1, 3, 2, 8, 512, 128, 0.1, "BNSD", 0, "bf16", None, None, None)
+    assert binding.fa_fwd_splitkv(*bad, 4, 4096, 1 << 20) == 1         # H % H_kv != 0

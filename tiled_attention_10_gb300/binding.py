@@ -18,7 +18,7 @@ FA_STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
              3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
 # Symbols the header declares; the library must export all of them.
-EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
+EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
            "fa_probe_wait_timeout", "fa_version")
 
 _lib = None
@@ -47,6 +47,13 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, ip, ip, ip,
                                vp, vp, vp, vp]
     lib.fa_fwd_gqa.restype = ip
+    sz = ctypes.c_size_t
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, ip, ip,
+                                   ip, vp, vp, vp, ip, vp, sz, vp]
+    lib.fa_fwd_splitkv.restype = ip
+    lib.fa_fwd_splitkv_plan.argtypes = [i64, i64, i64, i64, i64, ctypes.POINTER(ip),
+                                        ctypes.POINTER(sz)]
+    lib.fa_fwd_splitkv_plan.restype = ip
     lib.fa_status_string.argtypes = [ip]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_device_error.argtypes = [vp]
@@ -89,6 +96,29 @@ def fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout, causal,
     return int(lib.fa_fwd_gqa(q, k, v, o, lse, int(B), int(H), int(H_kv), int(S_q), int(S_kv),
                               int(D), float(scale), lay, int(bool(causal)), dt, descale_q,
                               descale_k, descale_v, stream))
+
+
+def fa_fwd_splitkv_plan(B, H, S_q, S_kv, D):
+    """(status, n_splits, workspace_bytes) chosen for the current device."""
+    lib = load()
+    n = ctypes.c_int(0)
+    nb = ctypes.c_size_t(0)
+    st = int(lib.fa_fwd_splitkv_plan(int(B), int(H), int(S_q), int(S_kv), int(D),
+                                     ctypes.byref(n), ctypes.byref(nb)))
+    return st, int(n.value), int(nb.value)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout, causal, dtype,
+                   descale_q, descale_k, descale_v, n_splits, workspace, workspace_bytes,
+                   stream=None) -> int:
+    """Split-KV forward: partials in the caller's workspace, then the merge."""
+    lib = load()
+    lay = FA_LAYOUT[layout] if isinstance(layout, str) else int(layout)
+    dt = FA_DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
+    return int(lib.fa_fwd_splitkv(q, k, v, o, lse, int(B), int(H), int(H_kv), int(S_q),
+                                  int(S_kv), int(D), float(scale), lay, int(bool(causal)), dt,
+                                  descale_q, descale_k, descale_v, int(n_splits), workspace,
+                                  int(workspace_bytes), stream))
 
 
 def fa_last_device_error(stream=None) -> int:

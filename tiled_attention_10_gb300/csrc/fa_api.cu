@@ -21,24 +21,25 @@
 #include <mutex>
 
 #include "../../include/fa_api.h"
+#include "fa_combine.cuh"
 #include "fa_kernel.cuh"
 
 namespace fa {
 // Explicit instantiations live in fa_inst_*.cu (compiled in parallel).
 extern template cudaError_t launch_fa_fwd<64, kDtF16>(const CUtensorMap&, const CUtensorMap&,
-                                                       const CUtensorMap&, const CUtensorMap&, const KernelParams&,
+                                                       const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&,
                                                        int, cudaStream_t);
 extern template cudaError_t launch_fa_fwd<128, kDtF16>(const CUtensorMap&, const CUtensorMap&,
-                                                        const CUtensorMap&, const CUtensorMap&, const KernelParams&,
+                                                        const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&,
                                                         int, cudaStream_t);
 extern template cudaError_t launch_fa_fwd<64, kDtBF16>(const CUtensorMap&, const CUtensorMap&,
-                                                        const CUtensorMap&, const CUtensorMap&, const KernelParams&,
+                                                        const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&,
                                                         int, cudaStream_t);
 extern template cudaError_t launch_fa_fwd<128, kDtBF16>(const CUtensorMap&, const CUtensorMap&,
-                                                         const CUtensorMap&, const CUtensorMap&, const KernelParams&,
+                                                         const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&,
                                                          int, cudaStream_t);
 extern template cudaError_t launch_fa_fwd<128, kDtE4M3>(const CUtensorMap&, const CUtensorMap&,
-                                                         const CUtensorMap&, const CUtensorMap&, const KernelParams&,
+                                                         const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&,
                                                          int, cudaStream_t);
 }  // namespace fa
 
@@ -122,6 +123,22 @@ bool make_map(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, fa_layout_t lay
   return r == CUDA_SUCCESS;
 }
 
+// fp32 partial-O map: [n, H, S, D] with n = n_splits * B, boxes of 32 rows x
+// 32 columns (128 bytes), 128-byte swizzle.
+bool make_map_f32(CUtensorMap* m, const void* ptr, int64_t n, int64_t H, int64_t S, int64_t D) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(n)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D * 4), static_cast<cuuint64_t>(S * D * 4),
+                           static_cast<cuuint64_t>(H * S * D * 4)};
+  cuuint32_t box[4] = {32, 32, 1, 1}, estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 __global__ void fa_wait_probe_kernel(uint32_t* err, uint64_t limit_ns) {
@@ -162,11 +179,15 @@ void fa_set_wait_limit_ns(uint64_t ns) {
   g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs);
 }
 
-fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+}  // extern "C"
+
+namespace {
+
+// Checks shared by every forward entry point (all before any CUDA call).
+fa_status_t check_args(const void* q, const void* k, const void* v, const void* o, const float* lse,
                        int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv, int64_t D,
-                       float scale, fa_layout_t layout, int causal, fa_dtype_t dtype,
-                       const float* descale_q, const float* descale_k, const float* descale_v,
-                       cudaStream_t stream) {
+                       float scale, fa_layout_t layout, fa_dtype_t dtype, const float* descale_q,
+                       const float* descale_k, const float* descale_v) {
   // ---- host-side checks: nothing below touches the device until they pass
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || S_q < 1 || S_kv < 1 || D < 1) return FA_ERR_INVALID_ARG;
@@ -194,7 +215,28 @@ fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
   const int64_t max_s = S_q > S_kv ? S_q : S_kv;
   if ((double)H * (double)max_s * (double)D * (double)eb >= 1099511627776.0)
     return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
 
+constexpr int kMaxSplits = 32;
+
+// Workspace of a split run: fp32 partial O [n_splits, B, H, S_q, D], then fp32
+// partial lse [n_splits, B, H, S_q]; each part 256-byte aligned.
+size_t split_workspace_bytes(int64_t B, int64_t H, int64_t S_q, int64_t D, int n_splits) {
+  const size_t rows = static_cast<size_t>(n_splits) * B * H * S_q;
+  const size_t o_bytes = (rows * D * 4 + 255) / 256 * 256;
+  return o_bytes + (rows * 4 + 255) / 256 * 256;
+}
+
+// The forward pass, whole (n_splits = 1: o / lse written directly) or split
+// over the keys (n_splits > 1: partials in `workspace`, then the merge).
+fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv, int64_t D,
+                        float scale, fa_layout_t layout, int causal, fa_dtype_t dtype,
+                        const float* descale_q, const float* descale_k, const float* descale_v,
+                        int n_splits, void* workspace, cudaStream_t stream) {
+  const int64_t eb = (dtype == FA_DTYPE_FP8E4M3) ? 1 : 2;
+  const int64_t n_pairs = ((S_q + 127) / 128 + 1) / 2;
   DeviceInfo dev;
   if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
 
@@ -206,13 +248,26 @@ fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
       !make_map(&mv, v, dtype, layout, B, H_kv, S_kv, D) ||
       !make_map(&mo, o, odt, layout, B, H, S_q, D, 32))
     return FA_ERR_CUDA;
+  // Split partials: fp32 [n_splits * B, H, S_q, D] (BNSD), boxes of 32 rows x
+  // 32 fp32 columns.
+  CUtensorMap mop = mo;
+  float* o_part = nullptr;
+  float* lse_part = nullptr;
+  if (n_splits > 1) {
+    o_part = static_cast<float*>(workspace);
+    const size_t rows = static_cast<size_t>(n_splits) * B * H * S_q;
+    lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * D * 4 + 255) / 256 * 256);
+    if (!make_map_f32(&mop, o_part, n_splits * B, H, S_q, D)) return FA_ERR_CUDA;
+  }
 
   fa::KernelParams p = {};
   p.B = B; p.H = H; p.S_q = S_q; p.S_kv = S_kv;
   p.kv_group = static_cast<int32_t>(H / H_kv);
   p.n_kv_blocks = static_cast<int32_t>((S_kv + 127) / 128);
   p.n_pairs = static_cast<int32_t>(n_pairs);
-  p.num_units = static_cast<int32_t>(B * H * n_pairs);
+  p.num_units = static_cast<int32_t>(B * H * n_pairs * n_splits);
+  p.n_splits = n_splits;
+  p.lse_part = lse_part;
   // Causal: group heads so that the K/V of the heads in flight together fit
   // comfortably in L2 (about 48 MB); longest pairs first inside each group.
   int64_t group = 1;
@@ -239,14 +294,86 @@ fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
   const int grid = static_cast<int>(p.num_units < dev.sm_count ? p.num_units : dev.sm_count);
   cudaError_t e;
   if (dtype == FA_DTYPE_F16)
-    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtF16>(mq, mk, mv, mo, p, grid, stream)
-                  : fa::launch_fa_fwd<128, fa::kDtF16>(mq, mk, mv, mo, p, grid, stream);
+    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtF16>(mq, mk, mv, mo, mop, p, grid, stream)
+                  : fa::launch_fa_fwd<128, fa::kDtF16>(mq, mk, mv, mo, mop, p, grid, stream);
   else if (dtype == FA_DTYPE_BF16)
-    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtBF16>(mq, mk, mv, mo, p, grid, stream)
-                  : fa::launch_fa_fwd<128, fa::kDtBF16>(mq, mk, mv, mo, p, grid, stream);
+    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtBF16>(mq, mk, mv, mo, mop, p, grid, stream)
+                  : fa::launch_fa_fwd<128, fa::kDtBF16>(mq, mk, mv, mo, mop, p, grid, stream);
   else
-    e = fa::launch_fa_fwd<128, fa::kDtE4M3>(mq, mk, mv, mo, p, grid, stream);
-  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    e = fa::launch_fa_fwd<128, fa::kDtE4M3>(mq, mk, mv, mo, mop, p, grid, stream);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if (n_splits > 1) {
+    fa::CombineParams c = {};
+    c.o_part = o_part;
+    c.lse_part = lse_part;
+    c.o = o;
+    c.lse = lse;
+    c.B = B; c.H = H; c.S_q = S_q;
+    c.D = static_cast<int32_t>(D);
+    c.n_splits = n_splits;
+    c.layout = static_cast<int32_t>(layout);
+    c.out_f16 = dtype == FA_DTYPE_F16 ? 1 : 0;
+    if (fa::launch_fa_combine(c, dev.sm_count, stream) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv, int64_t D,
+                       float scale, fa_layout_t layout, int causal, fa_dtype_t dtype,
+                       const float* descale_q, const float* descale_k, const float* descale_v,
+                       cudaStream_t stream) {
+  const fa_status_t st = check_args(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout,
+                                    dtype, descale_q, descale_k, descale_v);
+  if (st != FA_OK) return st;
+  return run_forward(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout, causal, dtype,
+                     descale_q, descale_k, descale_v, 1, nullptr, stream);
+}
+
+fa_status_t fa_fwd_splitkv_plan(int64_t B, int64_t H, int64_t S_q, int64_t S_kv, int64_t D,
+                                int* n_splits, size_t* workspace_bytes) {
+  if (!n_splits || !workspace_bytes) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S_q < 1 || S_kv < 1 || D < 1) return FA_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
+  const int64_t units = B * H * (((S_q + 127) / 128 + 1) / 2);
+  const int64_t kv_blocks = (S_kv + 127) / 128;
+  int64_t splits = 1;
+  if (units < dev.sm_count) {
+    splits = (2 * dev.sm_count + units - 1) / units;    // about two waves of items
+    if (splits > kv_blocks / 2) splits = kv_blocks / 2;  // at least two K/V blocks per split
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    if (splits < 1) splits = 1;
+  }
+  *n_splits = static_cast<int>(splits);
+  *workspace_bytes = splits > 1 ? split_workspace_bytes(B, H, S_q, D, static_cast<int>(splits)) : 0;
+  return FA_OK;
+}
+
+fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv,
+                           int64_t D, float scale, fa_layout_t layout, int causal,
+                           fa_dtype_t dtype, const float* descale_q, const float* descale_k,
+                           const float* descale_v, int n_splits, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  const fa_status_t st = check_args(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout,
+                                    dtype, descale_q, descale_k, descale_v);
+  if (st != FA_OK) return st;
+  if (n_splits < 1) return FA_ERR_INVALID_ARG;
+  if (n_splits > kMaxSplits) return FA_ERR_UNSUPPORTED;
+  if (n_splits > 1) {
+    if (!workspace || workspace_bytes < split_workspace_bytes(B, H, S_q, D, n_splits))
+      return FA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+    if (static_cast<double>(n_splits) * B * H * S_q * ((S_q + 127) / 128) > 2e9)
+      return FA_ERR_UNSUPPORTED;
+  }
+  return run_forward(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout, causal, dtype,
+                     descale_q, descale_k, descale_v, n_splits, workspace, stream);
 }
 
 fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,

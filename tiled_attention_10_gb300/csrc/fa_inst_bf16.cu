@@ -5,10 +5,10 @@
 namespace fa {
 template cudaError_t launch_fa_fwd<64, kDtBF16>(const CUtensorMap&, const CUtensorMap&,
                                                 const CUtensorMap&, const CUtensorMap&,
-                                                const KernelParams&, int,
+                                                const CUtensorMap&, const KernelParams&, int,
                                                 cudaStream_t);
 template cudaError_t launch_fa_fwd<128, kDtBF16>(const CUtensorMap&, const CUtensorMap&,
                                                 const CUtensorMap&, const CUtensorMap&,
-                                                const KernelParams&, int,
+                                                const CUtensorMap&, const KernelParams&, int,
                                                 cudaStream_t);
 }  // namespace fa

@@ -5,6 +5,6 @@
 namespace fa {
 template cudaError_t launch_fa_fwd<128, kDtE4M3>(const CUtensorMap&, const CUtensorMap&,
                                                 const CUtensorMap&, const CUtensorMap&,
-                                                const KernelParams&, int,
+                                                const CUtensorMap&, const KernelParams&, int,
                                                 cudaStream_t);
 }  // namespace fa

@@ -17,7 +17,7 @@
  *   warps 10-11 idle
  * The launch gives every thread 168 registers (three warps share each SM
  * sub-partition's register file); the control warpgroup then hands registers
- * to the softmax warpgroups with setmaxnreg (72 / 216), so that a softmax
+ * to the softmax warpgroups with setmaxnreg (104 / 200), so that a softmax
  * thread can hold its whole 128-column score row in registers.
  *
  * Tensor memory (512 columns x 128 lanes, fp32):
@@ -61,8 +61,8 @@ namespace fa {
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // key/value rows per tile
 constexpr int kThreads = 384;
-constexpr uint32_t kRegsSoftmax = 216;  // 256 * 216 + 128 * 72 = 384 * 168
-constexpr uint32_t kRegsControl = 72;
+constexpr uint32_t kRegsSoftmax = 200;  // 256 * 200 + 128 * 104 = 384 * 168
+constexpr uint32_t kRegsControl = 104;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -73,7 +73,7 @@ struct KernelParams {
   int32_t kv_group;     // query heads per key/value head (1 = multi-head)
   int32_t n_kv_blocks;  // ceil(S_kv / 128)
   int32_t n_pairs;      // ceil(ceil(S_q / 128) / 2)
-  int32_t num_units;    // B * H * n_pairs
+  int32_t num_units;    // work items: B * H * n_pairs * n_splits
   int32_t group_heads;  // heads per scheduling group (1 = head-major order)
   int32_t layout;       // 0 BNSD, 1 BSND
   int32_t causal;
@@ -85,6 +85,8 @@ struct KernelParams {
   float* lse;
   uint32_t* err;
   uint64_t wait_limit_ns;
+  int32_t n_splits;     // K/V splits per unit (1: no split; outputs go to o / lse)
+  float* lse_part;      // split > 1: fp32 [n_splits, B, H, S_q] partial log-sum-exp
 };
 
 template <int D, int DT>
@@ -150,6 +152,30 @@ __device__ __forceinline__ int tile_kv_blocks(const KernelParams& p, int q_tile)
   return static_cast<int>(max_col / kBN) + 1;
 }
 
+// Work item u = (unit, split): the unit's K/V blocks are cut into n_splits
+// chunks of equal length; the item covers blocks [lo, lo + chunk) and tile t
+// processes n[t] of them (0: nothing for that tile).  With n_splits = 1 an
+// item is a unit and lo = 0.
+struct Item {
+  int bh, pair, split, lo;
+  int n[2];
+};
+
+__device__ __forceinline__ Item decode_item(const KernelParams& p, int u) {
+  Item it;
+  const int unit = u / p.n_splits;
+  it.split = u - unit * p.n_splits;
+  decode_unit(p, unit, it.bh, it.pair);
+  const int f0 = tile_kv_blocks(p, 2 * it.pair), f1 = tile_kv_blocks(p, 2 * it.pair + 1);
+  const int nmax = max(f0, f1);
+  const int chunk = (nmax + p.n_splits - 1) / p.n_splits;
+  it.lo = it.split * chunk;
+  const int hi = min(nmax, it.lo + chunk);
+  it.n[0] = max(0, min(f0, hi) - it.lo);
+  it.n[1] = max(0, min(f1, hi) - it.lo);
+  return it;
+}
+
 // TMA coordinates of (column c0, row s) of head (b, h): BNSD maps are
 // {D, S, H, B}, BSND maps are {D, H, S, B}.
 __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -196,12 +222,13 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
   for (int w = 0; ok; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
-    int bh, pair;
-    decode_unit(p, u, bh, pair);
+    const Item item = decode_item(p, u);
+    const int bh = item.bh, pair = item.pair;
     const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
     const int32_t hk = h / p.kv_group;  // key/value head of query head h
-    const int n0 = tile_kv_blocks(p, 2 * pair), n1 = tile_kv_blocks(p, 2 * pair + 1);
+    const int n0 = item.n[0], n1 = item.n[1];
     const int nmax = max(n0, n1);
+    if (nmax == 0) continue;            // an empty split: no MMA work
     if (!mbar_wait(bars.q_empty(), (it & 1u) ^ 1u, wc)) { ok = false; break; }
     mbar_arrive_expect_tx(bars.q_full(), (n0 > 0 ? C::kTileBytes : 0) + (n1 > 0 ? C::kTileBytes : 0));
     for (int t = 0; t < 2; ++t) {
@@ -219,7 +246,7 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
         const CUtensorMap* map = kv == 0 ? tmK : tmV;
         for (int c = 0; c < C::kChunks; ++c)
           tma_tile(sRing + slot * C::kTileBytes + c * C::kChunkBytes, map, bars.full(slot),
-                   p.layout, c * C::kBoxElems, j * kBN, hk, b);
+                   p.layout, c * C::kBoxElems, (item.lo + j) * kBN, hk, b);
         ++ring;
       }
     }
@@ -300,10 +327,10 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
   for (int w = 0; ok; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
-    int bh, pair;
-    decode_unit(p, u, bh, pair);
-    const int n[2] = {tile_kv_blocks(p, 2 * pair), tile_kv_blocks(p, 2 * pair + 1)};
+    const Item item = decode_item(p, u);
+    const int n[2] = {item.n[0], item.n[1]};
     const int nmax = max(n[0], n[1]);
+    if (nmax == 0) continue;
     if (!mbar_wait(bars.q_full(), it & 1u, wc)) { ok = false; break; }
     ++it;
     // Prologue: S_t = Q_t K_0^T for both tiles.
@@ -493,9 +520,9 @@ __device__ __forceinline__ void softmax_block(float (&s)[128], int lim, int j, f
   }}
 
 template <int D, int DT>
-__device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, uint32_t tmem,
-                           uint32_t sEpi, int warp, int lane, const Bars& bars,
-                           const WaitCtl& wc) {
+__device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, const CUtensorMap* tmOp,
+                             uint32_t tmem, uint32_t sEpi, int warp, int lane, const Bars& bars,
+                             const WaitCtl& wc) {
   using C = Cfg<D, DT>;
   const int t = warp >> 2;            // query tile of this warpgroup
   const int wq = warp & 3;            // TMEM lane quarter
@@ -503,15 +530,16 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, uint
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t tS = tmem + lane_off + C::kTmemS + t * kBN;
   const uint32_t tO = tmem + lane_off + C::kTmemO + t * 128;
+  const bool split = p.n_splits > 1;
 
   float sl2 = p.scale_log2;
   float o_mul = 1.0f;
   if constexpr (C::kFp8) {
-  const float dq = p.descale_q ? *p.descale_q : 1.0f;
-  const float dk = p.descale_k ? *p.descale_k : 1.0f;
-  const float dv = p.descale_v ? *p.descale_v : 1.0f;
-  sl2 *= dq * dk;
-  o_mul = dv * (1.0f / 256.0f);  // P is stored as 256 * p in e4m3
+    const float dq = p.descale_q ? *p.descale_q : 1.0f;
+    const float dk = p.descale_k ? *p.descale_k : 1.0f;
+    const float dv = p.descale_v ? *p.descale_v : 1.0f;
+    sl2 *= dq * dk;
+    o_mul = dv * (1.0f / 256.0f);  // P is stored as 256 * p in e4m3
   }
   // A masked score is -inf and must give p = 0: keep the base-2 scale
   // strictly positive (a zero scale or descale becomes 1e-30, which changes
@@ -521,93 +549,110 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, uint
   uint32_t s_phase = 0u, o_phase = 0u;
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0;; ++w) {
-  const int u = unit_of_round(w, grid, bid);
-  if (u >= p.num_units) break;
-  int bh, pair;
-  decode_unit(p, u, bh, pair);
-  const int q_tile = 2 * pair + t;
-  const int n = tile_kv_blocks(p, q_tile);
-  if (n == 0) continue;
-  const int64_t row = static_cast<int64_t>(q_tile) * kBM + r;
-  const int64_t col_end = p.causal ? min(row + 1, p.S_kv) : p.S_kv;  // columns < col_end visible
-  const int64_t tile_row0 = static_cast<int64_t>(q_tile) * kBM;
-
-  float m_run = -CUDART_INF_F, l = 0.0f;
-  bool ok = true;
-  for (int j = 0; j < n; ++j) {
-    if (!mbar_wait(bars.s_full(t), s_phase, wc)) { ok = false; break; }
-    s_phase ^= 1u;
-    tc_fence_after();
-    uint32_t sr[4][32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tmem_ld_x32(tS + 32 * c, sr[c]);
-    tmem_wait_ld();
-#pragma unroll
-    for (int c = 0; c < 4; ++c) reg_dep_x32(sr[c]);
-    float s[128];
-#pragma unroll
-    for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
-
-    const int64_t col0 = static_cast<int64_t>(j) * kBN;
-    // Block-uniform: does any column of this block need a mask?
-    const bool masked = (col0 + kBN > p.S_kv) || (p.causal && col0 + (kBN - 1) > tile_row0);
-    const int lim = static_cast<int>(max(min(col_end - col0, static_cast<int64_t>(kBN)), int64_t(0)));
-
-    if (masked)
-      softmax_block<D, DT, true>(s, lim, j, sl2, m_run, l, tS, tO, bars, t);
-    else
-      softmax_block<D, DT, false>(s, kBN, j, sl2, m_run, l, tS, tO, bars, t);
-  }
-  if (!ok) break;
-
-  // Epilogue: O / l -> output dtype, staged per warp (32 rows x 64 columns,
-  // 128-byte swizzle) and written by a TMA store whose tensor map clips rows
-  // >= S_q; then lse for rows < S_q.
-  if (!mbar_wait(bars.o_done(t), o_phase, wc)) break;
-  o_phase ^= 1u;
-  tc_fence_after();
-  const float inv = o_mul / l;
-  const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
-  const int32_t box_row0 = q_tile * kBM + wq * 32;
-  const uint32_t stage = sEpi + static_cast<uint32_t>(warp) * C::kEpiBoxBytes;
-#pragma unroll 1
-  for (int hh = 0; hh < D / 64; ++hh) {
-    uint32_t o0[32], o1[32];
-    tmem_ld_x32(tO + 64 * hh, o0);
-    tmem_ld_x32(tO + 64 * hh + 32, o1);
-    tmem_wait_ld();
-    reg_dep_x32(o0);
-    reg_dep_x32(o1);
-    uint32_t pk[32];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float a0 = __uint_as_float(o0[2 * i]) * inv, a1 = __uint_as_float(o0[2 * i + 1]) * inv;
-      const float c0 = __uint_as_float(o1[2 * i]) * inv, c1 = __uint_as_float(o1[2 * i + 1]) * inv;
-      pk[i] = (DT == kDtF16) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
-      pk[16 + i] = (DT == kDtF16) ? pack_f16x2(c0, c1) : pack_bf16x2(c0, c1);
+    const int u = unit_of_round(w, grid, bid);
+    if (u >= p.num_units) break;
+    const Item item = decode_item(p, u);
+    const int bh = item.bh;
+    const int q_tile = 2 * item.pair + t;
+    const int n = t ? item.n[1] : item.n[0];
+    const int64_t row = static_cast<int64_t>(q_tile) * kBM + r;
+    const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
+    // lse of this row: the final one, or this split's partial one.
+    float* lse_out = split ? p.lse_part + ((static_cast<int64_t>(item.split) * p.B + b) * p.H + h) * p.S_q
+                           : p.lse + static_cast<int64_t>(bh) * p.S_q;
+    if (n == 0) {
+      // No key of this split is visible to this tile: an empty partial,
+      // which the merge gives zero weight.
+      if (split && row < p.S_q) lse_out[row] = -CUDART_INF_F;
+      continue;
     }
-    // The previous TMA store from this staging box must have read it.
-    if (lane == 0) bulk_wait_group_read0();
-    __syncwarp();
+    const int64_t col_end = p.causal ? min(row + 1, p.S_kv) : p.S_kv;  // columns < col_end visible
+    const int64_t tile_row0 = static_cast<int64_t>(q_tile) * kBM;
+
+    float m_run = -CUDART_INF_F, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait(bars.s_full(t), s_phase, wc)) { ok = false; break; }
+      s_phase ^= 1u;
+      tc_fence_after();
+      uint32_t sr[4][32];
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      st_shared_v4(stage + lane * 128 + ((u ^ (lane & 7)) << 4), pk[4 * u], pk[4 * u + 1],
-                   pk[4 * u + 2], pk[4 * u + 3]);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0 && box_row0 < p.S_q) {  // rows past S_q are clipped by the map
-      if (p.layout == 0)
-        tma_store_4d(tmO, stage, 64 * hh, box_row0, h, b);
+      for (int c = 0; c < 4; ++c) tmem_ld_x32(tS + 32 * c, sr[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_dep_x32(sr[c]);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+
+      const int64_t col0 = static_cast<int64_t>(item.lo + j) * kBN;
+      // Block-uniform: does any column of this block need a mask?
+      const bool masked = (col0 + kBN > p.S_kv) || (p.causal && col0 + (kBN - 1) > tile_row0);
+      const int lim = static_cast<int>(max(min(col_end - col0, static_cast<int64_t>(kBN)), int64_t(0)));
+      if (masked)
+        softmax_block<D, DT, true>(s, lim, j, sl2, m_run, l, tS, tO, bars, t);
       else
-        tma_store_4d(tmO, stage, 64 * hh, h, box_row0, b);
-      bulk_commit_group();
+        softmax_block<D, DT, false>(s, kBN, j, sl2, m_run, l, tS, tO, bars, t);
     }
-  }
-  if (row < p.S_q) {
-    const float lse2 = m_run + log2f(l);
-    p.lse[static_cast<int64_t>(bh) * p.S_q + row] = lse2 * 0.69314718055994531f;
-  }
-  tc_fence_before();
+    if (!ok) break;
+
+    // Epilogue.  O / l goes through a per-warp staging box in shared memory
+    // (32 rows x 128 bytes, 128-byte swizzle) and a TMA store whose tensor
+    // map clips rows >= S_q: 64 columns of 16-bit output per box, or -- for a
+    // split -- 32 columns of the fp32 partial O per box.  Then lse.
+    if (!mbar_wait(bars.o_done(t), o_phase, wc)) break;
+    o_phase ^= 1u;
+    tc_fence_after();
+    const float inv = o_mul / l;
+    const int32_t box_row0 = q_tile * kBM + wq * 32;
+    const uint32_t stage = sEpi + static_cast<uint32_t>(warp) * C::kEpiBoxBytes;
+    const int n_boxes = split ? D / 32 : D / 64;
+#pragma unroll 1
+    for (int bx = 0; bx < n_boxes; ++bx) {
+      uint32_t pk[32];
+      if (split) {
+        uint32_t o0[32];
+        tmem_ld_x32(tO + 32 * bx, o0);
+        tmem_wait_ld();
+        reg_dep_x32(o0);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = __float_as_uint(__uint_as_float(o0[i]) * inv);
+      } else {
+        uint32_t o0[32], o1[32];
+        tmem_ld_x32(tO + 64 * bx, o0);
+        tmem_ld_x32(tO + 64 * bx + 32, o1);
+        tmem_wait_ld();
+        reg_dep_x32(o0);
+        reg_dep_x32(o1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a0 = __uint_as_float(o0[2 * i]) * inv, a1 = __uint_as_float(o0[2 * i + 1]) * inv;
+          const float c0 = __uint_as_float(o1[2 * i]) * inv, c1 = __uint_as_float(o1[2 * i + 1]) * inv;
+          pk[i] = (DT == kDtF16) ? pack_f16x2(a0, a1) : pack_bf16x2(a0, a1);
+          pk[16 + i] = (DT == kDtF16) ? pack_f16x2(c0, c1) : pack_bf16x2(c0, c1);
+        }
+      }
+      // The previous TMA store from this staging box must have read it.
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_shared_v4(stage + lane * 128 + ((q ^ (lane & 7)) << 4), pk[4 * q], pk[4 * q + 1],
+                     pk[4 * q + 2], pk[4 * q + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && box_row0 < p.S_q) {  // rows past S_q are clipped by the map
+        if (split)
+          tma_store_4d(tmOp, stage, 32 * bx, box_row0, h, item.split * static_cast<int32_t>(p.B) + b);
+        else if (p.layout == 0)
+          tma_store_4d(tmO, stage, 64 * bx, box_row0, h, b);
+        else
+          tma_store_4d(tmO, stage, 64 * bx, h, box_row0, b);
+        bulk_commit_group();
+      }
+    }
+    if (row < p.S_q) lse_out[row] = (m_run + log2f(l)) * 0.69314718055994531f;
+    tc_fence_before();
   }
   // Every TMA store of this warp has completed before the CTA exits.
   if (lane == 0) bulk_wait_group0();
@@ -621,7 +666,7 @@ template <int D, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                  const __grid_constant__ KernelParams p) {
+                  const __grid_constant__ CUtensorMap tmOp, const __grid_constant__ KernelParams p) {
   using C = Cfg<D, DT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -670,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kProducerWarp) {
     reg_alloc_inc<kRegsSoftmax>();
-    softmax_role<D, DT>(p, &tmO, tmem, sEpi, warp, lane, bars, wc);
+    softmax_role<D, DT>(p, &tmO, &tmOp, tmem, sEpi, warp, lane, bars, wc);
   } else {
     reg_alloc_dec<kRegsControl>();
     if (warp == kProducerWarp) {
@@ -691,8 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Host-side launcher, one instantiation per (D, dtype).
 template <int D, int DT>
 cudaError_t launch_fa_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& o, const KernelParams& p, int grid,
-                          cudaStream_t stream) {
+                          const CUtensorMap& o, const CUtensorMap& op, const KernelParams& p,
+                          int grid, cudaStream_t stream) {
   using C = Cfg<D, DT>;
   auto kern = fa_fwd_kernel<D, DT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -702,7 +747,7 @@ cudaError_t launch_fa_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, p);
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, op, p);
 }
 
 }  // namespace fa

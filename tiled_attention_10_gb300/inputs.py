@@ -45,6 +45,7 @@ class Workload:
     poison: bool = False            # NaN-poisoned memory past the valid rows
     seed: int = 0
     H_kv: Optional[int] = None      # key/value heads (grouped-query attention); default H
+    split: bool = False             # run through the split-KV entry point
 
     @property
     def kv_heads(self) -> int:
@@ -93,6 +94,9 @@ EXTRA_WORKLOADS = {
                                           "bf16", "BNSD", False, H_kv=8),
     "bf16_gqa_causal_1x64kv8x8192x128": Workload("bf16_gqa_causal_1x64kv8x8192x128", 1, 64, 8192,
                                                  8192, 128, "bf16", "BSND", True, H_kv=8),
+    # few heads, short queries, long keys: split-KV fills the GPU
+    "bf16_splitkv_1x8x512x16384x128": Workload("bf16_splitkv_1x8x512x16384x128", 1, 8, 512, 16384,
+                                               128, "bf16", "BNSD", False, split=True),
 }
 ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
 
