@@ -119,9 +119,10 @@ fa_status_t fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, flo
  * retrospective (defect 7: per-partition exp_sums / max_logits, then a reduce
  * kernel); the result is the same attention as fa_fwd_gqa.
  *
- * fa_fwd_splitkv_plan -- picks n_splits for the current device (about two
- *   waves of work items, at least two 128-key blocks per split, at most 32;
- *   1 when the problem already fills the GPU) and the workspace it needs
+ * fa_fwd_splitkv_plan -- picks n_splits for the current device: the count
+ *   (1..32, at least two 128-key blocks per split) that minimises waves of
+ *   work items x (blocks per item + a fixed cost of about three blocks), so
+ *   1 when the problem already fills the GPU; and the workspace it needs
  *   (0 when n_splits == 1).  Host only; FA_ERR_INVALID_ARG on bad sizes or
  *   NULL outputs, FA_ERR_CUDA if the device cannot be queried.
  *

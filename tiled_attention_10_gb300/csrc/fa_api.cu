@@ -26,21 +26,46 @@
 
 namespace fa {
 // Explicit instantiations live in fa_inst_*.cu (compiled in parallel).
-extern template cudaError_t launch_fa_fwd<64, kDtF16>(const CUtensorMap&, const CUtensorMap&,
-                                                       const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&,
-                                                       int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<128, kDtF16>(const CUtensorMap&, const CUtensorMap&,
-                                                        const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&,
-                                                        int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<64, kDtBF16>(const CUtensorMap&, const CUtensorMap&,
-                                                        const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&,
-                                                        int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<128, kDtBF16>(const CUtensorMap&, const CUtensorMap&,
-                                                         const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&,
-                                                         int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<128, kDtE4M3>(const CUtensorMap&, const CUtensorMap&,
-                                                         const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KernelParams&,
-                                                         int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<64, kDtF16, false>(const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const KernelParams&,
+                                                              int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<64, kDtF16, true>(const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const KernelParams&,
+                                                              int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<128, kDtF16, false>(const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const KernelParams&,
+                                                              int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<128, kDtF16, true>(const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const KernelParams&,
+                                                              int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<64, kDtBF16, false>(const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const KernelParams&,
+                                                              int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<64, kDtBF16, true>(const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const KernelParams&,
+                                                              int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<128, kDtBF16, false>(const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const KernelParams&,
+                                                              int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<128, kDtBF16, true>(const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const KernelParams&,
+                                                              int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<128, kDtE4M3, false>(const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const KernelParams&,
+                                                              int, cudaStream_t);
+extern template cudaError_t launch_fa_fwd<128, kDtE4M3, true>(const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const CUtensorMap&,
+                                                              const CUtensorMap&, const KernelParams&,
+                                                              int, cudaStream_t);
 }  // namespace fa
 
 // Device error word: bounded waits OR their error bits in here.
@@ -292,15 +317,18 @@ fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, fl
   p.wait_limit_ns = g_wait_limit_ns.load();
 
   const int grid = static_cast<int>(p.num_units < dev.sm_count ? p.num_units : dev.sm_count);
+  const bool sp = n_splits > 1;
   cudaError_t e;
+#define FA_LAUNCH(DD, DTY)                                                               \
+  (sp ? fa::launch_fa_fwd<DD, DTY, true>(mq, mk, mv, mo, mop, p, grid, stream)           \
+      : fa::launch_fa_fwd<DD, DTY, false>(mq, mk, mv, mo, mop, p, grid, stream))
   if (dtype == FA_DTYPE_F16)
-    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtF16>(mq, mk, mv, mo, mop, p, grid, stream)
-                  : fa::launch_fa_fwd<128, fa::kDtF16>(mq, mk, mv, mo, mop, p, grid, stream);
+    e = (D == 64) ? FA_LAUNCH(64, fa::kDtF16) : FA_LAUNCH(128, fa::kDtF16);
   else if (dtype == FA_DTYPE_BF16)
-    e = (D == 64) ? fa::launch_fa_fwd<64, fa::kDtBF16>(mq, mk, mv, mo, mop, p, grid, stream)
-                  : fa::launch_fa_fwd<128, fa::kDtBF16>(mq, mk, mv, mo, mop, p, grid, stream);
+    e = (D == 64) ? FA_LAUNCH(64, fa::kDtBF16) : FA_LAUNCH(128, fa::kDtBF16);
   else
-    e = fa::launch_fa_fwd<128, fa::kDtE4M3>(mq, mk, mv, mo, mop, p, grid, stream);
+    e = FA_LAUNCH(128, fa::kDtE4M3);
+#undef FA_LAUNCH
   if (e != cudaSuccess) return FA_ERR_CUDA;
   if (n_splits > 1) {
     fa::CombineParams c = {};
@@ -342,12 +370,17 @@ fa_status_t fa_fwd_splitkv_plan(int64_t B, int64_t H, int64_t S_q, int64_t S_kv,
   if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
   const int64_t units = B * H * (((S_q + 127) / 128 + 1) / 2);
   const int64_t kv_blocks = (S_kv + 127) / 128;
-  int64_t splits = 1;
-  if (units < dev.sm_count) {
-    splits = (2 * dev.sm_count + units - 1) / units;    // about two waves of items
-    if (splits > kv_blocks / 2) splits = kv_blocks / 2;  // at least two K/V blocks per split
-    if (splits > kMaxSplits) splits = kMaxSplits;
-    if (splits < 1) splits = 1;
+  // Waves of work items times the blocks each item walks, plus about three
+  // blocks' worth of fixed cost per item (Q load, pipeline fill, partial
+  // write); the smallest estimate wins, ties to fewer splits.
+  int64_t splits = 1, best = -1;
+  for (int64_t sp = 1; sp <= kMaxSplits && sp <= (kv_blocks > 1 ? kv_blocks / 2 : 1); ++sp) {
+    const int64_t waves = (units * sp + dev.sm_count - 1) / dev.sm_count;
+    const int64_t cost = waves * ((kv_blocks + sp - 1) / sp + 3);
+    if (best < 0 || cost < best) {
+      best = cost;
+      splits = sp;
+    }
   }
   *n_splits = static_cast<int>(splits);
   *workspace_bytes = splits > 1 ? split_workspace_bytes(B, H, S_q, D, static_cast<int>(splits)) : 0;

@@ -3,8 +3,12 @@
 #include "fa_kernel.cuh"
 
 namespace fa {
-template cudaError_t launch_fa_fwd<128, kDtE4M3>(const CUtensorMap&, const CUtensorMap&,
-                                                const CUtensorMap&, const CUtensorMap&,
-                                                const CUtensorMap&, const KernelParams&, int,
-                                                cudaStream_t);
+template cudaError_t launch_fa_fwd<128, kDtE4M3, false>(const CUtensorMap&, const CUtensorMap&,
+                                                       const CUtensorMap&, const CUtensorMap&,
+                                                       const CUtensorMap&, const KernelParams&,
+                                                       int, cudaStream_t);
+template cudaError_t launch_fa_fwd<128, kDtE4M3, true>(const CUtensorMap&, const CUtensorMap&,
+                                                       const CUtensorMap&, const CUtensorMap&,
+                                                       const CUtensorMap&, const KernelParams&,
+                                                       int, cudaStream_t);
 }  // namespace fa

@@ -17,8 +17,9 @@
  *   warps 10-11 idle
  * The launch gives every thread 168 registers (three warps share each SM
  * sub-partition's register file); the control warpgroup then hands registers
- * to the softmax warpgroups with setmaxnreg (104 / 200), so that a softmax
- * thread can hold its whole 128-column score row in registers.
+ * to the softmax warpgroups with setmaxnreg (72 / 216; 104 / 200 for the
+ * split-KV kernel), so that a softmax thread can hold its whole 128-column
+ * score row in registers.
  *
  * Tensor memory (512 columns x 128 lanes, fp32):
  *   [0,128)   S for tile 0   (P for tile 0 overwrites its first columns)
@@ -61,8 +62,15 @@ namespace fa {
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // key/value rows per tile
 constexpr int kThreads = 384;
-constexpr uint32_t kRegsSoftmax = 200;  // 256 * 200 + 128 * 104 = 384 * 168
-constexpr uint32_t kRegsControl = 104;
+// Registers per thread after setmaxnreg: softmax warpgroups / control
+// warpgroup; 256 * softmax + 128 * control = 384 * 168 (the launch budget).
+// The split-KV kernel's control roles decode more per item and need more.
+template <bool kSplit>
+struct RegSplit {
+  static constexpr uint32_t kSoftmax = kSplit ? 200 : 216;
+  static constexpr uint32_t kControl = kSplit ? 104 : 72;
+  static_assert(256 * kSoftmax + 128 * kControl == 384 * 168, "register budget");
+};
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -161,14 +169,15 @@ struct Item {
   int n[2];
 };
 
+template <bool kSplit>
 __device__ __forceinline__ Item decode_item(const KernelParams& p, int u) {
   Item it;
-  const int unit = u / p.n_splits;
-  it.split = u - unit * p.n_splits;
+  const int unit = kSplit ? u / p.n_splits : u;
+  it.split = kSplit ? u - unit * p.n_splits : 0;
   decode_unit(p, unit, it.bh, it.pair);
   const int f0 = tile_kv_blocks(p, 2 * it.pair), f1 = tile_kv_blocks(p, 2 * it.pair + 1);
   const int nmax = max(f0, f1);
-  const int chunk = (nmax + p.n_splits - 1) / p.n_splits;
+  const int chunk = kSplit ? (nmax + p.n_splits - 1) / p.n_splits : nmax;
   it.lo = it.split * chunk;
   const int hi = min(nmax, it.lo + chunk);
   it.n[0] = max(0, min(f0, hi) - it.lo);
@@ -211,7 +220,7 @@ __device__ __forceinline__ void mbar_wait_teardown(uint32_t bar, uint32_t parity
 // ---------------------------------------------------------------------------
 // Producer (one thread): Q pair, then K_0, V_0, K_1, V_1, ... into the ring.
 // ---------------------------------------------------------------------------
-template <int D, int DT>
+template <int D, int DT, bool kSplit>
 __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
                               const CUtensorMap* tmK, const CUtensorMap* tmV, uint32_t sQ,
                               uint32_t sRing, const Bars& bars, const WaitCtl& wc) {
@@ -222,7 +231,7 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
   for (int w = 0; ok; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
-    const Item item = decode_item(p, u);
+    const Item item = decode_item<kSplit>(p, u);
     const int bh = item.bh, pair = item.pair;
     const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
     const int32_t hk = h / p.kv_group;  // key/value head of query head h
@@ -309,7 +318,7 @@ struct RingPos {
   }
 };
 
-template <int D, int DT>
+template <int D, int DT, bool kSplit>
 __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint32_t sRing,
                          const Bars& bars, const WaitCtl& wc) {
   using C = Cfg<D, DT>;
@@ -327,7 +336,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
   for (int w = 0; ok; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
-    const Item item = decode_item(p, u);
+    const Item item = decode_item<kSplit>(p, u);
     const int n[2] = {item.n[0], item.n[1]};
     const int nmax = max(n[0], n[1]);
     if (nmax == 0) continue;
@@ -519,7 +528,15 @@ __device__ __forceinline__ void softmax_block(float (&s)[128], int lim, int j, f
     l += x0 + x1;
   }}
 
-template <int D, int DT>
+// Where a row's lse goes: the final lse [B, H, S_q], or -- for a split --
+// that split's slice of the fp32 partial lse [n_splits, B, H, S_q].
+template <bool kSplit>
+__device__ __forceinline__ float* lse_row_base(const KernelParams& p, int split, int bh) {
+  if (!kSplit) return p.lse + static_cast<int64_t>(bh) * p.S_q;
+  return p.lse_part + (static_cast<int64_t>(split) * p.B * p.H + bh) * p.S_q;
+}
+
+template <int D, int DT, bool kSplit>
 __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, const CUtensorMap* tmOp,
                              uint32_t tmem, uint32_t sEpi, int warp, int lane, const Bars& bars,
                              const WaitCtl& wc) {
@@ -530,7 +547,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t tS = tmem + lane_off + C::kTmemS + t * kBN;
   const uint32_t tO = tmem + lane_off + C::kTmemO + t * 128;
-  const bool split = p.n_splits > 1;
+  constexpr bool split = kSplit;
 
   float sl2 = p.scale_log2;
   float o_mul = 1.0f;
@@ -551,19 +568,15 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
   for (int w = 0;; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
-    const Item item = decode_item(p, u);
+    const Item item = decode_item<kSplit>(p, u);
     const int bh = item.bh;
     const int q_tile = 2 * item.pair + t;
     const int n = t ? item.n[1] : item.n[0];
     const int64_t row = static_cast<int64_t>(q_tile) * kBM + r;
-    const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
-    // lse of this row: the final one, or this split's partial one.
-    float* lse_out = split ? p.lse_part + ((static_cast<int64_t>(item.split) * p.B + b) * p.H + h) * p.S_q
-                           : p.lse + static_cast<int64_t>(bh) * p.S_q;
     if (n == 0) {
       // No key of this split is visible to this tile: an empty partial,
       // which the merge gives zero weight.
-      if (split && row < p.S_q) lse_out[row] = -CUDART_INF_F;
+      if (split && row < p.S_q) lse_row_base<kSplit>(p, item.split, bh)[row] = -CUDART_INF_F;
       continue;
     }
     const int64_t col_end = p.causal ? min(row + 1, p.S_kv) : p.S_kv;  // columns < col_end visible
@@ -607,6 +620,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     const int32_t box_row0 = q_tile * kBM + wq * 32;
     const uint32_t stage = sEpi + static_cast<uint32_t>(warp) * C::kEpiBoxBytes;
     const int n_boxes = split ? D / 32 : D / 64;
+    const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
 #pragma unroll 1
     for (int bx = 0; bx < n_boxes; ++bx) {
       uint32_t pk[32];
@@ -651,7 +665,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
         bulk_commit_group();
       }
     }
-    if (row < p.S_q) lse_out[row] = (m_run + log2f(l)) * 0.69314718055994531f;
+    if (row < p.S_q) lse_row_base<kSplit>(p, item.split, bh)[row] = (m_run + log2f(l)) * 0.69314718055994531f;
     tc_fence_before();
   }
   // Every TMA store of this warp has completed before the CTA exits.
@@ -662,7 +676,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
 // ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
-template <int D, int DT>
+template <int D, int DT, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -714,14 +728,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{p.wait_limit_ns, p.err, abort_flag};
 
   if (warp < kProducerWarp) {
-    reg_alloc_inc<kRegsSoftmax>();
-    softmax_role<D, DT>(p, &tmO, &tmOp, tmem, sEpi, warp, lane, bars, wc);
+    reg_alloc_inc<RegSplit<kSplit>::kSoftmax>();
+    softmax_role<D, DT, kSplit>(p, &tmO, &tmOp, tmem, sEpi, warp, lane, bars, wc);
   } else {
-    reg_alloc_dec<kRegsControl>();
+    reg_alloc_dec<RegSplit<kSplit>::kControl>();
     if (warp == kProducerWarp) {
-      if (lane == 0) producer_role<D, DT>(p, &tmQ, &tmK, &tmV, sQ, sRing, bars, wc);
+      if (lane == 0) producer_role<D, DT, kSplit>(p, &tmQ, &tmK, &tmV, sQ, sRing, bars, wc);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) mma_role<D, DT>(p, tmem, sQ, sRing, bars, wc);
+      if (lane == 0) mma_role<D, DT, kSplit>(p, tmem, sQ, sRing, bars, wc);
     }
   }
   __syncwarp();
@@ -733,13 +747,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Host-side launcher, one instantiation per (D, dtype).
-template <int D, int DT>
+// Host-side launcher, one instantiation per (D, dtype, split mode).
+template <int D, int DT, bool kSplit>
 cudaError_t launch_fa_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& o, const CUtensorMap& op, const KernelParams& p,
                           int grid, cudaStream_t stream) {
   using C = Cfg<D, DT>;
-  auto kern = fa_fwd_kernel<D, DT>;
+  auto kern = fa_fwd_kernel<D, DT, kSplit>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
