@@ -145,6 +145,48 @@ fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
                            const float* descale_v, int n_splits, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv without a caller workspace.  The
+ * attention pages have no counterpart to this call; it is a convenience of
+ * this library.
+ *
+ * Who needs it: callers that may not allocate device memory where they run
+ * attention and have no spare buffer to hand over -- code running under a
+ * memory budget fixed up front, code called back from inside a memory
+ * allocator, or a runtime whose hot path must not make the device-wide
+ * synchronising calls that cudaMalloc / cudaFree can imply.  The library
+ * itself never allocates here: the partials go to a fixed buffer of
+ * FA_NOALLOC_SCRATCH_BYTES bytes that is part of the library's device image
+ * (a file-scope __device__ array, one copy per device).
+ *
+ * Arguments, checks and statuses as fa_fwd_splitkv, without workspace and
+ * workspace_bytes.  n_splits = 1 uses no scratch at all.
+ *   Limit: the workspace fa_fwd_splitkv would need for these B, H, S_q, D
+ *   and n_splits (fp32 partial O and lse, 4 * n_splits * B * H * S_q *
+ *   (D + 1) bytes plus alignment) must fit in FA_NOALLOC_SCRATCH_BYTES;
+ *   otherwise FA_ERR_UNSUPPORTED, before any CUDA call (use fa_fwd_splitkv
+ *   with your own workspace, or fewer splits).
+ *   Zeroing: none needed; every partial the merge reads is written earlier
+ *   in the same call.
+ *   First call on a device: looks up the buffer's device address with that
+ *   device current (cudaGetSymbolAddress) and caches it; FA_ERR_CUDA if the
+ *   lookup fails.  If the calls are to be made while a stream is being
+ *   captured, make one call on each device before capture begins, so that
+ *   this setup happens outside the capture.
+ *   Overlap: all callers on a device share the one buffer.  Two calls whose
+ *   execution can overlap on the same device (different streams, or host
+ *   threads with no ordering between their launches) race on it and may
+ *   return wrong results; order them on one stream or with events.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+fa_status_t fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int64_t B, int64_t H, int64_t H_kv, int64_t S_q,
+                                   int64_t S_kv, int64_t D, float scale, fa_layout_t layout,
+                                   int causal, fa_dtype_t dtype, const float* descale_q,
+                                   const float* descale_k, const float* descale_v, int n_splits,
+                                   cudaStream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* fa_status_string(fa_status_t s);
 

@@ -206,6 +206,18 @@ void fa_set_wait_limit_ns(uint64_t ns) {
 
 }  // extern "C"
 
+namespace fa {
+// Workspace of a split run: fp32 partial O [n_splits, B, H, S_q, D], then fp32
+// partial lse [n_splits, B, H, S_q]; each part 256-byte aligned.  (Also used
+// by the no-allocation entry point in fa_noalloc.cu.)
+size_t split_workspace_bytes(int64_t B, int64_t H, int64_t S_q, int64_t D, int n_splits) {
+  const size_t rows = static_cast<size_t>(n_splits) * B * H * S_q;
+  const size_t o_bytes = (rows * D * 4 + 255) / 256 * 256;
+  return o_bytes + (rows * 4 + 255) / 256 * 256;
+}
+}  // namespace fa
+using fa::split_workspace_bytes;
+
 namespace {
 
 // Checks shared by every forward entry point (all before any CUDA call).
@@ -244,14 +256,6 @@ fa_status_t check_args(const void* q, const void* k, const void* v, const void* 
 }
 
 constexpr int kMaxSplits = 32;
-
-// Workspace of a split run: fp32 partial O [n_splits, B, H, S_q, D], then fp32
-// partial lse [n_splits, B, H, S_q]; each part 256-byte aligned.
-size_t split_workspace_bytes(int64_t B, int64_t H, int64_t S_q, int64_t D, int n_splits) {
-  const size_t rows = static_cast<size_t>(n_splits) * B * H * S_q;
-  const size_t o_bytes = (rows * D * 4 + 255) / 256 * 256;
-  return o_bytes + (rows * 4 + 255) / 256 * 256;
-}
 
 // The forward pass, whole (n_splits = 1: o / lse written directly) or split
 // over the keys (n_splits > 1: partials in `workspace`, then the merge).
