@@ -187,6 +187,45 @@ fa_status_t fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, 
                                    const float* descale_k, const float* descale_v, int n_splits,
                                    cudaStream_t stream);
 
+/*
+ * Backward pass (fp16 / bf16): the gradients of the attention above with
+ * respect to q, k and v, given the forward's o and lse and the upstream
+ * gradient dout:
+ *     P  = exp(scale * Q K^T - lse)   (masked entries 0; recomputed)
+ *     dV = P^T dO,   dP = dO V^T,   dS = P * (dP - rowsum(dO * O))
+ *     dQ = scale * dS K,   dK = scale * dS^T Q
+ * -- the chain rule through the reference attention of "ops-transformer
+ * FlashAttention build and tuning" (section 4.3); the pages train with this
+ * operator (its mixed-precision training configuration) and describe the
+ * backward dQ loop over key/value blocks (Hygon retrospective, defect 13).
+ * With H_kv < H the gradient of a key/value head sums over the query heads
+ * that read it.
+ *
+ * fa_bwd_workspace_size -- bytes of device workspace fa_bwd needs:
+ *   2 * 4 * B * H * (S_q rounded up to 128), each half 256-byte aligned.
+ *   Host only; FA_ERR_INVALID_ARG on bad sizes or a NULL output.
+ *
+ * fa_bwd -- q, k, v, o, dout, lse: as the forward's arguments and outputs
+ *   (o and dout in q's layout and dtype, lse fp32 [B, H, S_q] natural log);
+ *   dq (q's shape), dk and dv (k's shape): written, in the input dtype,
+ *   round-to-nearest-even.  workspace: caller-owned device memory of at
+ *   least fa_bwd_workspace_size bytes, 256-byte aligned; its contents on
+ *   entry do not matter.  Checks and statuses as fa_fwd_gqa, plus:
+ *   FA_ERR_INVALID_ARG for NULL dout / dq / dk / dv or a missing or small
+ *   workspace; FA_ERR_MISALIGNED for those pointers off 16 bytes (workspace
+ *   off 256); FA_ERR_UNSUPPORTED for FA_DTYPE_FP8E4M3.  Three launches on
+ *   `stream` (a row-statistics pass, the dQ kernel, the dK/dV kernel); the
+ *   workspace is written and read by them, so calls sharing one workspace
+ *   must not overlap.  Deterministic: no atomics.
+ */
+fa_status_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t S_q, size_t* workspace_bytes);
+
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H,
+                   int64_t H_kv, int64_t S_q, int64_t S_kv, int64_t D, float scale,
+                   fa_layout_t layout, int causal, fa_dtype_t dtype, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* fa_status_string(fa_status_t s);
 

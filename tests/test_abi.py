@@ -103,3 +103,25 @@ def test_splitkv_host_checks(lib):
     assert binding.fa_fwd_splitkv(*base, 4, 4112, 1 << 20) == 3        # not 256-aligned
     bad = (16, 32, 48, 64, 80, 1, 3, 2, 8, 512, 128, 0.1, "BNSD", 0, "bf16", None, None, None)
     assert binding.fa_fwd_splitkv(*bad, 4, 4096, 1 << 20) == 1         # H % H_kv != 0
+
+
+def test_bwd_host_checks(lib):
+    # fake pointers, never dereferenced: each case fails before any CUDA call
+    st, n = binding.fa_bwd_workspace_size(2, 4, 300)
+    assert st == 0 and n == 2 * ((2 * 4 * 384 * 4 + 255) // 256 * 256)
+    assert binding.fa_bwd_workspace_size(0, 4, 300)[0] == 1
+    p = [16 * (i + 1) for i in range(9)]
+    base = p + [2, 4, 2, 300, 300, 128, 0.1, "BNSD", 1, "bf16"]
+    assert binding.fa_bwd(*base, 4096, 8) == 1                      # workspace too small
+    assert binding.fa_bwd(*base, None, n) == 1                      # no workspace
+    assert binding.fa_bwd(*base, 4096 + 16, n) == 3                 # workspace off 256 bytes
+    fp8 = p + [2, 4, 2, 300, 300, 128, 0.1, "BNSD", 1, "e4m3"]
+    assert binding.fa_bwd(*fp8, 4096, n) == 2                       # no fp8 backward
+    nodq = list(p)
+    nodq[6] = None
+    assert binding.fa_bwd(*(nodq + [2, 4, 2, 300, 300, 128, 0.1, "BNSD", 1, "bf16"]), 4096, n) == 1
+    odd = list(p)
+    odd[7] = 16 * 8 + 2
+    assert binding.fa_bwd(*(odd + [2, 4, 2, 300, 300, 128, 0.1, "BNSD", 1, "bf16"]), 4096, n) == 3
+    assert binding.fa_bwd(*(p + [2, 4, 3, 300, 300, 128, 0.1, "BNSD", 1, "bf16"]), 4096, n) == 1
+    assert binding.fa_bwd(*(p + [2, 4, 2, 300, 300, 80, 0.1, "BNSD", 1, "bf16"]), 4096, n) == 2

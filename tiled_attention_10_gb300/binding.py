@@ -18,7 +18,7 @@ FA_STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
              3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
 # Symbols the header declares; the library must export all of them.
-EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_splitkv_noalloc", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
+EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_splitkv_noalloc", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
            "fa_probe_wait_timeout", "fa_version")
 
 _lib = None
@@ -57,6 +57,10 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32,
                                            ip, ip, ip, vp, vp, vp, ip, vp]
     lib.fa_fwd_splitkv_noalloc.restype = ip
+    lib.fa_bwd_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(sz)]
+    lib.fa_bwd_workspace_size.restype = ip
+    lib.fa_bwd.argtypes = [vp] * 9 + [i64] * 6 + [f32, ip, ip, ip, vp, sz, vp]
+    lib.fa_bwd.restype = ip
     lib.fa_status_string.argtypes = [ip]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_device_error.argtypes = [vp]
@@ -136,6 +140,25 @@ def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, lay
                                           int(S_kv), int(D), float(scale), lay,
                                           int(bool(causal)), dt, descale_q, descale_k, descale_v,
                                           int(n_splits), stream))
+
+
+def fa_bwd_workspace_size(B, H, S_q):
+    """(status, bytes) of device workspace fa_bwd needs."""
+    lib = load()
+    n = ctypes.c_size_t(0)
+    st = int(lib.fa_bwd_workspace_size(int(B), int(H), int(S_q), ctypes.byref(n)))
+    return st, int(n.value)
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S_q, S_kv, D, scale, layout, causal,
+           dtype, workspace, workspace_bytes, stream=None) -> int:
+    """Backward pass: dq, dk, dv from q, k, v, o, dout and lse (device pointers)."""
+    lib = load()
+    lay = FA_LAYOUT[layout] if isinstance(layout, str) else int(layout)
+    dt = FA_DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
+    return int(lib.fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, int(B), int(H), int(H_kv), int(S_q),
+                          int(S_kv), int(D), float(scale), lay, int(bool(causal)), dt, workspace,
+                          int(workspace_bytes), stream))
 
 
 def fa_last_device_error(stream=None) -> int:

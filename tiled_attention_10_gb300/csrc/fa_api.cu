@@ -21,6 +21,7 @@
 #include <mutex>
 
 #include "../../include/fa_api.h"
+#include "fa_bwd.cuh"
 #include "fa_combine.cuh"
 #include "fa_kernel.cuh"
 
@@ -67,6 +68,12 @@ extern template cudaError_t launch_fa_fwd<128, kDtE4M3, true>(const CUtensorMap&
                                                               const CUtensorMap&, const KernelParams&,
                                                               int, cudaStream_t);
 }  // namespace fa
+
+// Backward launchers live in fa_bwd_inst_*.cu.
+FA_BWD_INSTANTIATE(extern, 64, fa::bwd::kF16)
+FA_BWD_INSTANTIATE(extern, 128, fa::bwd::kF16)
+FA_BWD_INSTANTIATE(extern, 64, fa::bwd::kBF16)
+FA_BWD_INSTANTIATE(extern, 128, fa::bwd::kBF16)
 
 // Device error word: bounded waits OR their error bits in here.
 __device__ uint32_t g_fa_device_error = 0;
@@ -440,6 +447,122 @@ fa_status_t fa_probe_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
   fa_wait_probe_kernel<<<1, 32, 0, stream>>>(dev.err_word, limit_ns ? limit_ns : 1000000ull);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   return fa_last_device_error(stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Backward workspace: lse * log2(e), then rowsum(dO * O), each fp32
+// [B * H, S_q rounded up to 128], 256-byte aligned.
+size_t bwd_workspace_bytes(int64_t B, int64_t H, int64_t S_q) {
+  const size_t rows = static_cast<size_t>(B) * H * ((S_q + 127) / 128 * 128);
+  return 2 * ((rows * 4 + 255) / 256 * 256);
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t S_q, size_t* workspace_bytes) {
+  if (!workspace_bytes || B < 1 || H < 1 || S_q < 1) return FA_ERR_INVALID_ARG;
+  *workspace_bytes = bwd_workspace_bytes(B, H, S_q);
+  return FA_OK;
+}
+
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H,
+                   int64_t H_kv, int64_t S_q, int64_t S_kv, int64_t D, float scale,
+                   fa_layout_t layout, int causal, fa_dtype_t dtype, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+  fa_status_t st = check_args(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout, dtype,
+                              nullptr, nullptr, nullptr);
+  if (st != FA_OK) return st;
+  if (!dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (dtype == FA_DTYPE_FP8E4M3) return FA_ERR_UNSUPPORTED;
+  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return FA_ERR_MISALIGNED;
+  if (!workspace || workspace_bytes < bwd_workspace_bytes(B, H, S_q)) return FA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  const int64_t n_q = (S_q + 127) / 128, n_kv = (S_kv + 127) / 128;
+  if (B * H > INT32_MAX / n_q || B * H_kv > INT32_MAX / n_kv) return FA_ERR_UNSUPPORTED;
+
+  DeviceInfo dev;
+  if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
+  if (!make_map(&mq, q, dtype, layout, B, H, S_q, D) ||
+      !make_map(&mk, k, dtype, layout, B, H_kv, S_kv, D) ||
+      !make_map(&mv, v, dtype, layout, B, H_kv, S_kv, D) ||
+      !make_map(&mdo, dout, dtype, layout, B, H, S_q, D) ||
+      !make_map(&mdq, dq, dtype, layout, B, H, S_q, D, 32) ||
+      !make_map(&mdk, dk, dtype, layout, B, H_kv, S_kv, D, 32) ||
+      !make_map(&mdv, dv, dtype, layout, B, H_kv, S_kv, D, 32))
+    return FA_ERR_CUDA;
+
+  const int64_t S_q_pad = n_q * 128;
+  const size_t half_ws = bwd_workspace_bytes(B, H, S_q) / 2;
+  float* lse2 = static_cast<float*>(workspace);
+  float* dsum = reinterpret_cast<float*>(static_cast<char*>(workspace) + half_ws);
+
+  fa::bwd::BwdParams p = {};
+  p.B = B; p.H = H; p.H_kv = H_kv; p.S_q = S_q; p.S_kv = S_kv;
+  p.S_q_pad = S_q_pad;
+  p.kv_group = static_cast<int32_t>(H / H_kv);
+  p.n_q_tiles = static_cast<int32_t>(n_q);
+  p.n_kv_tiles = static_cast<int32_t>(n_kv);
+  p.layout = static_cast<int32_t>(layout);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale = scale;
+  p.lse2 = lse2;
+  p.dsum = dsum;
+  p.err = dev.err_word;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+
+  // dQ: one unit per (query head, query tile); causal runs group heads so
+  // that the K/V in flight fit in about 48 MB of L2 (as the forward).
+  fa::bwd::BwdParams pq = p;
+  pq.num_units = static_cast<int32_t>(B * H * n_q);
+  int64_t gq = 1;
+  if (causal) {
+    const int64_t kv_bytes = 2 * S_kv * D * 2 * H_kv / H;
+    gq = (48ll << 20) / (kv_bytes > 0 ? kv_bytes : 1);
+    gq = gq < 1 ? 1 : (gq > B * H ? B * H : gq);
+  }
+  pq.group_heads = static_cast<int32_t>(gq);
+  // dK / dV: one unit per (key/value head, key tile); heads grouped so that
+  // the Q / dO their query heads stream fit in about 48 MB of L2.
+  fa::bwd::BwdParams pk = p;
+  pk.num_units = static_cast<int32_t>(B * H_kv * n_kv);
+  int64_t gk = 1;
+  if (causal) {
+    const int64_t qdo_bytes = 2 * S_q * D * 2 * (H / H_kv);
+    gk = (48ll << 20) / (qdo_bytes > 0 ? qdo_bytes : 1);
+    gk = gk < 1 ? 1 : (gk > B * H_kv ? B * H_kv : gk);
+  }
+  pk.group_heads = static_cast<int32_t>(gk);
+
+  const int grid_q = static_cast<int>(pq.num_units < dev.sm_count ? pq.num_units : dev.sm_count);
+  const int grid_k = static_cast<int>(pk.num_units < dev.sm_count ? pk.num_units : dev.sm_count);
+  const int64_t prep_threads = B * H * S_q_pad * (D / 8);
+  const int64_t prep_blocks = (prep_threads + 255) / 256;
+  const int grid_p = static_cast<int>(prep_blocks < 8ll * dev.sm_count ? prep_blocks : 8ll * dev.sm_count);
+  cudaError_t e;
+  if (dtype == FA_DTYPE_F16)
+    e = (D == 64) ? fa::bwd::launch_fa_bwd<64, fa::bwd::kF16>(mq, mk, mv, mdo, mdq, mdk, mdv, o, dout,
+                                                              lse, lse2, dsum, pq, pk, grid_q,
+                                                              grid_k, grid_p, stream)
+                  : fa::bwd::launch_fa_bwd<128, fa::bwd::kF16>(mq, mk, mv, mdo, mdq, mdk, mdv, o,
+                                                               dout, lse, lse2, dsum, pq, pk,
+                                                               grid_q, grid_k, grid_p, stream);
+  else
+    e = (D == 64) ? fa::bwd::launch_fa_bwd<64, fa::bwd::kBF16>(mq, mk, mv, mdo, mdq, mdk, mdv, o,
+                                                               dout, lse, lse2, dsum, pq, pk,
+                                                               grid_q, grid_k, grid_p, stream)
+                  : fa::bwd::launch_fa_bwd<128, fa::bwd::kBF16>(mq, mk, mv, mdo, mdq, mdk, mdv, o,
+                                                                dout, lse, lse2, dsum, pq, pk,
+                                                                grid_q, grid_k, grid_p, stream);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // extern "C"
