@@ -214,6 +214,32 @@ def cpu_baseline(w, x, budget_s: float = 12.0):
                       f"float64, {t:.1f} s"}
 
 
+def oracle_bwd_head(w, x, do, b: int = 0, hk: int = 0) -> float:
+    """Backward oracle for one key/value head (all query heads that read it);
+    returns seconds."""
+    from oracle import backward as ob
+    t0 = time.perf_counter()
+    ob.attention_bwd(x.q, x.k, x.v, do, dtype=w.dtype, layout=w.layout, B=w.B, H=w.H,
+                     S_q=w.S_q, S_kv=w.S_kv, D=w.D, scale=w.softmax_scale, causal=w.causal,
+                     H_kv=w.kv_heads, kv_heads=[(b, hk)])
+    return time.perf_counter() - t0
+
+
+def bwd_sample_flops(w) -> float:
+    """Nominal backward FLOPs of one key/value head's query heads."""
+    return w.flops / (w.B * w.kv_heads)
+
+
+def cpu_baseline_bwd(w, x, do):
+    import oracle
+    oracle.build()
+    t = oracle_bwd_head(w, x, do)
+    return {"value": round(bwd_sample_flops(w) / t / 1e12, 6), "unit": "TFLOP/s",
+            "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"one (batch, key/value head) of {w.B * w.kv_heads}: {w.H // w.kv_heads} "
+                      f"query head(s) x {w.S_q} x {w.S_kv}, float64 numpy, {t:.1f} s"}
+
+
 # ---------------------------------------------------------------------------
 # Arms.
 # ---------------------------------------------------------------------------
@@ -223,8 +249,30 @@ def run_reference(args, w, world, rank):
     if rank != 0:
         return 0
     import oracle
-    from tiled_attention_10_gb300.inputs import make_inputs
+    from tiled_attention_10_gb300.inputs import make_dout, make_inputs
     oracle.build()
+    if w.bwd:
+        one = type(w)(**{**w.__dict__, "B": 1, "H": w.H // w.kv_heads, "H_kv": 1})
+        x, do = make_inputs(one), make_dout(one)
+        for _ in range(args.warmup):
+            oracle_bwd_head(one, x, do)
+        times = [oracle_bwd_head(one, x, do) for _ in range(args.steps)]
+        t = sum(times) / len(times)
+        val = bwd_sample_flops(one) / t / 1e12
+        sample = (f"backward of one (batch, key/value head) per step: {one.H} query head(s) x "
+                  f"{w.S_q} x {w.S_kv}, float64")
+        cores = oracle.max_threads()
+        line = {"impl": "reference", "metric": "attention bwd TFLOP/s", "value": round(val, 6),
+                "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {**w.describe(), "sample_per_step": sample},
+                "cpu_baseline": {"value": round(val, 6), "unit": "TFLOP/s", "cores": cores,
+                                 "kind": "oracle", "sample": sample},
+                "e2e": {"value": round(val, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
     one = type(w)(**{**w.__dict__, "B": 1, "H": 1, "H_kv": None})
     x = make_inputs(one)
     cores = oracle.max_threads()
@@ -378,6 +426,128 @@ def run_ours(args, w, world, rank, local):
     return 0
 
 
+def run_ours_bwd(args, w, world, rank, local):
+    """Backward workloads: one step = one fa_bwd call (three launches: row
+    statistics, dQ kernel, dK/dV kernel) with Q, K, V, O, dO, lse resident."""
+    import torch
+    from tiled_attention_10_gb300 import binding
+    from tiled_attention_10_gb300.inputs import make_dout, make_inputs
+
+    binding.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if world > 1:
+        w = type(w)(**{**w.__dict__, "seed": w.seed + 1000 * rank})
+    x = make_inputs(w, device=dev)
+    q, k, v = x.q, x.k, x.v
+    do = make_dout(w, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.S_q, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    st = binding.fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D, w.softmax_scale, w.layout,
+                            w.causal, w.dtype, None, None, None, sp)
+    if st != 0:
+        raise RuntimeError(f"fa_fwd: {binding.fa_status_string(st)}")
+    st, ws_bytes = binding.fa_bwd_workspace_size(w.B, w.H, w.S_q)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def step(qq=q, kk=k, vv=v, oo=o, dd=do, ll=lse):
+        st = binding.fa_bwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(),
+                            dd.data_ptr(), ll.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                            dv.data_ptr(), w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D,
+                            w.softmax_scale, w.layout, w.causal, w.dtype, ws.data_ptr(), ws_bytes,
+                            sp)
+        if st != 0:
+            raise RuntimeError(f"fa_bwd: {binding.fa_status_string(st)}")
+
+    sampler = ClockSampler(local)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if binding.fa_last_device_error(sp) != 0:
+        raise RuntimeError("device-side error during warm-up")
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler.summarize(sampler.stop())
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    ms_max = max_over_ranks(total_ms / args.steps, world)
+    if binding.fa_last_device_error(sp) != 0:
+        raise RuntimeError("device-side error during the timed steps")
+
+    # End to end: pinned host Q, K, V, O, dO, lse in; dQ, dK, dV out.
+    ins = (q, k, v, o, do, lse)
+    hins = [t.cpu().pin_memory() for t in ins]
+    dins = [torch.empty_like(t) for t in ins]
+    houts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+
+    def e2e_step():
+        for d_, h_ in zip(dins, hins):
+            d_.copy_(h_, non_blocking=True)
+        step(*dins)
+        for h_, d_ in zip(houts, (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 30))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in ins)
+    d2h = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
+    if rank != 0:
+        return 0
+    flops = w.flops
+    peaks, peak_src = load_peaks()
+    sustained = total_ms > 1000.0
+    peak = tensor_peak(peaks, w.dtype, sustained)
+    step_ms = statistics.mean(per_step)
+    achieved = flops / (step_ms * 1e-3) / 1e12
+    # Products the tensor cores actually run per step: the dQ kernel
+    # recomputes S and dP, so 7 forward-sized products against the 5 counted.
+    executed = flops * 7.0 / 5.0 / (step_ms * 1e-3) / 1e12
+    line = {
+        "metric": "attention bwd TFLOP/s", "value": round(world * flops / (ms_max * 1e-3) / 1e12, 3),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {**w.describe(),
+                   "l2": "no flush: inputs (Q, K, V, O, dO) exceed the 129 MB L2",
+                   "parallelism": f"{world} independent shard(s) of B*H, one per GPU",
+                   "flops": "2.5 x the forward's 4*B*H*S_q*S_kv*D (halved when causal)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "scope": "whole fa_bwd step (row statistics + dQ + dK/dV kernels, CUDA "
+                              "events around each call)",
+                     "executed_frac": round(executed / peak, 4),
+                     "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} bf16 GEMM"},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * 3,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_bwd(w, make_inputs(w), make_dout(w))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description="FlashAttention forward benchmark (libfa_b200)")
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,6 +565,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             return run_reference(args, w, world, rank)
+        if w.bwd:
+            return run_ours_bwd(args, w, world, rank, local)
         return run_ours(args, w, world, rank, local)
     finally:
         if world > 1:

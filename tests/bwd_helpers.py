@@ -29,7 +29,7 @@ import torch
 
 from oracle import backward as ob
 from tiled_attention_10_gb300 import binding
-from tiled_attention_10_gb300.inputs import OUT_DTYPE, Workload, make_inputs, shape_of
+from tiled_attention_10_gb300.inputs import OUT_DTYPE, Workload, make_dout, shape_of
 
 U = {"bf16": 2.0 ** -8, "f16": 2.0 ** -11}
 A16 = {"bf16": 0.0, "f16": 2.0 ** -25}
@@ -148,10 +148,8 @@ class BwdRun:
 
 
 def make_do(w: Workload, device="cpu"):
-    """Upstream gradient dO: iid N(0,1) in q's shape and dtype, its own seed."""
-    wd = Workload("do", w.B, w.H, w.S_q, w.S_q, w.D, w.dtype, w.layout, False,
-                  seed=1000 + w.seed, poison=w.poison)
-    return make_inputs(wd, device=device).q
+    """Upstream gradient dO (seeded, in q's shape and dtype)."""
+    return make_dout(w, device=device)
 
 
 def oracle_o_lse(w: Workload, terms):

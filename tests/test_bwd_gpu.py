@@ -16,8 +16,9 @@ import torch
 
 from oracle import backward as ob
 from tiled_attention_10_gb300 import binding
-from tiled_attention_10_gb300.inputs import Workload, make_inputs
-from tests.bwd_helpers import BwdRun, bounds, make_do, oracle_o_lse, to_bnsd64
+from tiled_attention_10_gb300.inputs import BWD_WORKLOADS, Workload, make_dout, make_inputs
+from tests.bwd_helpers import (SAFETY, U, BwdRun, bounds, head_bounds, make_do, oracle_o_lse,
+                               to_bnsd64)
 from tests.gpu_helpers import Run, to_device
 
 pytestmark = pytest.mark.gpu
@@ -148,3 +149,60 @@ def test_bwd_bad_arguments_launch_nothing(cuda_lib):
         assert binding.fa_bwd(*a) == code, (idx, val)
     torch.cuda.synchronize()
     assert bool((dq == 7.0).all()) and bool((dk == 7.0).all()) and bool((dv == 7.0).all())
+
+
+def _head(t, layout, b, h):
+    """One head of a device tensor as float64 numpy [S, D] (torch's exact
+    upcast of the 16-bit values)."""
+    x = t[b, h] if layout == "BNSD" else t[b, :, h]
+    return x.double().cpu().numpy()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", sorted(BWD_WORKLOADS))
+def test_bwd_workload_sampled_heads(name, cuda_lib):
+    """The measured backward workloads at full size, in the benchmark's launch
+    configuration (O and lse from the GPU forward): every element of two
+    key/value heads (the first and the last) against the oracle and the
+    bound; no NaN / Inf anywhere; canaries intact."""
+    w = BWD_WORKLOADS[name]
+    x = make_inputs(w, device="cuda")
+    do = make_dout(w, device="cuda")
+    f = Run(w, x.q, x.k, x.v)
+    torch.cuda.synchronize()
+    assert f.status == 0 and f.device_status == 0
+    r = BwdRun(w, x.q, x.k, x.v, f.o, do, f.lse)
+    torch.cuda.synchronize()
+    assert r.status == 0 and r.device_status == 0 and r.guards_intact()
+    for t in (r.dq, r.dk, r.dv):
+        assert bool(torch.isfinite(t.float()).all())
+    g = w.H // w.kv_heads
+    for (b, hk) in ((0, 0), (w.B - 1, w.kv_heads - 1)):
+        k64, v64 = _head(x.k, w.layout, b, hk), _head(x.v, w.layout, b, hk)
+        sum_dk = np.zeros_like(k64)
+        sum_dv = np.zeros_like(v64)
+        bnd_dk = np.zeros_like(k64)
+        bnd_dv = np.zeros_like(v64)
+        for h in range(hk * g, (hk + 1) * g):
+            q64, do64 = _head(x.q, w.layout, b, h), _head(do, w.layout, b, h)
+            t = ob.head_terms(q64, k64, v64, do64, w.softmax_scale, w.causal)
+            o_in = _head(f.o, w.layout, b, h)
+            lse_in = f.lse[b, h].double().cpu().numpy()
+            b_dq, b_dk, b_dv = head_bounds(t, q64, k64, v64, do64, o_in, lse_in,
+                                           w.softmax_scale, w.dtype)
+            u = U[w.dtype] + 2.0 ** -24
+            got = _head(r.dq, w.layout, b, h)
+            lim = SAFETY * (b_dq + u * np.abs(t["dQ"]) + 2.0 ** -25)
+            err = np.abs(got - t["dQ"])
+            assert (err <= lim).all(), ("dQ", b, h, float((err / lim).max()))
+            sum_dk += t["dK"]
+            sum_dv += t["dV"]
+            bnd_dk += b_dk
+            bnd_dv += b_dv
+        for nm, got_t, want, bb in (("dK", r.dk, sum_dk, bnd_dk), ("dV", r.dv, sum_dv, bnd_dv)):
+            got = _head(got_t, w.layout, b, hk)
+            lim = SAFETY * (bb + (U[w.dtype] + 2.0 ** -24) * np.abs(want) + 2.0 ** -25)
+            err = np.abs(got - want)
+            assert (err <= lim).all(), (nm, b, hk, float((err / lim).max()))
+            print(f"{name} (b={b}, hk={hk}) {nm}: max|err|={err.max():.3g} "
+                  f"max err/bound={(err / lim).max():.3f}")

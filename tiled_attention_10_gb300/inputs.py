@@ -46,6 +46,7 @@ class Workload:
     seed: int = 0
     H_kv: Optional[int] = None      # key/value heads (grouped-query attention); default H
     split: bool = False             # run through the split-KV entry point
+    bwd: bool = False               # a backward-pass workload (gradients of the forward)
 
     @property
     def kv_heads(self) -> int:
@@ -57,9 +58,12 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """Nominal attention FLOPs: 4*B*H*S_q*S_kv*D, halved when causal."""
+        """Nominal attention FLOPs: 4*B*H*S_q*S_kv*D, halved when causal; a
+        backward pass counts 2.5 times that (five products of the forward's
+        size: S recomputed, dP, dV, dK, dQ)."""
         f = 4.0 * self.B * self.H * self.S_q * self.S_kv * self.D
-        return f / 2 if self.causal else f
+        f = f / 2 if self.causal else f
+        return 2.5 * f if self.bwd else f
 
     def describe(self) -> dict:
         return {"workload": self.name, "B": self.B, "H": self.H, "H_kv": self.kv_heads,
@@ -68,7 +72,8 @@ class Workload:
                 "causal": self.causal, "scale": self.softmax_scale,
                 "values": f"iid N(0,{self.std}^2), seed {self.seed}"
                           + (", per-tensor amax e4m3" if self.dtype == "e4m3" else "")
-                          + (", NaN-poisoned tail" if self.poison else "")}
+                          + (", NaN-poisoned tail" if self.poison else ""),
+                **({"pass": "backward (dQ, dK, dV from O, dO, lse)"} if self.bwd else {})}
 
 
 # The five workloads the method is measured and checked on.
@@ -98,6 +103,16 @@ EXTRA_WORKLOADS = {
     "bf16_splitkv_1x8x512x16384x128": Workload("bf16_splitkv_1x8x512x16384x128", 1, 8, 512, 16384,
                                                128, "bf16", "BNSD", False, split=True),
 }
+# Backward pass: the training configuration of the Ascend page (32 heads,
+# head dim 128, causal, bf16) at the forward's 4 x 4096 tokens, and the
+# forward's non-causal shape.
+BWD_WORKLOADS = {
+    "bf16_bwd_causal_4x32x4096x128": Workload("bf16_bwd_causal_4x32x4096x128", 4, 32, 4096, 4096,
+                                              128, "bf16", "BNSD", True, bwd=True),
+    "bf16_bwd_4x32x4096x128": Workload("bf16_bwd_4x32x4096x128", 4, 32, 4096, 4096, 128, "bf16",
+                                       "BNSD", False, bwd=True),
+}
+EXTRA_WORKLOADS.update(BWD_WORKLOADS)
 ALL_WORKLOADS = {**WORKLOADS, **EXTRA_WORKLOADS}
 
 
@@ -179,3 +194,11 @@ def sample_rows(w: Workload, n: int, seed: int = 0):
     for _ in range(max(0, n - 2)):
         rows.append((int(rng.integers(w.B)), int(rng.integers(w.H)), int(rng.integers(w.S_q))))
     return np.asarray(rows[:n], dtype=np.int64)
+
+
+def make_dout(w: Workload, device="cpu") -> torch.Tensor:
+    """Upstream gradient dO for a backward workload: iid N(0, 1) in Q's shape,
+    layout and storage type, from its own seed (1000 + the workload's)."""
+    wd = dataclasses.replace(w, name=w.name + "/dO", S_kv=w.S_q, H_kv=None, seed=1000 + w.seed,
+                             std=1.0, split=False, bwd=False)
+    return make_inputs(wd, device=device).q

@@ -36,6 +36,8 @@ KEY_METRICS = [
     ("launch__grid_size", "grid"),
     ("launch__block_size", "block"),
     ("l1tex__data_bank_conflicts_pipe_lsu_mem_shared.sum", "smem bank conflicts (LSU)"),
+    ("l1tex__data_pipe_tc_wavefronts_mem_shared.sum.pct_of_peak_sustained_elapsed",
+     "shared memory read by the tensor cores, % of peak"),
 ]
 
 
@@ -69,13 +71,13 @@ def launches(csv_path: str, out_md: str, command: str) -> None:
     open(out_md, "w").write("\n".join(lines) + "\n")
 
 
-def kernel(rep: str, workload: str, out_md: str, command: str) -> None:
+def kernel(rep: str, workload: str, out_md: str, command: str, kname: str = "fa_fwd") -> None:
     raw = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], capture_output=True,
                          text=True, check=True).stdout
     rows = list(csv.reader(io.StringIO(raw)))
     hdr, units, vals = rows[0], rows[1], rows[2]
     col = {h: i for i, h in enumerate(hdr)}
-    lines = [f"# ncu `--set full`: fa_fwd_kernel on {workload}", "",
+    lines = [f"# ncu `--set full`: {kname}_kernel on {workload}", "",
              f"Command: `{command}`", "", "| metric | value | unit |", "|---|---|---|"]
     for key, label in KEY_METRICS:
         if key in col:
@@ -93,7 +95,7 @@ def kernel(rep: str, workload: str, out_md: str, command: str) -> None:
     import bench
     rec = {"workload": workload, "dram_bytes_per_launch": rd + wr, "dram_read": rd,
            "dram_write": wr, "kernel_sha": bench.kernel_source_sha(), "command": command}
-    with open(os.path.join(os.path.dirname(out_md), f"fa_fwd_{workload}.ncu.json"), "w") as f:
+    with open(os.path.join(os.path.dirname(out_md), f"{kname}_{workload}.ncu.json"), "w") as f:
         json.dump(rec, f, indent=1)
 
 
@@ -101,4 +103,4 @@ if __name__ == "__main__":
     if sys.argv[1] == "launches":
         launches(sys.argv[2], sys.argv[3], sys.argv[4])
     else:
-        kernel(sys.argv[2], sys.argv[3], sys.argv[4], sys.argv[5])
+        kernel(sys.argv[2], sys.argv[3], sys.argv[4], sys.argv[5], *sys.argv[6:7])
