@@ -188,6 +188,64 @@ fa_status_t fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, 
                                    cudaStream_t stream);
 
 /*
+ * Variable-length sequences and paged K/V (forward).
+ *
+ * Packed queries: q and o are [total_q, H, D] (o in the output dtype), the
+ * queries of sequence s are rows [cu_seqlens_q[s], cu_seqlens_q[s+1]); lse
+ * is fp32 [H, total_q].  Each sequence is attended on its own, as the dense
+ * call would on a [1, S_q, H, D] problem (query head h reads key/value head
+ * h / (H / H_kv)).  cu_seqlens_q (and cu_seqlens_k, seqused_k,
+ * block_table) are device int32 arrays read by the kernel; the host cannot
+ * check them.  Offsets outside [0, total] or lengths that do not fit are
+ * clamped so that nothing outside o and lse is ever written.
+ *
+ * causal: 0 none; FA_CAUSAL_TOP_LEFT (1): query i sees key j iff j <= i (the
+ * dense call's mask); FA_CAUSAL_BOTTOM_RIGHT (2): iff j <= i + S_kv - S_q,
+ * i.e. the queries are the last S_q positions of the key sequence (prefill
+ * after a cached prefix, decode).  A query row that sees no key gets O = 0
+ * and lse = -inf.
+ *
+ * max_seqlen_q: at least every sequence's query length (rows past it are not
+ * computed); it sizes the launch.  total_q = 0 returns FA_OK at once.
+ *
+ * fa_fwd_varlen -- contiguous packed K/V: k and v are [total_k, H_kv, D], the
+ *   keys of sequence s are rows [cu_seqlens_k[s], cu_seqlens_k[s+1]).
+ *
+ * fa_fwd_paged -- K/V in a paged cache (the PagedAttention scheme of the
+ *   Hygon retrospective, defect 11): k_cache and v_cache are [num_pages,
+ *   page_size, H_kv, D]; sequence s has seqused_k[s] keys and its key j is row
+ *   j % page_size of page block_table[s * max_pages_per_seq + j / page_size].
+ *   page_size: 16, 32, 64 or 128, or a multiple of 128 (else
+ *   FA_ERR_UNSUPPORTED); a 128-key tile spanning several pages is fetched page
+ *   by page, never as if the pages were adjacent.  Page ids outside
+ *   [0, num_pages) read as zeros.
+ *
+ * Statuses as fa_fwd_gqa (dtype, D, alignment, descales), plus
+ * FA_ERR_INVALID_ARG for NULL arrays, n_seqs < 1, total_q < 0,
+ * max_seqlen_q < 1, causal outside {0, 1, 2} or paging sizes < 1;
+ * FA_ERR_MISALIGNED for the int32 arrays off 4 bytes.  One launch on
+ * `stream`; the library allocates nothing.
+ */
+#define FA_CAUSAL_NONE 0
+#define FA_CAUSAL_TOP_LEFT 1
+#define FA_CAUSAL_BOTTOM_RIGHT 2
+
+fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                          int64_t n_seqs, int64_t total_q, int64_t total_k, int64_t max_seqlen_q,
+                          int64_t H, int64_t H_kv, int64_t D, float scale, int causal,
+                          fa_dtype_t dtype, const float* descale_q, const float* descale_k,
+                          const float* descale_v, cudaStream_t stream);
+
+fa_status_t fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, void* o,
+                         float* lse, const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                         const int32_t* block_table, int64_t n_seqs, int64_t max_pages_per_seq,
+                         int64_t page_size, int64_t num_pages, int64_t total_q,
+                         int64_t max_seqlen_q, int64_t H, int64_t H_kv, int64_t D, float scale,
+                         int causal, fa_dtype_t dtype, const float* descale_q,
+                         const float* descale_k, const float* descale_v, cudaStream_t stream);
+
+/*
  * Backward pass (fp16 / bf16): the gradients of the attention above with
  * respect to q, k and v, given the forward's o and lse and the upstream
  * gradient dout:

@@ -125,3 +125,21 @@ def test_bwd_host_checks(lib):
     assert binding.fa_bwd(*(odd + [2, 4, 2, 300, 300, 128, 0.1, "BNSD", 1, "bf16"]), 4096, n) == 3
     assert binding.fa_bwd(*(p + [2, 4, 3, 300, 300, 128, 0.1, "BNSD", 1, "bf16"]), 4096, n) == 1
     assert binding.fa_bwd(*(p + [2, 4, 2, 300, 300, 80, 0.1, "BNSD", 1, "bf16"]), 4096, n) == 2
+
+
+def test_varlen_paged_host_checks(lib):
+    # fake pointers, never dereferenced: each case fails before any CUDA call
+    a = 4096
+    vb = [a] * 7 + [2, 300, 300, 300, 4, 2, 128, 0.1, 1, "bf16"]
+    assert binding.fa_fwd_varlen(*vb[:5], None, *vb[6:]) == 1          # no cu_seqlens_q
+    assert binding.fa_fwd_varlen(*vb[:7], 0, *vb[8:]) == 1             # n_seqs < 1
+    assert binding.fa_fwd_varlen(*vb[:16], 3, "bf16") == 1             # causal 3
+    assert binding.fa_fwd_varlen(*vb[:13], 80, *vb[14:]) == 2          # D = 80
+    assert binding.fa_fwd_varlen(*vb[:6], a + 2, *vb[7:]) == 3         # cu_seqlens_k off 4 bytes
+    assert binding.fa_fwd_varlen(*vb[:8], 0, *vb[9:]) == 0             # total_q = 0: nothing to do
+    pg = [a] * 8 + [2, 8, 64, 100, 300, 300, 4, 2, 128, 0.1, 2, "bf16"]
+    assert binding.fa_fwd_paged(*pg[:10], 48, *pg[11:]) == 2           # page size 48
+    assert binding.fa_fwd_paged(*pg[:10], 8, *pg[11:]) == 1            # page size < 16
+    assert binding.fa_fwd_paged(*pg[:7], None, *pg[8:]) == 1           # no block table
+    assert binding.fa_fwd_paged(*pg[:9], 0, *pg[10:]) == 1             # max pages 0
+    assert binding.fa_fwd_paged(*pg[:15], 3, *pg[16:]) == 1            # H % H_kv != 0

@@ -18,7 +18,7 @@ FA_STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
              3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
 # Symbols the header declares; the library must export all of them.
-EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_splitkv_noalloc", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
+EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_splitkv_noalloc", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd_varlen", "fa_fwd_paged", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
            "fa_probe_wait_timeout", "fa_version")
 
 _lib = None
@@ -61,6 +61,10 @@ def load(path: str = LIB_PATH):
     lib.fa_bwd_workspace_size.restype = ip
     lib.fa_bwd.argtypes = [vp] * 9 + [i64] * 6 + [f32, ip, ip, ip, vp, sz, vp]
     lib.fa_bwd.restype = ip
+    lib.fa_fwd_varlen.argtypes = [vp] * 7 + [i64] * 7 + [f32, ip, ip, vp, vp, vp, vp]
+    lib.fa_fwd_varlen.restype = ip
+    lib.fa_fwd_paged.argtypes = [vp] * 8 + [i64] * 9 + [f32, ip, ip, vp, vp, vp, vp]
+    lib.fa_fwd_paged.restype = ip
     lib.fa_status_string.argtypes = [ip]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_device_error.argtypes = [vp]
@@ -159,6 +163,34 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S_q, S_kv, D, scale, l
     return int(lib.fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, int(B), int(H), int(H_kv), int(S_q),
                           int(S_kv), int(D), float(scale), lay, int(bool(causal)), dt, workspace,
                           int(workspace_bytes), stream))
+
+
+CAUSAL = {"none": 0, "top_left": 1, "bottom_right": 2}
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, n_seqs, total_q, total_k, max_seqlen_q, H, H_kv,
+                  D, scale, causal, dtype, descale_q=None, descale_k=None, descale_v=None,
+                  stream=None) -> int:
+    """Packed variable-length forward (device pointers; causal 0 / 1 / 2)."""
+    lib = load()
+    dt = FA_DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
+    c = CAUSAL[causal] if isinstance(causal, str) else int(causal)
+    return int(lib.fa_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, int(n_seqs), int(total_q),
+                                 int(total_k), int(max_seqlen_q), int(H), int(H_kv), int(D),
+                                 float(scale), c, dt, descale_q, descale_k, descale_v, stream))
+
+
+def fa_fwd_paged(q, k_cache, v_cache, o, lse, cu_q, seqused_k, block_table, n_seqs, max_pages,
+                 page_size, num_pages, total_q, max_seqlen_q, H, H_kv, D, scale, causal, dtype,
+                 descale_q=None, descale_k=None, descale_v=None, stream=None) -> int:
+    """Packed queries against a paged K/V cache (device pointers)."""
+    lib = load()
+    dt = FA_DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
+    c = CAUSAL[causal] if isinstance(causal, str) else int(causal)
+    return int(lib.fa_fwd_paged(q, k_cache, v_cache, o, lse, cu_q, seqused_k, block_table,
+                                int(n_seqs), int(max_pages), int(page_size), int(num_pages),
+                                int(total_q), int(max_seqlen_q), int(H), int(H_kv), int(D),
+                                float(scale), c, dt, descale_q, descale_k, descale_v, stream))
 
 
 def fa_last_device_error(stream=None) -> int:

@@ -25,49 +25,18 @@
 #include "fa_combine.cuh"
 #include "fa_kernel.cuh"
 
-namespace fa {
 // Explicit instantiations live in fa_inst_*.cu (compiled in parallel).
-extern template cudaError_t launch_fa_fwd<64, kDtF16, false>(const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const KernelParams&,
-                                                              int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<64, kDtF16, true>(const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const KernelParams&,
-                                                              int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<128, kDtF16, false>(const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const KernelParams&,
-                                                              int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<128, kDtF16, true>(const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const KernelParams&,
-                                                              int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<64, kDtBF16, false>(const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const KernelParams&,
-                                                              int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<64, kDtBF16, true>(const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const KernelParams&,
-                                                              int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<128, kDtBF16, false>(const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const KernelParams&,
-                                                              int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<128, kDtBF16, true>(const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const KernelParams&,
-                                                              int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<128, kDtE4M3, false>(const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const KernelParams&,
-                                                              int, cudaStream_t);
-extern template cudaError_t launch_fa_fwd<128, kDtE4M3, true>(const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const CUtensorMap&,
-                                                              const CUtensorMap&, const KernelParams&,
-                                                              int, cudaStream_t);
-}  // namespace fa
+#define FA_FWD_EXTERN_ALL_MODES(D, DT)                    \
+  FA_FWD_INSTANTIATE(extern, D, DT, fa::kModeDense)       \
+  FA_FWD_INSTANTIATE(extern, D, DT, fa::kModeSplit)       \
+  FA_FWD_INSTANTIATE(extern, D, DT, fa::kModeVarlen)      \
+  FA_FWD_INSTANTIATE(extern, D, DT, fa::kModePaged)
+FA_FWD_EXTERN_ALL_MODES(64, fa::kDtF16)
+FA_FWD_EXTERN_ALL_MODES(128, fa::kDtF16)
+FA_FWD_EXTERN_ALL_MODES(64, fa::kDtBF16)
+FA_FWD_EXTERN_ALL_MODES(128, fa::kDtBF16)
+FA_FWD_EXTERN_ALL_MODES(128, fa::kDtE4M3)
+#undef FA_FWD_EXTERN_ALL_MODES
 
 // Backward launchers live in fa_bwd_inst_*.cu.
 FA_BWD_INSTANTIATE(extern, 64, fa::bwd::kF16)
@@ -167,6 +136,29 @@ bool make_map_f32(CUtensorMap* m, const void* ptr, int64_t n, int64_t H, int64_t
   cuuint32_t box[4] = {32, 32, 1, 1}, estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Paged K/V cache [num_pages, page_size, H_kv, D]: map {D, H_kv, page_size,
+// num_pages}, boxes of min(page_size, 128) rows x 128 bytes of one head of one
+// page, 128-byte swizzle, zero fill out of bounds.
+bool make_map_paged(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, int64_t num_pages,
+                    int64_t page_size, int64_t H_kv, int64_t D) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const uint64_t eb = (dtype == FA_DTYPE_FP8E4M3) ? 1 : 2;
+  const CUtensorMapDataType t = dtype == FA_DTYPE_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                : dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H_kv),
+                        static_cast<cuuint64_t>(page_size), static_cast<cuuint64_t>(num_pages)};
+  cuuint64_t strides[3] = {D * eb, H_kv * D * eb, page_size * H_kv * D * eb};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), 1,
+                       static_cast<cuuint32_t>(page_size < 128 ? page_size : 128), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, t, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -330,9 +322,9 @@ fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, fl
   const int grid = static_cast<int>(p.num_units < dev.sm_count ? p.num_units : dev.sm_count);
   const bool sp = n_splits > 1;
   cudaError_t e;
-#define FA_LAUNCH(DD, DTY)                                                               \
-  (sp ? fa::launch_fa_fwd<DD, DTY, true>(mq, mk, mv, mo, mop, p, grid, stream)           \
-      : fa::launch_fa_fwd<DD, DTY, false>(mq, mk, mv, mo, mop, p, grid, stream))
+#define FA_LAUNCH(DD, DTY)                                                                     \
+  (sp ? fa::launch_fa_fwd<DD, DTY, fa::kModeSplit>(mq, mk, mv, mo, mop, p, grid, stream)       \
+      : fa::launch_fa_fwd<DD, DTY, fa::kModeDense>(mq, mk, mv, mo, mop, p, grid, stream))
   if (dtype == FA_DTYPE_F16)
     e = (D == 64) ? FA_LAUNCH(64, fa::kDtF16) : FA_LAUNCH(128, fa::kDtF16);
   else if (dtype == FA_DTYPE_BF16)
@@ -563,6 +555,138 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
                                                                 dout, lse, lse2, dsum, pq, pk,
                                                                 grid_q, grid_k, grid_p, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Varlen and paged forward passes: packed queries [total_q, H, D], one unit
+// per (sequence, head, pair of 128-row query tiles up to max_seqlen_q).
+fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int32_t* cu_q, const int32_t* cu_k, const int32_t* seqused_k,
+                    const int32_t* block_table, int64_t n_seqs, int64_t max_pages,
+                    int64_t page_size, int64_t num_pages, int64_t total_q, int64_t total_k,
+                    int64_t max_seqlen_q, int64_t H, int64_t H_kv, int64_t D, float scale,
+                    int causal, fa_dtype_t dtype, const float* descale_q, const float* descale_k,
+                    const float* descale_v, cudaStream_t stream) {
+  const bool paged = block_table != nullptr;
+  // ---- host-side checks: nothing below touches the device until they pass
+  if (!q || !k || !v || !o || !lse || !cu_q) return FA_ERR_INVALID_ARG;
+  if (paged ? !seqused_k : !cu_k) return FA_ERR_INVALID_ARG;
+  if (n_seqs < 1 || total_q < 0 || max_seqlen_q < 1 || H < 1 || D < 1) return FA_ERR_INVALID_ARG;
+  if (!paged && total_k < 0) return FA_ERR_INVALID_ARG;
+  if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+  if (causal < 0 || causal > 2) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP8E4M3)
+    return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.0f) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_FP8E4M3 && (descale_q || descale_k || descale_v)) return FA_ERR_INVALID_ARG;
+  if (paged) {
+    if (max_pages < 1 || num_pages < 1 || page_size < 16) return FA_ERR_INVALID_ARG;
+    if (!((page_size <= 128 && 128 % page_size == 0) || (page_size > 128 && page_size % 128 == 0)))
+      return FA_ERR_UNSUPPORTED;
+  }
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_FP8E4M3 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(cu_q, 4) || !aligned(cu_k, 4) || !aligned(seqused_k, 4) || !aligned(block_table, 4))
+    return FA_ERR_MISALIGNED;
+  if (dtype == FA_DTYPE_FP8E4M3 &&
+      (!aligned(descale_q, 4) || !aligned(descale_k, 4) || !aligned(descale_v, 4)))
+    return FA_ERR_MISALIGNED;
+  const int64_t kMaxRows = (int64_t(1) << 31) - 256;
+  if (total_q > kMaxRows || total_k > kMaxRows || max_seqlen_q > kMaxRows || H > INT32_MAX ||
+      n_seqs > INT32_MAX - 1 || max_pages > INT32_MAX || num_pages > INT32_MAX ||
+      page_size > 65536 || max_pages * page_size > kMaxRows)
+    return FA_ERR_UNSUPPORTED;
+  const int64_t n_pairs = ((max_seqlen_q + 127) / 128 + 1) / 2;
+  if (n_seqs * H > INT32_MAX / n_pairs) return FA_ERR_UNSUPPORTED;
+  if (total_q == 0) return FA_OK;  // no query rows: nothing to compute or write
+
+  DeviceInfo dev;
+  if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
+  const fa_dtype_t odt = (dtype == FA_DTYPE_F16) ? FA_DTYPE_F16 : FA_DTYPE_BF16;
+  CUtensorMap mq, mk, mv, mo;
+  bool ok = make_map(&mq, q, dtype, FA_LAYOUT_BSND, 1, H, total_q, D) &&
+            make_map(&mo, o, odt, FA_LAYOUT_BSND, 1, H, total_q, D, 32);
+  if (paged)
+    ok = ok && make_map_paged(&mk, k, dtype, num_pages, page_size, H_kv, D) &&
+         make_map_paged(&mv, v, dtype, num_pages, page_size, H_kv, D);
+  else
+    ok = ok && make_map(&mk, k, dtype, FA_LAYOUT_BSND, 1, H_kv, total_k > 0 ? total_k : 1, D) &&
+         make_map(&mv, v, dtype, FA_LAYOUT_BSND, 1, H_kv, total_k > 0 ? total_k : 1, D);
+  if (!ok) return FA_ERR_CUDA;
+
+  fa::KernelParams p = {};
+  p.B = 1; p.H = H; p.S_q = total_q; p.S_kv = paged ? 0 : total_k;
+  p.kv_group = static_cast<int32_t>(H / H_kv);
+  p.n_kv_blocks = 0;
+  p.n_pairs = static_cast<int32_t>(n_pairs);
+  p.num_units = static_cast<int32_t>(n_seqs * H * n_pairs);
+  p.group_heads = 1;
+  p.layout = 1;
+  p.causal = causal != 0 ? 1 : 0;
+  p.causal_br = causal == 2 ? 1 : 0;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.descale_q = descale_q;
+  p.descale_k = descale_k;
+  p.descale_v = descale_v;
+  p.o = o;
+  p.lse = lse;
+  p.err = dev.err_word;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.n_splits = 1;
+  p.lse_part = nullptr;
+  p.cu_q = cu_q;
+  p.cu_k = cu_k;
+  p.seqused_k = seqused_k;
+  p.block_table = block_table;
+  p.n_seqs = static_cast<int32_t>(n_seqs);
+  p.max_pages = static_cast<int32_t>(paged ? max_pages : 0);
+  p.page_size = static_cast<int32_t>(paged ? page_size : 0);
+
+  const int grid = static_cast<int>(p.num_units < dev.sm_count ? p.num_units : dev.sm_count);
+  cudaError_t e;
+#define FA_LAUNCH_VAR(DD, DTY)                                                                \
+  (paged ? fa::launch_fa_fwd<DD, DTY, fa::kModePaged>(mq, mk, mv, mo, mo, p, grid, stream)     \
+         : fa::launch_fa_fwd<DD, DTY, fa::kModeVarlen>(mq, mk, mv, mo, mo, p, grid, stream))
+  if (dtype == FA_DTYPE_F16)
+    e = (D == 64) ? FA_LAUNCH_VAR(64, fa::kDtF16) : FA_LAUNCH_VAR(128, fa::kDtF16);
+  else if (dtype == FA_DTYPE_BF16)
+    e = (D == 64) ? FA_LAUNCH_VAR(64, fa::kDtBF16) : FA_LAUNCH_VAR(128, fa::kDtBF16);
+  else
+    e = FA_LAUNCH_VAR(128, fa::kDtE4M3);
+#undef FA_LAUNCH_VAR
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                          const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                          int64_t n_seqs, int64_t total_q, int64_t total_k, int64_t max_seqlen_q,
+                          int64_t H, int64_t H_kv, int64_t D, float scale, int causal,
+                          fa_dtype_t dtype, const float* descale_q, const float* descale_k,
+                          const float* descale_v, cudaStream_t stream) {
+  return run_var(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, nullptr, nullptr, n_seqs, 0, 0, 0,
+                 total_q, total_k, max_seqlen_q, H, H_kv, D, scale, causal, dtype, descale_q,
+                 descale_k, descale_v, stream);
+}
+
+fa_status_t fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache, void* o,
+                         float* lse, const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                         const int32_t* block_table, int64_t n_seqs, int64_t max_pages_per_seq,
+                         int64_t page_size, int64_t num_pages, int64_t total_q,
+                         int64_t max_seqlen_q, int64_t H, int64_t H_kv, int64_t D, float scale,
+                         int causal, fa_dtype_t dtype, const float* descale_q,
+                         const float* descale_k, const float* descale_v, cudaStream_t stream) {
+  if (!block_table) return FA_ERR_INVALID_ARG;
+  return run_var(q, k_cache, v_cache, o, lse, cu_seqlens_q, nullptr, seqused_k, block_table,
+                 n_seqs, max_pages_per_seq, page_size, num_pages, total_q, 0, max_seqlen_q, H,
+                 H_kv, D, scale, causal, dtype, descale_q, descale_k, descale_v, stream);
 }
 
 }  // extern "C"

@@ -1,14 +1,6 @@
-// Kernel instantiations for e4m3 inputs (one translation unit per element
-// type so the library builds in parallel).
+// Forward kernel instantiations for e4m3 inputs, dense and split-KV modes (one
+// translation unit per element type and mode group so the library builds in parallel).
 #include "fa_kernel.cuh"
 
-namespace fa {
-template cudaError_t launch_fa_fwd<128, kDtE4M3, false>(const CUtensorMap&, const CUtensorMap&,
-                                                       const CUtensorMap&, const CUtensorMap&,
-                                                       const CUtensorMap&, const KernelParams&,
-                                                       int, cudaStream_t);
-template cudaError_t launch_fa_fwd<128, kDtE4M3, true>(const CUtensorMap&, const CUtensorMap&,
-                                                       const CUtensorMap&, const CUtensorMap&,
-                                                       const CUtensorMap&, const KernelParams&,
-                                                       int, cudaStream_t);
-}  // namespace fa
+FA_FWD_INSTANTIATE(, 128, fa::kDtE4M3, fa::kModeDense)
+FA_FWD_INSTANTIATE(, 128, fa::kDtE4M3, fa::kModeSplit)

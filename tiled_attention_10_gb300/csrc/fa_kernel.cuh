@@ -64,11 +64,16 @@ constexpr int kBN = 128;  // key/value rows per tile
 constexpr int kThreads = 384;
 // Registers per thread after setmaxnreg: softmax warpgroups / control
 // warpgroup; 256 * softmax + 128 * control = 384 * 168 (the launch budget).
-// The split-KV kernel's control roles decode more per item and need more.
-template <bool kSplit>
+// The split-KV, varlen and paged kernels' control roles decode more per item
+// and need more.
+// Kernel modes: the whole pass over dense [B,H,S,D] tensors, the split-KV
+// pass (partials in a workspace), packed variable-length sequences, and
+// packed queries against a paged K/V cache.
+constexpr int kModeDense = 0, kModeSplit = 1, kModeVarlen = 2, kModePaged = 3;
+template <bool kWide>
 struct RegSplit {
-  static constexpr uint32_t kSoftmax = kSplit ? 200 : 216;
-  static constexpr uint32_t kControl = kSplit ? 104 : 72;
+  static constexpr uint32_t kSoftmax = kWide ? 200 : 216;
+  static constexpr uint32_t kControl = kWide ? 104 : 72;
   static_assert(256 * kSoftmax + 128 * kControl == 384 * 168, "register budget");
 };
 constexpr int kProducerWarp = 8;
@@ -95,6 +100,14 @@ struct KernelParams {
   uint64_t wait_limit_ns;
   int32_t n_splits;     // K/V splits per unit (1: no split; outputs go to o / lse)
   float* lse_part;      // split > 1: fp32 [n_splits, B, H, S_q] partial log-sum-exp
+  // Varlen / paged modes (B = 1; S_q = total_q rows of q / o, lse is [H, total_q]).
+  const int32_t* cu_q;         // [n_seqs + 1] query row offsets of each sequence
+  const int32_t* cu_k;         // [n_seqs + 1] key row offsets (varlen)
+  const int32_t* seqused_k;    // [n_seqs] keys of each sequence (paged)
+  const int32_t* block_table;  // [n_seqs, max_pages] page of each key block (paged)
+  int32_t n_seqs, max_pages, page_size;
+  int32_t causal_br;           // causal mask aligned bottom-right (key j visible to
+                               // query i iff j <= i + S_kv - S_q)
 };
 
 template <int D, int DT>
@@ -167,11 +180,63 @@ __device__ __forceinline__ int tile_kv_blocks(const KernelParams& p, int q_tile)
 struct Item {
   int bh, pair, split, lo;
   int n[2];
+  // Varlen / paged modes: the unit's sequence, its query / key lengths, the
+  // packed row of its first query / key, and the causal offset (0 top-left,
+  // S_kv - S_q bottom-right).
+  int seq;
+  int64_t q_len, k_len, q_row0, k_row0, off;
 };
 
-template <bool kSplit>
+// K/V blocks that query tile q_tile of a sequence needs (varlen / paged).
+__device__ __forceinline__ int var_tile_kv_blocks(const KernelParams& p, const Item& it, int q_tile) {
+  const int64_t row0 = static_cast<int64_t>(q_tile) * kBM;
+  if (row0 >= it.q_len || it.k_len <= 0) return 0;
+  if (!p.causal) return static_cast<int>((it.k_len + kBN - 1) / kBN);
+  const int64_t last_row = min(row0 + (kBM - 1), it.q_len - 1);
+  const int64_t max_col = min(last_row + it.off, it.k_len - 1);
+  return max_col < 0 ? 0 : static_cast<int>(max_col / kBN) + 1;
+}
+
+template <int kMode>
 __device__ __forceinline__ Item decode_item(const KernelParams& p, int u) {
+  constexpr bool kSplit = kMode == kModeSplit;
   Item it;
+  if constexpr (kMode >= kModeVarlen) {
+    // unit = (sequence, head, query-tile pair); pairs past the sequence
+    // are empty.
+    const int per_seq = static_cast<int>(p.H) * p.n_pairs;
+    it.seq = u / per_seq;
+    const int rem = u - it.seq * per_seq;
+    it.bh = rem / p.n_pairs;
+    it.pair = rem - it.bh * p.n_pairs;
+    it.split = 0;
+    it.lo = 0;
+    // Lengths are clamped to what the tensors can hold, so that offsets
+    // that make no sense cost no more than a full pass and never move a
+    // store outside the outputs (stores also check rows against [0, S_q)).
+    const int64_t q0 = p.cu_q[it.seq], q1 = p.cu_q[it.seq + 1];
+    it.q_row0 = q0;
+    it.q_len = min(max(q1 - q0, int64_t(0)), p.S_q);
+    if constexpr (kMode == kModeVarlen) {
+      const int64_t k0 = p.cu_k[it.seq], k1 = p.cu_k[it.seq + 1];
+      it.k_row0 = k0;
+      it.k_len = min(max(k1 - k0, int64_t(0)), p.S_kv);
+    } else {
+      it.k_row0 = 0;
+      it.k_len = min(max(static_cast<int64_t>(p.seqused_k[it.seq]), int64_t(0)),
+                     static_cast<int64_t>(p.max_pages) * p.page_size);
+    }
+    it.off = p.causal_br ? it.k_len - it.q_len : 0;
+    it.n[0] = var_tile_kv_blocks(p, it, 2 * it.pair);
+    it.n[1] = var_tile_kv_blocks(p, it, 2 * it.pair + 1);
+    return it;
+  }
+  it.seq = 0;
+  it.q_len = p.S_q;
+  it.k_len = p.S_kv;
+  it.q_row0 = 0;
+  it.k_row0 = 0;
+  it.off = 0;
   const int unit = kSplit ? u / p.n_splits : u;
   it.split = kSplit ? u - unit * p.n_splits : 0;
   decode_unit(p, unit, it.bh, it.pair);
@@ -220,7 +285,31 @@ __device__ __forceinline__ void mbar_wait_teardown(uint32_t bar, uint32_t parity
 // ---------------------------------------------------------------------------
 // Producer (one thread): Q pair, then K_0, V_0, K_1, V_1, ... into the ring.
 // ---------------------------------------------------------------------------
-template <int D, int DT, bool kSplit>
+// Paged K/V: the 128 keys of block j of sequence `seq` come from one page
+// (page_size >= 128) or from 128 / page_size pages, one TMA box each.  Page
+// indices past the sequence's last page are clamped to it (their keys are
+// masked); the block table is read only within the sequence's pages.
+template <int D, int DT>
+__device__ __forceinline__ void paged_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                           const KernelParams& p, const Item& item, int j,
+                                           int32_t hk) {
+  using C = Cfg<D, DT>;
+  const int64_t key0 = static_cast<int64_t>(j) * kBN;
+  const int64_t n_pages = max((item.k_len + p.page_size - 1) / p.page_size, int64_t(1));
+  const int32_t* table = p.block_table + static_cast<int64_t>(item.seq) * p.max_pages;
+  const int rows = p.page_size < kBN ? p.page_size : kBN;
+  for (int sub = 0; sub < kBN / rows; ++sub) {
+    const int64_t key = key0 + static_cast<int64_t>(sub) * rows;
+    const int64_t pidx = min(min(key / p.page_size, n_pages - 1), int64_t(p.max_pages - 1));
+    const int32_t page = table[pidx];
+    const int32_t in_page = static_cast<int32_t>(key % p.page_size);
+    for (int c = 0; c < C::kChunks; ++c)
+      tma_load_4d(dst + c * C::kChunkBytes + sub * rows * 128, map, bar, c * C::kBoxElems, hk,
+                  in_page, page);
+  }
+}
+
+template <int D, int DT, int kMode>
 __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
                               const CUtensorMap* tmK, const CUtensorMap* tmV, uint32_t sQ,
                               uint32_t sRing, const Bars& bars, const WaitCtl& wc) {
@@ -231,7 +320,7 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
   for (int w = 0; ok; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
-    const Item item = decode_item<kSplit>(p, u);
+    const Item item = decode_item<kMode>(p, u);
     const int bh = item.bh, pair = item.pair;
     const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
     const int32_t hk = h / p.kv_group;  // key/value head of query head h
@@ -244,7 +333,7 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
       if ((t == 0 ? n0 : n1) == 0) continue;
       for (int c = 0; c < C::kChunks; ++c)
         tma_tile(sQ + t * C::kTileBytes + c * C::kChunkBytes, tmQ, bars.q_full(), p.layout,
-                 c * C::kBoxElems, (2 * pair + t) * kBM, h, b);
+                 c * C::kBoxElems, static_cast<int32_t>(item.q_row0) + (2 * pair + t) * kBM, h, b);
     }
     ++it;
     for (int j = 0; j < nmax && ok; ++j) {
@@ -253,9 +342,14 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
         if (!mbar_wait(bars.empty(slot), ((ring / C::kSlots) & 1u) ^ 1u, wc)) { ok = false; break; }
         mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
         const CUtensorMap* map = kv == 0 ? tmK : tmV;
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_tile(sRing + slot * C::kTileBytes + c * C::kChunkBytes, map, bars.full(slot),
-                   p.layout, c * C::kBoxElems, (item.lo + j) * kBN, hk, b);
+        if constexpr (kMode == kModePaged) {
+          paged_tile<D, DT>(sRing + slot * C::kTileBytes, map, bars.full(slot), p, item, j, hk);
+        } else {
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_tile(sRing + slot * C::kTileBytes + c * C::kChunkBytes, map, bars.full(slot),
+                     p.layout, c * C::kBoxElems,
+                     static_cast<int32_t>(item.k_row0) + (item.lo + j) * kBN, hk, b);
+        }
         ++ring;
       }
     }
@@ -318,7 +412,7 @@ struct RingPos {
   }
 };
 
-template <int D, int DT, bool kSplit>
+template <int D, int DT, int kMode>
 __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint32_t sRing,
                          const Bars& bars, const WaitCtl& wc) {
   using C = Cfg<D, DT>;
@@ -336,7 +430,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
   for (int w = 0; ok; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
-    const Item item = decode_item<kSplit>(p, u);
+    const Item item = decode_item<kMode>(p, u);
     const int n[2] = {item.n[0], item.n[1]};
     const int nmax = max(n[0], n[1]);
     if (nmax == 0) continue;
@@ -536,7 +630,14 @@ __device__ __forceinline__ float* lse_row_base(const KernelParams& p, int split,
   return p.lse_part + (static_cast<int64_t>(split) * p.B * p.H + bh) * p.S_q;
 }
 
-template <int D, int DT, bool kSplit>
+__device__ __forceinline__ void st_global_v4(void* ptr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+template <int D, int DT, int kMode>
 __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, const CUtensorMap* tmOp,
                              uint32_t tmem, uint32_t sEpi, int warp, int lane, const Bars& bars,
                              const WaitCtl& wc) {
@@ -547,7 +648,9 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t tS = tmem + lane_off + C::kTmemS + t * kBN;
   const uint32_t tO = tmem + lane_off + C::kTmemO + t * 128;
+  constexpr bool kSplit = kMode == kModeSplit;
   constexpr bool split = kSplit;
+  constexpr bool kVar = kMode >= kModeVarlen;
 
   float sl2 = p.scale_log2;
   float o_mul = 1.0f;
@@ -568,19 +671,29 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
   for (int w = 0;; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
-    const Item item = decode_item<kSplit>(p, u);
+    const Item item = decode_item<kMode>(p, u);
     const int bh = item.bh;
     const int q_tile = 2 * item.pair + t;
     const int n = t ? item.n[1] : item.n[0];
-    const int64_t row = static_cast<int64_t>(q_tile) * kBM + r;
+    const int64_t row = static_cast<int64_t>(q_tile) * kBM + r;  // row within the sequence
+    const int64_t q_len = item.q_len, k_len = item.k_len;
+    const int64_t tile_row0 = static_cast<int64_t>(q_tile) * kBM;
     if (n == 0) {
       // No key of this split is visible to this tile: an empty partial,
       // which the merge gives zero weight.
       if (split && row < p.S_q) lse_row_base<kSplit>(p, item.split, bh)[row] = -CUDART_INF_F;
+      // A varlen / paged tile whose rows see no key at all: O = 0, lse = -inf.
+      if (kVar && row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0) {
+        const int64_t grow = item.q_row0 + row;
+        uint8_t* orow = static_cast<uint8_t*>(p.o) + ((grow * p.H + bh) * D) * 2;
+        for (int c = 0; c < D / 8; ++c) st_global_v4(orow + 16 * c, 0u, 0u, 0u, 0u);
+        p.lse[static_cast<int64_t>(bh) * p.S_q + grow] = -CUDART_INF_F;
+      }
       continue;
     }
-    const int64_t col_end = p.causal ? min(row + 1, p.S_kv) : p.S_kv;  // columns < col_end visible
-    const int64_t tile_row0 = static_cast<int64_t>(q_tile) * kBM;
+    // Key j of the sequence is visible to this row iff j < col_end.
+    const int64_t col_end =
+        p.causal ? max(min(row + item.off + 1, k_len), int64_t(0)) : k_len;
 
     float m_run = -CUDART_INF_F, l = 0.0f;
     bool ok = true;
@@ -600,7 +713,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
 
       const int64_t col0 = static_cast<int64_t>(item.lo + j) * kBN;
       // Block-uniform: does any column of this block need a mask?
-      const bool masked = (col0 + kBN > p.S_kv) || (p.causal && col0 + (kBN - 1) > tile_row0);
+      const bool masked = (col0 + kBN > k_len) || (p.causal && col0 + (kBN - 1) > tile_row0 + item.off);
       const int lim = static_cast<int>(max(min(col_end - col0, static_cast<int64_t>(kBN)), int64_t(0)));
       if (masked)
         softmax_block<D, DT, true>(s, lim, j, sl2, m_run, l, tS, tO, bars, t);
@@ -616,7 +729,8 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     if (!mbar_wait(bars.o_done(t), o_phase, wc)) break;
     o_phase ^= 1u;
     tc_fence_after();
-    const float inv = o_mul / l;
+    // (A varlen / paged row that saw no key has l = 0: O = 0.)
+    const float inv = (kVar && l == 0.0f) ? 0.0f : o_mul / l;
     const int32_t box_row0 = q_tile * kBM + wq * 32;
     const uint32_t stage = sEpi + static_cast<uint32_t>(warp) * C::kEpiBoxBytes;
     const int n_boxes = split ? D / 32 : D / 64;
@@ -646,6 +760,20 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
           pk[16 + i] = (DT == kDtF16) ? pack_f16x2(c0, c1) : pack_bf16x2(c0, c1);
         }
       }
+      if constexpr (kVar) {
+        // A box that runs past the sequence's last row: per-row stores of
+        // the rows inside it (a TMA store would write the next sequence's).
+        if (box_row0 + 32 > q_len) {
+          if (row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0) {
+            uint8_t* orow = static_cast<uint8_t*>(p.o) +
+                            (((item.q_row0 + row) * p.H + bh) * D + 64 * bx) * 2;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st_global_v4(orow + 16 * q, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+          continue;
+        }
+      }
       // The previous TMA store from this staging box must have read it.
       if (lane == 0) bulk_wait_group_read0();
       __syncwarp();
@@ -655,8 +783,13 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
                      pk[4 * q + 2], pk[4 * q + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0 && box_row0 < p.S_q) {  // rows past S_q are clipped by the map
-        if (split)
+      // Rows past S_q are clipped by the map; a store never starts at a
+      // negative row.
+      if (lane == 0 && (kVar ? (item.q_row0 + box_row0 >= 0 && item.q_row0 + box_row0 < p.S_q)
+                             : box_row0 < p.S_q)) {
+        if (kVar)
+          tma_store_4d(tmO, stage, 64 * bx, h, static_cast<int32_t>(item.q_row0) + box_row0, 0);
+        else if (split)
           tma_store_4d(tmOp, stage, 32 * bx, box_row0, h, item.split * static_cast<int32_t>(p.B) + b);
         else if (p.layout == 0)
           tma_store_4d(tmO, stage, 64 * bx, box_row0, h, b);
@@ -665,7 +798,13 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
         bulk_commit_group();
       }
     }
-    if (row < p.S_q) lse_row_base<kSplit>(p, item.split, bh)[row] = (m_run + log2f(l)) * 0.69314718055994531f;
+    if constexpr (kVar) {
+      if (row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0)
+        p.lse[static_cast<int64_t>(bh) * p.S_q + item.q_row0 + row] =
+            l > 0.0f ? (m_run + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+    } else if (row < p.S_q) {
+      lse_row_base<kSplit>(p, item.split, bh)[row] = (m_run + log2f(l)) * 0.69314718055994531f;
+    }
     tc_fence_before();
   }
   // Every TMA store of this warp has completed before the CTA exits.
@@ -676,7 +815,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
 // ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
-template <int D, int DT, bool kSplit>
+template <int D, int DT, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -728,14 +867,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{p.wait_limit_ns, p.err, abort_flag};
 
   if (warp < kProducerWarp) {
-    reg_alloc_inc<RegSplit<kSplit>::kSoftmax>();
-    softmax_role<D, DT, kSplit>(p, &tmO, &tmOp, tmem, sEpi, warp, lane, bars, wc);
+    reg_alloc_inc<RegSplit<kMode != kModeDense>::kSoftmax>();
+    softmax_role<D, DT, kMode>(p, &tmO, &tmOp, tmem, sEpi, warp, lane, bars, wc);
   } else {
-    reg_alloc_dec<RegSplit<kSplit>::kControl>();
+    reg_alloc_dec<RegSplit<kMode != kModeDense>::kControl>();
     if (warp == kProducerWarp) {
-      if (lane == 0) producer_role<D, DT, kSplit>(p, &tmQ, &tmK, &tmV, sQ, sRing, bars, wc);
+      if (lane == 0) producer_role<D, DT, kMode>(p, &tmQ, &tmK, &tmV, sQ, sRing, bars, wc);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) mma_role<D, DT, kSplit>(p, tmem, sQ, sRing, bars, wc);
+      if (lane == 0) mma_role<D, DT, kMode>(p, tmem, sQ, sRing, bars, wc);
     }
   }
   __syncwarp();
@@ -747,13 +886,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Host-side launcher, one instantiation per (D, dtype, split mode).
-template <int D, int DT, bool kSplit>
+// Host-side launcher, one instantiation per (D, dtype, mode).
+template <int D, int DT, int kMode>
 cudaError_t launch_fa_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                           const CUtensorMap& o, const CUtensorMap& op, const KernelParams& p,
                           int grid, cudaStream_t stream) {
   using C = Cfg<D, DT>;
-  auto kern = fa_fwd_kernel<D, DT, kSplit>;
+  auto kern = fa_fwd_kernel<D, DT, kMode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -765,3 +904,9 @@ cudaError_t launch_fa_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
 }
 
 }  // namespace fa
+
+// Explicit instantiation (PREFIX empty) or its declaration (PREFIX extern).
+#define FA_FWD_INSTANTIATE(PREFIX, D, DT, MODE)                                              \
+  PREFIX template cudaError_t fa::launch_fa_fwd<D, DT, MODE>(                                \
+      const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,        \
+      const CUtensorMap&, const fa::KernelParams&, int, cudaStream_t);
