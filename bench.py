@@ -548,6 +548,198 @@ def run_ours_bwd(args, w, world, rank, local):
     return 0
 
 
+def packed_oracle_sample(w, x):
+    """Oracle on the packed workload's cheapest sequence (all heads): returns
+    (seconds, FLOPs of that sequence, description)."""
+    from oracle import varlen as ov
+    import numpy as np
+    cost = [sq * sk for sq, sk in zip(w.seq_q, w.seq_k)]
+    s = int(np.argmin(cost))
+    cu_q = x.cu_q.cpu().numpy()
+    t0 = time.perf_counter()
+    if w.page_size:
+        ov.attention_paged(x.q.cpu(), x.k.cpu(), x.v.cpu(), cu_q=cu_q,
+                           seqused_k=x.seqused_k.cpu().numpy(), block_table=x.block_table.cpu().numpy(),
+                           page_size=w.page_size, H=w.H, H_kv=w.H_kv, D=w.D, scale=w.softmax_scale,
+                           causal_mode=w.causal, dtype=w.dtype, descale=x.descale, seqs=[s])
+    else:
+        ov.attention_varlen(x.q.cpu(), x.k.cpu(), x.v.cpu(), cu_q=cu_q, cu_k=x.cu_k.cpu().numpy(),
+                            H=w.H, H_kv=w.H_kv, D=w.D, scale=w.softmax_scale, causal_mode=w.causal,
+                            dtype=w.dtype, descale=x.descale, seqs=[s])
+    t = time.perf_counter() - t0
+    one = type(w)(**{**w.__dict__, "seq_q": (w.seq_q[s],), "seq_k": (w.seq_k[s],)})
+    return t, one, f"sequence {s} ({w.seq_q[s]} x {w.seq_k[s]}), all {w.H} heads, float64 numpy"
+
+
+def run_reference_packed(args, w, world, rank):
+    """Reference arm for packed workloads: the float64 oracle on the cheapest
+    sequence of the batch per step."""
+    if rank != 0:
+        return 0
+    import oracle
+    from tiled_attention_10_gb300.inputs import make_packed_inputs
+    x = make_packed_inputs(w)
+    for _ in range(args.warmup):
+        packed_oracle_sample(w, x)
+    runs = [packed_oracle_sample(w, x) for _ in range(args.steps)]
+    t = sum(r[0] for r in runs) / len(runs)
+    one, sample = runs[0][1], runs[0][2]
+    if w.decode:
+        metric, unit, val = "attention decode GB/s", "GB/s", one.kv_bytes / t / 1e9
+    else:
+        metric, unit, val = "attention fwd TFLOP/s", "TFLOP/s", one.flops / t / 1e12
+    line = {"impl": "reference", "metric": metric, "value": round(val, 6), "unit": unit,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {**w.describe(), "sample_per_step": sample},
+            "cpu_baseline": {"value": round(val, 6), "unit": unit, "cores": oracle.max_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(val, 6), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours_packed(args, w, world, rank, local):
+    """Packed workloads: one step = one fa_fwd_varlen / fa_fwd_paged call."""
+    import torch
+    from tiled_attention_10_gb300 import binding
+    from tiled_attention_10_gb300.inputs import OUT_DTYPE, make_packed_inputs
+
+    binding.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if world > 1:
+        w = type(w)(**{**w.__dict__, "seed": w.seed + 1000 * rank})
+    x = make_packed_inputs(w, device=dev)
+    tq = sum(w.seq_q)
+    o = torch.empty(tq, w.H, w.D, dtype=OUT_DTYPE[w.dtype], device=dev)
+    lse = torch.empty(w.H, tq, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    ds = [None, None, None]
+    if w.dtype == "e4m3":
+        dst = [torch.tensor([d], dtype=torch.float32, device=dev) for d in x.descale]
+        ds = [t.data_ptr() for t in dst]
+
+    def step(qq=x.q, kk=x.k, vv=x.v):
+        if w.page_size:
+            st = binding.fa_fwd_paged(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr(), x.cu_q.data_ptr(), x.seqused_k.data_ptr(),
+                                      x.block_table.data_ptr(), len(w.seq_q), x.block_table.shape[1],
+                                      w.page_size, kk.shape[0], tq, max(w.seq_q), w.H, w.H_kv, w.D,
+                                      w.softmax_scale, w.causal, w.dtype, *ds, sp)
+        else:
+            st = binding.fa_fwd_varlen(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
+                                       lse.data_ptr(), x.cu_q.data_ptr(), x.cu_k.data_ptr(),
+                                       len(w.seq_q), tq, sum(w.seq_k), max(w.seq_q), w.H, w.H_kv,
+                                       w.D, w.softmax_scale, w.causal, w.dtype, *ds, sp)
+        if st != 0:
+            raise RuntimeError(f"packed forward: {binding.fa_status_string(st)}")
+
+    sampler = ClockSampler(local)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if binding.fa_last_device_error(sp) != 0:
+        raise RuntimeError("device-side error during warm-up")
+    barrier(world)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = ClockSampler.summarize(sampler.stop())
+    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    ms_max = max_over_ranks(total_ms / args.steps, world)
+    if binding.fa_last_device_error(sp) != 0:
+        raise RuntimeError("device-side error during the timed steps")
+
+    # End to end: pinned host Q and K / V (or caches) in, O and lse out.
+    hq, hk, hv = (t.cpu().pin_memory() for t in (x.q, x.k, x.v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    qd, kd, vd = torch.empty_like(x.q), torch.empty_like(x.k), torch.empty_like(x.v)
+
+    def e2e_step():
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        step(qd, kd, vd)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 20))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in (x.q, x.k, x.v))
+    d2h = o.numel() * o.element_size() + lse.numel() * 4
+    if rank != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    launch_ms = statistics.mean(per_launch)
+    q_bytes = x.q.numel() * x.q.element_size()
+    algo_bytes = w.kv_bytes + q_bytes + d2h       # K / V read once, Q read, O and lse written
+    if w.decode:
+        metric, unit = "attention decode GB/s", "GB/s"
+        value = world * algo_bytes / (ms_max * 1e-3) / 1e9
+        achieved = algo_bytes / (launch_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "algorithmic_bytes": algo_bytes,
+                "peak_source": f"{peak_src} HBM copy bandwidth"}
+        e2e_val = world * algo_bytes / (e2e_ms * 1e-3) / 1e9
+    else:
+        metric, unit = "attention fwd TFLOP/s", "TFLOP/s"
+        value = world * w.flops / (ms_max * 1e-3) / 1e12
+        achieved = w.flops / (launch_ms * 1e-3) / 1e12
+        sustained = total_ms > 1000.0
+        peak = tensor_peak(peaks, w.dtype, sustained)
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} bf16 GEMM"}
+        e2e_val = world * w.flops / (e2e_ms * 1e-3) / 1e12
+    line = {
+        "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {**w.describe(),
+                   "flops": "4*D*H per visible (query, key) pair",
+                   "l2": ("no flush: K/V exceed the 129 MB L2" if w.kv_bytes > (129 << 20)
+                          else "no flush: inputs fit in L2"),
+                   "parallelism": f"{world} independent shard(s), one per GPU"},
+        "roofline": roof,
+        "e2e": {"value": round(e2e_val, 3), "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        t, one, sample = packed_oracle_sample(w, make_packed_inputs(w))
+        val = (one.flops / t / 1e12) if not w.decode else (one.kv_bytes / t / 1e9)
+        line["cpu_baseline"] = {"value": round(val, 6), "unit": unit,
+                                "cores": oracle.max_threads(), "kind": "oracle",
+                                "sample": f"{sample}, {t:.2f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description="FlashAttention forward benchmark (libfa_b200)")
     ap.add_argument("--gpus", type=int, default=1)
@@ -559,10 +751,14 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    from tiled_attention_10_gb300.inputs import ALL_WORKLOADS, HEADLINE
-    w = ALL_WORKLOADS[args.workload or HEADLINE]
+    from tiled_attention_10_gb300.inputs import ALL_WORKLOADS, HEADLINE, PACKED_WORKLOADS
+    w = {**ALL_WORKLOADS, **PACKED_WORKLOADS}[args.workload or HEADLINE]
     world, rank, local = dist_setup()
     try:
+        if hasattr(w, "seq_q"):
+            if args.impl == "reference":
+                return run_reference_packed(args, w, world, rank)
+            return run_ours_packed(args, w, world, rank, local)
         if args.impl == "reference":
             return run_reference(args, w, world, rank)
         if w.bwd:

@@ -58,9 +58,11 @@ def attend(q, k, v, scale, causal_mode):
     return O, lse
 
 
-def _rows(x, dtype, heads, D):
-    a = decode(x, dtype).reshape(-1)
-    return a[: (a.size // (heads * D)) * heads * D].reshape(-1, heads, D)
+def _rows(x, dtype, heads, D, r0, r1):
+    """Rows [r0, r1) of a packed [rows, heads, D] buffer, decoded to float64."""
+    n = heads * D
+    flat = x.reshape(-1) if hasattr(x, "reshape") else x
+    return decode(flat[r0 * n: r1 * n], dtype).reshape(r1 - r0, heads, D)
 
 
 def attention_varlen(q, k, v, *, cu_q, cu_k, H, H_kv, D, scale, causal_mode, dtype,
@@ -69,17 +71,17 @@ def attention_varlen(q, k, v, *, cu_q, cu_k, H, H_kv, D, scale, causal_mode, dty
     raw buffers; cu_q, cu_k int arrays of n_seqs + 1 offsets.  Returns
     O [total_q, H, D] and lse [H, total_q] (float64); with `seqs` only those
     sequences are computed (other rows NaN)."""
-    Q = _rows(q, dtype, H, D) * descale[0]
-    K = _rows(k, dtype, H_kv, D) * descale[1]
-    V = _rows(v, dtype, H_kv, D) * descale[2]
-    total_q = Q.shape[0]
+    total_q = q.numel() // (H * D) if hasattr(q, "numel") else q.size // (H * D)
     O = np.full((total_q, H, D), np.nan)
     L = np.full((H, total_q), np.nan)
     g = H // H_kv
     for s in (range(len(cu_q) - 1) if seqs is None else seqs):
         q0, q1, k0, k1 = int(cu_q[s]), int(cu_q[s + 1]), int(cu_k[s]), int(cu_k[s + 1])
+        Q = _rows(q, dtype, H, D, q0, q1) * descale[0]
+        K = _rows(k, dtype, H_kv, D, k0, k1) * descale[1]
+        V = _rows(v, dtype, H_kv, D, k0, k1) * descale[2]
         for h in range(H):
-            o, l = attend(Q[q0:q1, h], K[k0:k1, h // g], V[k0:k1, h // g], scale, causal_mode)
+            o, l = attend(Q[:, h], K[:, h // g], V[:, h // g], scale, causal_mode)
             O[q0:q1, h] = o
             L[h, q0:q1] = l
     return O, L
@@ -88,10 +90,16 @@ def attention_varlen(q, k, v, *, cu_q, cu_k, H, H_kv, D, scale, causal_mode, dty
 def gather_pages(cache, dtype, block_table, s, n_keys, page_size, H_kv, D):
     """Keys 0..n_keys-1 of sequence s from a paged cache [num_pages,
     page_size, H_kv, D]: row j % page_size of page block_table[s][j // page_size]."""
-    C = decode(cache, dtype).reshape(-1, page_size, H_kv, D)
+    page_elems = page_size * H_kv * D
+    flat = cache.reshape(-1) if hasattr(cache, "reshape") else cache
+    pages = {}
     out = np.empty((n_keys, H_kv, D))
     for j in range(n_keys):
-        out[j] = C[int(block_table[s][j // page_size]), j % page_size]
+        pid = int(block_table[s][j // page_size])
+        if pid not in pages:
+            pages[pid] = decode(flat[pid * page_elems:(pid + 1) * page_elems],
+                                dtype).reshape(page_size, H_kv, D)
+        out[j] = pages[pid][j % page_size]
     return out
 
 
@@ -99,17 +107,17 @@ def attention_paged(q, k_cache, v_cache, *, cu_q, seqused_k, block_table, page_s
                     D, scale, causal_mode, dtype, descale=(1.0, 1.0, 1.0), seqs=None):
     """Packed queries against a paged K/V cache.  Returns O [total_q, H, D]
     and lse [H, total_q] (float64)."""
-    Q = _rows(q, dtype, H, D) * descale[0]
-    total_q = Q.shape[0]
+    total_q = q.numel() // (H * D) if hasattr(q, "numel") else q.size // (H * D)
     O = np.full((total_q, H, D), np.nan)
     L = np.full((H, total_q), np.nan)
     g = H // H_kv
     for s in (range(len(cu_q) - 1) if seqs is None else seqs):
         q0, q1, n = int(cu_q[s]), int(cu_q[s + 1]), int(seqused_k[s])
+        Q = _rows(q, dtype, H, D, q0, q1) * descale[0]
         K = gather_pages(k_cache, dtype, block_table, s, n, page_size, H_kv, D) * descale[1]
         V = gather_pages(v_cache, dtype, block_table, s, n, page_size, H_kv, D) * descale[2]
         for h in range(H):
-            o, l = attend(Q[q0:q1, h], K[:, h // g], V[:, h // g], scale, causal_mode)
+            o, l = attend(Q[:, h], K[:, h // g], V[:, h // g], scale, causal_mode)
             O[q0:q1, h] = o
             L[h, q0:q1] = l
     return O, L

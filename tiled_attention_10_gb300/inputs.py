@@ -15,6 +15,7 @@ from past the tail tile turns 0 * NaN into NaN inside the accumulator.
 from __future__ import annotations
 
 import dataclasses
+import itertools
 import math
 from typing import Optional
 
@@ -202,3 +203,134 @@ def make_dout(w: Workload, device="cpu") -> torch.Tensor:
     wd = dataclasses.replace(w, name=w.name + "/dO", S_kv=w.S_q, H_kv=None, seed=1000 + w.seed,
                              std=1.0, split=False, bwd=False)
     return make_inputs(wd, device=device).q
+
+
+# ---------------------------------------------------------------------------
+# Packed variable-length batches (varlen / paged K/V).
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass
+class PackedWorkload:
+    """A batch of sequences packed row after row: queries [total_q, H, D];
+    keys and values packed the same way (page_size 0) or in a paged cache
+    [num_pages, page_size, H_kv, D] whose pages are shuffled (seeded)."""
+    name: str
+    seq_q: tuple
+    seq_k: tuple
+    H: int
+    H_kv: int
+    D: int
+    dtype: str
+    causal: int             # 0 none, 1 top-left, 2 bottom-right
+    page_size: int = 0      # 0: contiguous packed K/V
+    seed: int = 0
+    std: float = 1.0
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def decode(self) -> bool:
+        return all(n == 1 for n in self.seq_q)
+
+    def visible_pairs(self) -> int:
+        """(query, key) pairs the masks leave, summed over sequences."""
+        tot = 0
+        for sq, sk in zip(self.seq_q, self.seq_k):
+            if self.causal == 0:
+                tot += sq * sk
+                continue
+            off = 0 if self.causal == 1 else sk - sq
+            for i in range(sq):
+                tot += max(0, min(sk, i + off + 1))
+        return tot
+
+    @property
+    def flops(self) -> float:
+        """4 * D * H FLOPs per visible (query, key) pair."""
+        return 4.0 * self.D * self.H * self.visible_pairs()
+
+    @property
+    def kv_bytes(self) -> int:
+        eb = 1 if self.dtype == "e4m3" else 2
+        return 2 * sum(self.seq_k) * self.H_kv * self.D * eb
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "n_seqs": len(self.seq_q), "total_q": sum(self.seq_q),
+                "total_k": sum(self.seq_k), "seq_q": f"{min(self.seq_q)}..{max(self.seq_q)}",
+                "seq_k": f"{min(self.seq_k)}..{max(self.seq_k)}", "H": self.H,
+                "H_kv": self.H_kv, "D": self.D, "dtype": self.dtype,
+                "causal": ["none", "top-left", "bottom-right"][self.causal],
+                "page_size": self.page_size or "contiguous",
+                "values": f"iid N(0,{self.std}^2), seed {self.seed}"}
+
+
+def _log_uniform_lengths(n, lo, hi, seed):
+    g = torch.Generator().manual_seed(seed)
+    u = torch.rand(n, generator=g, dtype=torch.float64)
+    return tuple(int(round(math.exp(math.log(lo) + float(x) * (math.log(hi) - math.log(lo)))))
+                 for x in u)
+
+
+PACKED_WORKLOADS = {
+    # training-style packed batch: 32 sequences, lengths log-uniform in [512, 8192]
+    "bf16_varlen_causal_32seq_512-8192_h32x128": PackedWorkload(
+        "bf16_varlen_causal_32seq_512-8192_h32x128", _log_uniform_lengths(32, 512, 8192, 11),
+        _log_uniform_lengths(32, 512, 8192, 11), 32, 32, 128, "bf16", 1),
+    # prefix prefill against a paged cache of 64-token pages (the page size of
+    # the Hygon retrospective's defect 11): 1024 new tokens after 7168 cached
+    "bf16_paged_prefill_8x1024of8192_p64_h32kv8": PackedWorkload(
+        "bf16_paged_prefill_8x1024of8192_p64_h32kv8", (1024,) * 8, (8192,) * 8, 32, 8, 128,
+        "bf16", 2, page_size=64),
+    # decode: one new token per sequence, cached lengths log-uniform in [1K, 32K]
+    "bf16_paged_decode_128seq_1k-32k_p64_h32kv8": PackedWorkload(
+        "bf16_paged_decode_128seq_1k-32k_p64_h32kv8", (1,) * 128,
+        _log_uniform_lengths(128, 1024, 32768, 12), 32, 8, 128, "bf16", 2, page_size=64),
+}
+
+
+@dataclasses.dataclass
+class PackedInputs:
+    q: torch.Tensor
+    k: torch.Tensor           # packed [total_k, H_kv, D] or cache [pages, page_size, H_kv, D]
+    v: torch.Tensor
+    cu_q: torch.Tensor        # int32 [n_seqs + 1]
+    cu_k: Optional[torch.Tensor]
+    seqused_k: Optional[torch.Tensor]
+    block_table: Optional[torch.Tensor]
+    descale: tuple
+
+
+def make_packed_inputs(w: PackedWorkload, device="cpu") -> PackedInputs:
+    """Seeded inputs of a packed workload (no attention arithmetic here)."""
+    tq, tk = sum(w.seq_q), sum(w.seq_k)
+    cu_q = torch.tensor([0] + list(itertools.accumulate(w.seq_q)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(itertools.accumulate(w.seq_k)), dtype=torch.int32)
+    q, dq = _cast(_draw((tq, w.H, w.D), w.std, 3 * w.seed, device), w.dtype)
+    k, dk = _cast(_draw((tk, w.H_kv, w.D), w.std, 3 * w.seed + 1, device), w.dtype)
+    v, dv = _cast(_draw((tk, w.H_kv, w.D), w.std, 3 * w.seed + 2, device), w.dtype)
+    if not w.page_size:
+        return PackedInputs(q, k, v, cu_q.to(device), cu_k.to(device), None, None, (dq, dk, dv))
+    ps = w.page_size
+    n_pages = [max(1, -(-n // ps)) for n in w.seq_k]
+    total_pages = sum(n_pages)
+    g = torch.Generator().manual_seed(1000 + w.seed)
+    phys = torch.randperm(total_pages, generator=g).tolist()
+    table = torch.zeros(len(w.seq_k), max(n_pages), dtype=torch.int32)
+    caches = []
+    for src in (k, v):
+        cache = torch.zeros((total_pages, ps, w.H_kv, w.D), dtype=src.dtype, device=device)
+        nxt = 0
+        for s, n in enumerate(w.seq_k):
+            base = int(cu_k[s])
+            for pg in range(n_pages[s]):
+                pid = phys[nxt]
+                nxt += 1
+                table[s, pg] = pid
+                lo, hi = base + pg * ps, base + min(n, (pg + 1) * ps)
+                if hi > lo:
+                    cache[pid, : hi - lo] = src[lo:hi]
+        caches.append(cache)
+    seqused = torch.tensor(w.seq_k, dtype=torch.int32)
+    return PackedInputs(q, caches[0], caches[1], cu_q.to(device), None, seqused.to(device),
+                        table.to(device), (dq, dk, dv))
