@@ -99,7 +99,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // sequence dimension is its own map dimension, so rows >= S are never read
 // (in BSND the bytes after row S-1 of batch b are batch b+1's rows).
 bool make_map(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, fa_layout_t layout, int64_t B,
-              int64_t H, int64_t S, int64_t D, cuuint32_t box_rows = 128) {
+              int64_t H, int64_t S, int64_t D, cuuint32_t box_rows = 128,
+              cuuint32_t box_heads = 1) {
   auto enc = encode_fn();
   if (!enc) return false;
   const uint64_t eb = (dtype == FA_DTYPE_FP8E4M3) ? 1 : 2;
@@ -116,7 +117,7 @@ bool make_map(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, fa_layout_t lay
   } else {
     dims[0] = D; dims[1] = H; dims[2] = S; dims[3] = B;
     strides[0] = D * eb; strides[1] = H * D * eb; strides[2] = S * H * D * eb;
-    box[0] = inner; box[1] = 1; box[2] = box_rows; box[3] = 1;
+    box[0] = inner; box[1] = box_heads; box[2] = box_rows; box[3] = 1;
   }
   CUresult r = enc(m, t, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -600,16 +601,27 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
       n_seqs > INT32_MAX - 1 || max_pages > INT32_MAX || num_pages > INT32_MAX ||
       page_size > 65536 || max_pages * page_size > kMaxRows)
     return FA_ERR_UNSUPPORTED;
-  const int64_t n_pairs = ((max_seqlen_q + 127) / 128 + 1) / 2;
-  if (n_seqs * H > INT32_MAX / n_pairs) return FA_ERR_UNSUPPORTED;
+  // GQA packing: the query heads that share a key/value head fill one tile
+  // together (2^shift heads x 128 >> shift tokens), so a K/V block is read
+  // once for all of them -- what makes decoding (one token per sequence)
+  // use more than one row of the 128.
+  const int64_t g = H / H_kv;
+  int shift = 0;
+  if (g > 1 && g <= 32 && (g & (g - 1)) == 0)
+    while ((int64_t(1) << shift) < g) ++shift;
+  const int64_t toks = 128 >> shift;
+  const int64_t n_pairs = ((max_seqlen_q + toks - 1) / toks + 1) / 2;
+  if (n_seqs * (H >> shift) > INT32_MAX / n_pairs) return FA_ERR_UNSUPPORTED;
   if (total_q == 0) return FA_OK;  // no query rows: nothing to compute or write
 
   DeviceInfo dev;
   if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
   const fa_dtype_t odt = (dtype == FA_DTYPE_F16) ? FA_DTYPE_F16 : FA_DTYPE_BF16;
   CUtensorMap mq, mk, mv, mo;
-  bool ok = make_map(&mq, q, dtype, FA_LAYOUT_BSND, 1, H, total_q, D) &&
-            make_map(&mo, o, odt, FA_LAYOUT_BSND, 1, H, total_q, D, 32);
+  bool ok = make_map(&mq, q, dtype, FA_LAYOUT_BSND, 1, H, total_q, D,
+                     static_cast<cuuint32_t>(toks), static_cast<cuuint32_t>(1 << shift)) &&
+            make_map(&mo, o, odt, FA_LAYOUT_BSND, 1, H, total_q, D,
+                     static_cast<cuuint32_t>(32 >> shift), static_cast<cuuint32_t>(1 << shift));
   if (paged)
     ok = ok && make_map_paged(&mk, k, dtype, num_pages, page_size, H_kv, D) &&
          make_map_paged(&mv, v, dtype, num_pages, page_size, H_kv, D);
@@ -623,8 +635,9 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
   p.kv_group = static_cast<int32_t>(H / H_kv);
   p.n_kv_blocks = 0;
   p.n_pairs = static_cast<int32_t>(n_pairs);
-  p.num_units = static_cast<int32_t>(n_seqs * H * n_pairs);
+  p.num_units = static_cast<int32_t>(n_seqs * (H >> shift) * n_pairs);
   p.group_heads = 1;
+  p.q_pack_log2 = shift;
   p.layout = 1;
   p.causal = causal != 0 ? 1 : 0;
   p.causal_br = causal == 2 ? 1 : 0;

@@ -106,6 +106,8 @@ struct KernelParams {
   const int32_t* seqused_k;    // [n_seqs] keys of each sequence (paged)
   const int32_t* block_table;  // [n_seqs, max_pages] page of each key block (paged)
   int32_t n_seqs, max_pages, page_size;
+  int32_t q_pack_log2;         // GQA packing: a query tile holds 2^q_pack_log2 heads of
+                               // each of 128 >> q_pack_log2 tokens (row = token * 2^.. + head)
   int32_t causal_br;           // causal mask aligned bottom-right (key j visible to
                                // query i iff j <= i + S_kv - S_q)
 };
@@ -187,12 +189,14 @@ struct Item {
   int64_t q_len, k_len, q_row0, k_row0, off;
 };
 
-// K/V blocks that query tile q_tile of a sequence needs (varlen / paged).
+// K/V blocks that query tile q_tile of a sequence needs (varlen / paged); the
+// tile covers tokens [q_tile * T, q_tile * T + T), T = 128 >> q_pack_log2.
 __device__ __forceinline__ int var_tile_kv_blocks(const KernelParams& p, const Item& it, int q_tile) {
-  const int64_t row0 = static_cast<int64_t>(q_tile) * kBM;
+  const int64_t tok_per_tile = kBM >> p.q_pack_log2;
+  const int64_t row0 = static_cast<int64_t>(q_tile) * tok_per_tile;
   if (row0 >= it.q_len || it.k_len <= 0) return 0;
   if (!p.causal) return static_cast<int>((it.k_len + kBN - 1) / kBN);
-  const int64_t last_row = min(row0 + (kBM - 1), it.q_len - 1);
+  const int64_t last_row = min(row0 + (tok_per_tile - 1), it.q_len - 1);
   const int64_t max_col = min(last_row + it.off, it.k_len - 1);
   return max_col < 0 ? 0 : static_cast<int>(max_col / kBN) + 1;
 }
@@ -202,13 +206,19 @@ __device__ __forceinline__ Item decode_item(const KernelParams& p, int u) {
   constexpr bool kSplit = kMode == kModeSplit;
   Item it;
   if constexpr (kMode >= kModeVarlen) {
-    // unit = (sequence, head, query-tile pair); pairs past the sequence
-    // are empty.
-    const int per_seq = static_cast<int>(p.H) * p.n_pairs;
-    it.seq = u / per_seq;
-    const int rem = u - it.seq * per_seq;
-    it.bh = rem / p.n_pairs;
-    it.pair = rem - it.bh * p.n_pairs;
+    // unit = (query-tile pair, sequence, head group), pairs outermost and
+    // the last pairs first: only long sequences have high pairs, and when
+    // causal a sequence's last pairs see the most keys, so the costliest
+    // units start early (longest-first order).  Pairs past a sequence's
+    // length are empty.  A head group is 2^q_pack_log2 query heads (those of
+    // one key/value head when packed, else one head); bh is its index.
+    const int groups = static_cast<int>(p.H) >> p.q_pack_log2;
+    const int per_rank = p.n_seqs * groups;
+    const int rank = u / per_rank;
+    const int rem = u - rank * per_rank;
+    it.seq = rem / groups;
+    it.bh = rem - it.seq * groups;
+    it.pair = p.n_pairs - 1 - rank;
     it.split = 0;
     it.lo = 0;
     // Lengths are clamped to what the tensors can hold, so that offsets
@@ -322,8 +332,12 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
     if (u >= p.num_units) break;
     const Item item = decode_item<kMode>(p, u);
     const int bh = item.bh, pair = item.pair;
-    const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
+    // First query head of the tile (varlen / paged: of the head group) and
+    // its key/value head; the Q tile's first row.
+    const int32_t b = kMode >= kModeVarlen ? 0 : static_cast<int32_t>(bh / p.H);
+    const int32_t h = kMode >= kModeVarlen ? (bh << p.q_pack_log2) : static_cast<int32_t>(bh % p.H);
     const int32_t hk = h / p.kv_group;  // key/value head of query head h
+    const int32_t tok_per_tile = kMode >= kModeVarlen ? (kBM >> p.q_pack_log2) : kBM;
     const int n0 = item.n[0], n1 = item.n[1];
     const int nmax = max(n0, n1);
     if (nmax == 0) continue;            // an empty split: no MMA work
@@ -333,7 +347,8 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
       if ((t == 0 ? n0 : n1) == 0) continue;
       for (int c = 0; c < C::kChunks; ++c)
         tma_tile(sQ + t * C::kTileBytes + c * C::kChunkBytes, tmQ, bars.q_full(), p.layout,
-                 c * C::kBoxElems, static_cast<int32_t>(item.q_row0) + (2 * pair + t) * kBM, h, b);
+                 c * C::kBoxElems, static_cast<int32_t>(item.q_row0) + (2 * pair + t) * tok_per_tile,
+                 h, b);
     }
     ++it;
     for (int j = 0; j < nmax && ok; ++j) {
@@ -675,9 +690,13 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     const int bh = item.bh;
     const int q_tile = 2 * item.pair + t;
     const int n = t ? item.n[1] : item.n[0];
-    const int64_t row = static_cast<int64_t>(q_tile) * kBM + r;  // row within the sequence
+    // Tile rows are tokens (dense, split: 128 of one head); varlen / paged
+    // with GQA packing: 2^shift heads of each of 128 >> shift tokens.
+    const int shift = kVar ? p.q_pack_log2 : 0;
+    const int64_t tile_row0 = static_cast<int64_t>(q_tile) * (kBM >> shift);  // first token
+    const int64_t row = tile_row0 + (r >> shift);                              // this row's token
+    const int hrow = kVar ? (bh << shift) + (r & ((1 << shift) - 1)) : bh;     // and its head
     const int64_t q_len = item.q_len, k_len = item.k_len;
-    const int64_t tile_row0 = static_cast<int64_t>(q_tile) * kBM;
     if (n == 0) {
       // No key of this split is visible to this tile: an empty partial,
       // which the merge gives zero weight.
@@ -685,9 +704,9 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
       // A varlen / paged tile whose rows see no key at all: O = 0, lse = -inf.
       if (kVar && row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0) {
         const int64_t grow = item.q_row0 + row;
-        uint8_t* orow = static_cast<uint8_t*>(p.o) + ((grow * p.H + bh) * D) * 2;
+        uint8_t* orow = static_cast<uint8_t*>(p.o) + ((grow * p.H + hrow) * D) * 2;
         for (int c = 0; c < D / 8; ++c) st_global_v4(orow + 16 * c, 0u, 0u, 0u, 0u);
-        p.lse[static_cast<int64_t>(bh) * p.S_q + grow] = -CUDART_INF_F;
+        p.lse[static_cast<int64_t>(hrow) * p.S_q + grow] = -CUDART_INF_F;
       }
       continue;
     }
@@ -731,7 +750,9 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     tc_fence_after();
     // (A varlen / paged row that saw no key has l = 0: O = 0.)
     const float inv = (kVar && l == 0.0f) ? 0.0f : o_mul / l;
-    const int32_t box_row0 = q_tile * kBM + wq * 32;
+    // This warp's 32 rows: tokens [box_row0, box_row0 + box_toks).
+    const int box_toks = 32 >> shift;
+    const int32_t box_row0 = static_cast<int32_t>(tile_row0) + wq * box_toks;
     const uint32_t stage = sEpi + static_cast<uint32_t>(warp) * C::kEpiBoxBytes;
     const int n_boxes = split ? D / 32 : D / 64;
     const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
@@ -763,10 +784,10 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
       if constexpr (kVar) {
         // A box that runs past the sequence's last row: per-row stores of
         // the rows inside it (a TMA store would write the next sequence's).
-        if (box_row0 + 32 > q_len) {
+        if (box_row0 + box_toks > q_len) {
           if (row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0) {
             uint8_t* orow = static_cast<uint8_t*>(p.o) +
-                            (((item.q_row0 + row) * p.H + bh) * D + 64 * bx) * 2;
+                            (((item.q_row0 + row) * p.H + hrow) * D + 64 * bx) * 2;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               st_global_v4(orow + 16 * q, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
@@ -788,7 +809,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
       if (lane == 0 && (kVar ? (item.q_row0 + box_row0 >= 0 && item.q_row0 + box_row0 < p.S_q)
                              : box_row0 < p.S_q)) {
         if (kVar)
-          tma_store_4d(tmO, stage, 64 * bx, h, static_cast<int32_t>(item.q_row0) + box_row0, 0);
+          tma_store_4d(tmO, stage, 64 * bx, bh << shift, static_cast<int32_t>(item.q_row0) + box_row0, 0);
         else if (split)
           tma_store_4d(tmOp, stage, 32 * bx, box_row0, h, item.split * static_cast<int32_t>(p.B) + b);
         else if (p.layout == 0)
@@ -800,7 +821,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     }
     if constexpr (kVar) {
       if (row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0)
-        p.lse[static_cast<int64_t>(bh) * p.S_q + item.q_row0 + row] =
+        p.lse[static_cast<int64_t>(hrow) * p.S_q + item.q_row0 + row] =
             l > 0.0f ? (m_run + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
     } else if (row < p.S_q) {
       lse_row_base<kSplit>(p, item.split, bh)[row] = (m_run + log2f(l)) * 0.69314718055994531f;
