@@ -482,12 +482,11 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
 
   DeviceInfo dev;
   if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
-  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv;
   if (!make_map(&mq, q, dtype, layout, B, H, S_q, D) ||
       !make_map(&mk, k, dtype, layout, B, H_kv, S_kv, D) ||
       !make_map(&mv, v, dtype, layout, B, H_kv, S_kv, D) ||
       !make_map(&mdo, dout, dtype, layout, B, H, S_q, D) ||
-      !make_map(&mdq, dq, dtype, layout, B, H, S_q, D, 32) ||
       !make_map(&mdk, dk, dtype, layout, B, H_kv, S_kv, D, 32) ||
       !make_map(&mdv, dv, dtype, layout, B, H_kv, S_kv, D, 32))
     return FA_ERR_CUDA;
@@ -542,17 +541,17 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
   const int grid_p = static_cast<int>(prep_blocks < 8ll * dev.sm_count ? prep_blocks : 8ll * dev.sm_count);
   cudaError_t e;
   if (dtype == FA_DTYPE_F16)
-    e = (D == 64) ? fa::bwd::launch_fa_bwd<64, fa::bwd::kF16>(mq, mk, mv, mdo, mdq, mdk, mdv, o, dout,
+    e = (D == 64) ? fa::bwd::launch_fa_bwd<64, fa::bwd::kF16>(mq, mk, mv, mdo, dq, mdk, mdv, o, dout,
                                                               lse, lse2, dsum, pq, pk, grid_q,
                                                               grid_k, grid_p, stream)
-                  : fa::bwd::launch_fa_bwd<128, fa::bwd::kF16>(mq, mk, mv, mdo, mdq, mdk, mdv, o,
+                  : fa::bwd::launch_fa_bwd<128, fa::bwd::kF16>(mq, mk, mv, mdo, dq, mdk, mdv, o,
                                                                dout, lse, lse2, dsum, pq, pk,
                                                                grid_q, grid_k, grid_p, stream);
   else
-    e = (D == 64) ? fa::bwd::launch_fa_bwd<64, fa::bwd::kBF16>(mq, mk, mv, mdo, mdq, mdk, mdv, o,
+    e = (D == 64) ? fa::bwd::launch_fa_bwd<64, fa::bwd::kBF16>(mq, mk, mv, mdo, dq, mdk, mdv, o,
                                                                dout, lse, lse2, dsum, pq, pk,
                                                                grid_q, grid_k, grid_p, stream)
-                  : fa::bwd::launch_fa_bwd<128, fa::bwd::kBF16>(mq, mk, mv, mdo, mdq, mdk, mdv, o,
+                  : fa::bwd::launch_fa_bwd<128, fa::bwd::kBF16>(mq, mk, mv, mdo, dq, mdk, mdv, o,
                                                                 dout, lse, lse2, dsum, pq, pk,
                                                                 grid_q, grid_k, grid_p, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

@@ -277,17 +277,20 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __rest
 // ===========================================================================
 // dQ kernel.
 // ===========================================================================
+// K and V stream through rings of their own: K_j is read by S_j and, a block
+// later in time, by dQ += dS_j K_j, so K needs three slots for K_{j+1} to be
+// in flight while K_{j-1} and K_j are still held; V_j is read by dP_j only.
 template <int D>
 struct DqCfg {
   using T = Tile<D>;
-  static constexpr int kSlots = T::kBytes >= 32768 ? 4 : 8;
+  static constexpr int kKSlots = T::kBytes >= 32768 ? 3 : 6;
+  static constexpr int kVSlots = T::kBytes >= 32768 ? 2 : 4;
   static constexpr int kQOff = 0;
   static constexpr int kDOOff = T::kBytes;
-  static constexpr int kRingOff = 2 * T::kBytes;
-  static constexpr int kEpiOff = kRingOff + kSlots * T::kBytes;
-  static constexpr int kEpiBox = 32 * 128;
-  static constexpr int kBarOff = kEpiOff + 8 * kEpiBox;
-  static constexpr int kNumBars = 2 * kSlots + 9;
+  static constexpr int kKOff = 2 * T::kBytes;
+  static constexpr int kVOff = kKOff + kKSlots * T::kBytes;
+  static constexpr int kBarOff = kVOff + kVSlots * T::kBytes;
+  static constexpr int kNumBars = 2 * (kKSlots + kVSlots) + 9;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
   // Requested at launch: more than half of an SM's shared memory, so that
@@ -299,33 +302,38 @@ struct DqCfg {
 
 struct DqBars {
   uint32_t base;
-  int ns;
-  __device__ uint32_t full(int s) const { return base + 8u * s; }
-  __device__ uint32_t empty(int s) const { return base + 8u * (ns + s); }
-  __device__ uint32_t q_full() const { return base + 8u * (2 * ns); }
-  __device__ uint32_t q_empty() const { return base + 8u * (2 * ns + 1); }
-  __device__ uint32_t s_full() const { return base + 8u * (2 * ns + 2); }
-  __device__ uint32_t s_free() const { return base + 8u * (2 * ns + 3); }
-  __device__ uint32_t dp_full() const { return base + 8u * (2 * ns + 4); }
-  __device__ uint32_t ds_ready() const { return base + 8u * (2 * ns + 5); }
-  __device__ uint32_t dq_done() const { return base + 8u * (2 * ns + 6); }
-  __device__ uint32_t dq_free() const { return base + 8u * (2 * ns + 7); }
-  __device__ uint32_t drain() const { return base + 8u * (2 * ns + 8); }
+  int nk, nv;
+  __device__ uint32_t kfull(int s) const { return base + 8u * s; }
+  __device__ uint32_t kempty(int s) const { return base + 8u * (nk + s); }
+  __device__ uint32_t vfull(int s) const { return base + 8u * (2 * nk + s); }
+  __device__ uint32_t vempty(int s) const { return base + 8u * (2 * nk + nv + s); }
+  __device__ uint32_t x(int i) const { return base + 8u * (2 * (nk + nv) + i); }
+  __device__ uint32_t q_full() const { return x(0); }
+  __device__ uint32_t q_empty() const { return x(1); }
+  __device__ uint32_t s_full() const { return x(2); }
+  __device__ uint32_t s_free() const { return x(3); }
+  __device__ uint32_t dp_full() const { return x(4); }
+  __device__ uint32_t ds_ready() const { return x(5); }
+  __device__ uint32_t dq_done() const { return x(6); }
+  __device__ uint32_t dq_free() const { return x(7); }
+  __device__ uint32_t drain() const { return x(8); }
 };
 
 __device__ __forceinline__ void dq_decode(const BwdParams& p, int u, int& bh, int& i) {
   decode_unit(u, static_cast<int>(p.B * p.H), p.n_q_tiles, p.group_heads, p.causal != 0, bh, i);
 }
 
-// Producer: Q_i and dO_i once per unit, then K_0, V_0, K_1, V_1, ... .
+// Producer: Q_i and dO_i once per unit, then K_0, V_0, K_1, V_1, ... into
+// their rings.
 template <int D>
 __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK,
                             const CUtensorMap* tmV, const CUtensorMap* tmDO, uint32_t smem,
                             const DqBars& bars, const WaitCtl& wc) {
   using C = DqCfg<D>;
   using T = Tile<D>;
-  Ring<C::kSlots> ring;
-  uint32_t issued = 0, it = 0;
+  Ring<C::kKSlots> kr;
+  Ring<C::kVSlots> vr;
+  uint32_t k_issued = 0, v_issued = 0, it = 0;
   bool ok = true;
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0; ok; ++w) {
@@ -346,23 +354,30 @@ __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
     }
     ++it;
     for (int j = 0; j < n && ok; ++j) {
-      for (int kv = 0; kv < 2; ++kv) {
-        if (!mbar_wait(bars.empty(ring.slot), ring.phase ^ 1u, wc)) { ok = false; break; }
-        mbar_arrive_expect_tx(bars.full(ring.slot), T::kBytes);
-        const uint32_t dst = smem + C::kRingOff + ring.slot * T::kBytes;
-        for (int c = 0; c < T::kChunks; ++c)
-          tma_tile(dst + c * T::kChunkBytes, kv == 0 ? tmK : tmV, bars.full(ring.slot), p.layout,
-                   c * 64, j * 128, hk, b);
-        ring.advance();
-        ++issued;
-      }
+      if (!mbar_wait(bars.kempty(kr.slot), kr.phase ^ 1u, wc)) { ok = false; break; }
+      mbar_arrive_expect_tx(bars.kfull(kr.slot), T::kBytes);
+      for (int c = 0; c < T::kChunks; ++c)
+        tma_tile(smem + C::kKOff + kr.slot * T::kBytes + c * T::kChunkBytes, tmK,
+                 bars.kfull(kr.slot), p.layout, c * 64, j * 128, hk, b);
+      kr.advance();
+      ++k_issued;
+      if (!mbar_wait(bars.vempty(vr.slot), vr.phase ^ 1u, wc)) { ok = false; break; }
+      mbar_arrive_expect_tx(bars.vfull(vr.slot), T::kBytes);
+      for (int c = 0; c < T::kChunks; ++c)
+        tma_tile(smem + C::kVOff + vr.slot * T::kBytes + c * T::kChunkBytes, tmV,
+                 bars.vfull(vr.slot), p.layout, c * 64, j * 128, hk, b);
+      vr.advance();
+      ++v_issued;
     }
   }
   if (!ok) {
     // Let loads already in flight land before the CTA's shared memory goes away.
-    const uint32_t first = issued > static_cast<uint32_t>(C::kSlots) ? issued - C::kSlots : 0u;
-    for (uint32_t r = first; r < issued; ++r)
-      mbar_wait_teardown(bars.full(r % C::kSlots), (r / C::kSlots) & 1u, 20000000ull);
+    const uint32_t fk = k_issued > static_cast<uint32_t>(C::kKSlots) ? k_issued - C::kKSlots : 0u;
+    for (uint32_t r = fk; r < k_issued; ++r)
+      mbar_wait_teardown(bars.kfull(r % C::kKSlots), (r / C::kKSlots) & 1u, 20000000ull);
+    const uint32_t fv = v_issued > static_cast<uint32_t>(C::kVSlots) ? v_issued - C::kVSlots : 0u;
+    for (uint32_t r = fv; r < v_issued; ++r)
+      mbar_wait_teardown(bars.vfull(r % C::kVSlots), (r / C::kVSlots) & 1u, 20000000ull);
     if (it > 0) mbar_wait_teardown(bars.q_full(), (it - 1) & 1u, 20000000ull);
   }
 }
@@ -406,10 +421,12 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
   constexpr uint32_t kTileW = T::kBytes >> 4;
   const uint32_t q_lo = umma_desc_lo(smem + C::kQOff, 16);
   const uint32_t do_lo = umma_desc_lo(smem + C::kDOOff, 16);
-  const uint32_t kmaj0 = umma_desc_lo(smem + C::kRingOff, 16);
-  const uint32_t mn0 = umma_desc_lo(smem + C::kRingOff, T::kChunkBytes);
+  const uint32_t k_kmaj0 = umma_desc_lo(smem + C::kKOff, 16);
+  const uint32_t k_mn0 = umma_desc_lo(smem + C::kKOff, T::kChunkBytes);
+  const uint32_t v_kmaj0 = umma_desc_lo(smem + C::kVOff, 16);
   const uint32_t tS = tmem + C::kS, tDP = tmem + C::kDP, tDQ = tmem + C::kDQ, tDS = tmem + C::kDS;
-  Ring<C::kSlots> ring;
+  Ring<C::kKSlots> kr;
+  Ring<C::kVSlots> vr;
   uint32_t it = 0, s_issued = 0, ds_ph = 0, units = 0;
   bool ok = true;
   const int grid = gridDim.x, bid = blockIdx.x;
@@ -422,34 +439,34 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
     if (!mbar_wait(bars.q_full(), it & 1u, wc)) { ok = false; break; }
     ++it;
     // S_0 = Q K_0^T once the softmax warps have read the previous S.
-    int slotK = ring.slot;
-    if (!mbar_wait(bars.full(slotK), ring.phase, wc)) { ok = false; break; }
-    ring.advance();
+    int slotK = kr.slot;
+    if (!mbar_wait(bars.kfull(slotK), kr.phase, wc)) { ok = false; break; }
+    kr.advance();
     if (s_issued > 0 && !mbar_wait(bars.s_free(), (s_issued - 1) & 1u, wc)) { ok = false; break; }
     tc_fence_after();
-    issue_ss<D, DT>(tS, q_lo, kmaj0 + slotK * kTileW);
+    issue_ss<D, DT>(tS, q_lo, k_kmaj0 + slotK * kTileW);
     umma_commit(bars.s_full());
     ++s_issued;
     // dP_0 = dO V_0^T.
     {
-      const int slotV = ring.slot;
-      if (!mbar_wait(bars.full(slotV), ring.phase, wc)) { ok = false; break; }
-      ring.advance();
+      const int slotV = vr.slot;
+      if (!mbar_wait(bars.vfull(slotV), vr.phase, wc)) { ok = false; break; }
+      vr.advance();
       tc_fence_after();
-      issue_ss<D, DT>(tDP, do_lo, kmaj0 + slotV * kTileW);
+      issue_ss<D, DT>(tDP, do_lo, v_kmaj0 + slotV * kTileW);
       umma_commit(bars.dp_full());
-      umma_commit(bars.empty(slotV));
+      umma_commit(bars.vempty(slotV));
     }
     for (int j = 0; j < n; ++j) {
       const bool has_next = j + 1 < n;
       int slotKn = slotK;
       if (has_next) {
-        slotKn = ring.slot;
-        if (!mbar_wait(bars.full(slotKn), ring.phase, wc)) { ok = false; break; }
-        ring.advance();
+        slotKn = kr.slot;
+        if (!mbar_wait(bars.kfull(slotKn), kr.phase, wc)) { ok = false; break; }
+        kr.advance();
         if (!mbar_wait(bars.s_free(), (s_issued - 1) & 1u, wc)) { ok = false; break; }
         tc_fence_after();
-        issue_ss<D, DT>(tS, q_lo, kmaj0 + slotKn * kTileW);
+        issue_ss<D, DT>(tS, q_lo, k_kmaj0 + slotKn * kTileW);
         umma_commit(bars.s_full());
         ++s_issued;
       }
@@ -459,16 +476,16 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
       ds_ph ^= 1u;
       if (j == 0 && units > 0 && !mbar_wait(bars.dq_free(), (units - 1) & 1u, wc)) { ok = false; break; }
       tc_fence_after();
-      issue_ts<D, DT, false>(tDQ, tDS, mn0 + slotK * kTileW, j > 0 ? 1u : 0u);
-      umma_commit(bars.empty(slotK));
+      issue_ts<D, DT, false>(tDQ, tDS, k_mn0 + slotK * kTileW, j > 0 ? 1u : 0u);
+      umma_commit(bars.kempty(slotK));
       if (has_next) {
-        const int slotV = ring.slot;
-        if (!mbar_wait(bars.full(slotV), ring.phase, wc)) { ok = false; break; }
-        ring.advance();
+        const int slotV = vr.slot;
+        if (!mbar_wait(bars.vfull(slotV), vr.phase, wc)) { ok = false; break; }
+        vr.advance();
         tc_fence_after();
-        issue_ss<D, DT>(tDP, do_lo, kmaj0 + slotV * kTileW);
+        issue_ss<D, DT>(tDP, do_lo, v_kmaj0 + slotV * kTileW);
         umma_commit(bars.dp_full());
-        umma_commit(bars.empty(slotV));
+        umma_commit(bars.vempty(slotV));
       }
       slotK = slotKn;
     }
@@ -481,10 +498,16 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
   mbar_wait_teardown(bars.drain(), 0u, ok ? 2000000000ull : 20000000ull);
 }
 
+__device__ __forceinline__ void st_global_v4(void* ptr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
 template <int D, int DT>
-__device__ void dq_softmax(const BwdParams& p, const CUtensorMap* tmDQ, uint32_t tmem,
-                           uint32_t sEpi, int warp, int lane, const DqBars& bars,
-                           const WaitCtl& wc) {
+__device__ void dq_softmax(const BwdParams& p, void* dq_out, uint32_t tmem, int warp, int lane,
+                           const DqBars& bars, const WaitCtl& wc) {
   using C = DqCfg<D>;
   const int quad = warp & 3, half = warp >> 2;
   const int r = quad * 32 + lane;
@@ -493,7 +516,6 @@ __device__ void dq_softmax(const BwdParams& p, const CUtensorMap* tmDQ, uint32_t
   const uint32_t tDP = tmem + lane_off + C::kDP + 64 * half;
   const uint32_t tDS = tmem + lane_off + C::kDS + 32 * half;
   const uint32_t tDQ = tmem + lane_off + C::kDQ;
-  const uint32_t stage = sEpi + static_cast<uint32_t>(warp) * C::kEpiBox;
   // A masked score is -inf and must give p = 0: keep the scale positive.
   const float sl2 = fmaxf(p.scale_log2, 1e-30f);
   uint32_t s_ph = 0, dp_ph = 0, dq_ph = 0;
@@ -557,41 +579,66 @@ __device__ void dq_softmax(const BwdParams& p, const CUtensorMap* tmDQ, uint32_t
       if (lane == 0) mbar_arrive(bars.ds_ready());
     }
     if (!ok) break;
-    // Epilogue: dQ = scale * (dS K), 16-bit, TMA store clipped at S_q.
+    // Epilogue: dQ = scale * (dS K), 16-bit, this thread's row written with
+    // 16-byte stores (rows past S_q are not written).
     if (!mbar_wait(bars.dq_done(), dq_ph, wc)) break;
     dq_ph ^= 1u;
     tc_fence_after();
-    const int32_t b = static_cast<int32_t>(bh / p.H), h = static_cast<int32_t>(bh % p.H);
-    const int32_t row0 = i * 128 + quad * 32;
-    if (D == 128 || half == 0)
-      store_box64<DT>(tDQ + 64 * half, p.scale, false, stage, lane, tmDQ, p.layout, 64 * half,
-                      row0, h, b, row0 < p.S_q);
+    if (D == 128 || half == 0) {
+      uint32_t a0[32], a1[32];
+      tmem_ld_x32(tDQ + 64 * half, a0);
+      tmem_ld_x32(tDQ + 64 * half + 32, a1);
+      tmem_wait_ld();
+      reg_dep_x32(a0);
+      reg_dep_x32(a1);
+      if (qi < p.S_q) {
+        const int64_t b = bh / p.H, h = bh - b * p.H;
+        const int64_t off = (p.layout == 0 ? ((bh * p.S_q + qi) * D) : (((b * p.S_q + qi) * p.H + h) * D)) +
+                            64 * half;
+        uint8_t* dst = static_cast<uint8_t*>(dq_out) + off * 2;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int c = 4 * q;
+          st_global_v4(dst + 16 * q,
+                       pack2<DT>(__uint_as_float((c < 16 ? a0 : a1)[(2 * c) & 31]) * p.scale,
+                                 __uint_as_float((c < 16 ? a0 : a1)[(2 * c + 1) & 31]) * p.scale),
+                       pack2<DT>(__uint_as_float((c < 16 ? a0 : a1)[(2 * c + 2) & 31]) * p.scale,
+                                 __uint_as_float((c < 16 ? a0 : a1)[(2 * c + 3) & 31]) * p.scale),
+                       pack2<DT>(__uint_as_float((c < 16 ? a0 : a1)[(2 * c + 4) & 31]) * p.scale,
+                                 __uint_as_float((c < 16 ? a0 : a1)[(2 * c + 5) & 31]) * p.scale),
+                       pack2<DT>(__uint_as_float((c < 16 ? a0 : a1)[(2 * c + 6) & 31]) * p.scale,
+                                 __uint_as_float((c < 16 ? a0 : a1)[(2 * c + 7) & 31]) * p.scale));
+        }
+      }
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.dq_free());
   }
-  if (lane == 0) bulk_wait_group0();
-  __syncwarp();
 }
 
 template <int D, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                     const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ BwdParams p) {
+                     void* dq_out, const __grid_constant__ BwdParams p) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const DqBars bars{base + static_cast<uint32_t>(C::kBarOff), C::kSlots};
+  const DqBars bars{base + static_cast<uint32_t>(C::kBarOff), C::kKSlots, C::kVSlots};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kBarOff + C::kNumBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(bars.full(s), 1);
-      mbar_init(bars.empty(s), 1);
+    for (int s = 0; s < C::kKSlots; ++s) {
+      mbar_init(bars.kfull(s), 1);
+      mbar_init(bars.kempty(s), 1);
+    }
+    for (int s = 0; s < C::kVSlots; ++s) {
+      mbar_init(bars.vfull(s), 1);
+      mbar_init(bars.vempty(s), 1);
     }
     mbar_init(bars.q_full(), 1);
     mbar_init(bars.q_empty(), 1);
@@ -610,7 +657,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
-    tma_prefetch_desc(&tmDQ);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -622,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{p.wait_limit_ns, p.err, abort_flag};
   if (warp < kProducerWarp) {
-    dq_softmax<D, DT>(p, &tmDQ, tmem, base + C::kEpiOff, warp, lane, bars, wc);
+    dq_softmax<D, DT>(p, dq_out, tmem, warp, lane, bars, wc);
   } else if (warp == kProducerWarp) {
     if (lane == 0) dq_producer<D>(p, &tmQ, &tmK, &tmV, &tmDO, base, bars, wc);
   } else if (warp == kMmaWarp) {
@@ -1030,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Host-side launchers (explicit instantiations in fa_bwd_inst_*.cu).
 template <int D, int DT>
 cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& dout, const CUtensorMap& dq, const CUtensorMap& dk,
+                          const CUtensorMap& dout, void* dq_ptr, const CUtensorMap& dk,
                           const CUtensorMap& dv, const void* o, const void* dout_ptr,
                           const float* lse, float* lse2, float* dsum, const BwdParams& p_dq,
                           const BwdParams& p_kv, int grid_dq, int grid_kv, int grid_prep,
@@ -1049,7 +1095,7 @@ cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = DqCfg<D>::kLaunchSmem;
     cfg.stream = stream;
-    e = cudaLaunchKernelEx(&cfg, kern, q, k, v, dout, dq, p_dq);
+    e = cudaLaunchKernelEx(&cfg, kern, q, k, v, dout, dq_ptr, p_dq);
     if (e != cudaSuccess) return e;
   }
   {
@@ -1072,7 +1118,7 @@ cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
 // Explicit instantiation (PREFIX empty) or its declaration (PREFIX extern).
 #define FA_BWD_INSTANTIATE(PREFIX, D, DT)                                                      \
   PREFIX template cudaError_t fa::bwd::launch_fa_bwd<D, DT>(                                   \
-      const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,          \
-      const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const void*, const void*,    \
+      const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, void*,   \
+      const CUtensorMap&, const CUtensorMap&, const void*, const void*,                        \
       const float*, float*, float*, const fa::bwd::BwdParams&, const fa::bwd::BwdParams&, int, \
       int, int, cudaStream_t);
