@@ -622,8 +622,21 @@ def run_ours_packed(args, w, world, rank, local):
         dst = [torch.tensor([d], dtype=torch.float32, device=dev) for d in x.descale]
         ds = [t.data_ptr() for t in dst]
 
+    ws, ws_bytes = None, 0
+    if w.page_size and w.n_splits > 1:   # workspace allocated outside the timed region
+        st, ws_bytes = binding.fa_fwd_paged_split_workspace_size(w.H, tq, w.D, w.n_splits)
+        ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+
     def step(qq=x.q, kk=x.k, vv=x.v):
-        if w.page_size:
+        if w.page_size and w.n_splits > 1:
+            st = binding.fa_fwd_paged_split(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(),
+                                            o.data_ptr(), lse.data_ptr(), x.cu_q.data_ptr(),
+                                            x.seqused_k.data_ptr(), x.block_table.data_ptr(),
+                                            len(w.seq_q), x.block_table.shape[1], w.page_size,
+                                            kk.shape[0], tq, max(w.seq_q), w.H, w.H_kv, w.D,
+                                            w.softmax_scale, w.causal, w.dtype, *ds, w.n_splits,
+                                            ws.data_ptr(), ws_bytes, sp)
+        elif w.page_size:
             st = binding.fa_fwd_paged(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
                                       lse.data_ptr(), x.cu_q.data_ptr(), x.seqused_k.data_ptr(),
                                       x.block_table.data_ptr(), len(w.seq_q), x.block_table.shape[1],
@@ -726,7 +739,7 @@ def run_ours_packed(args, w, world, rank, local):
         "roofline": roof,
         "e2e": {"value": round(e2e_val, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if (w.page_size and w.n_splits > 1) else 1),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

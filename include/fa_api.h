@@ -246,6 +246,37 @@ fa_status_t fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache
                          const float* descale_k, const float* descale_v, cudaStream_t stream);
 
 /*
+ * fa_fwd_paged_split -- fa_fwd_paged with each (sequence, query tile)'s keys
+ *   cut into n_splits chunks processed in parallel (fp32 partial O and lse
+ *   in `workspace`, then the merge kernel: lse = log sum_s exp(lse_s),
+ *   O = sum_s exp(lse_s - lse) O_s) -- the per-partition exp-sums and reduce
+ *   of the paged-decode kernels in the Hygon retrospective (defect 7).  For
+ *   decoding, where a few long sequences would otherwise leave most SMs
+ *   idle.  Splits past a sequence's last key block are empty and get zero
+ *   weight.  n_splits 1..32 (1: exactly fa_fwd_paged, workspace unused);
+ *   workspace: caller-owned device memory of at least
+ *   fa_fwd_paged_split_workspace_size bytes (fp32 [n_splits, H, total_q, D],
+ *   then fp32 [n_splits, H, total_q], each 256-byte aligned), 256-byte
+ *   aligned, contents on entry irrelevant.  Statuses as fa_fwd_paged plus
+ *   FA_ERR_INVALID_ARG (n_splits < 1, workspace missing or small),
+ *   FA_ERR_MISALIGNED (workspace off 256 bytes), FA_ERR_UNSUPPORTED
+ *   (n_splits > 32).  Two launches on `stream`; calls sharing a workspace
+ *   must not overlap.
+ */
+fa_status_t fa_fwd_paged_split_workspace_size(int64_t H, int64_t total_q, int64_t D, int n_splits,
+                                              size_t* workspace_bytes);
+
+fa_status_t fa_fwd_paged_split(const void* q, const void* k_cache, const void* v_cache, void* o,
+                               float* lse, const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                               const int32_t* block_table, int64_t n_seqs,
+                               int64_t max_pages_per_seq, int64_t page_size, int64_t num_pages,
+                               int64_t total_q, int64_t max_seqlen_q, int64_t H, int64_t H_kv,
+                               int64_t D, float scale, int causal, fa_dtype_t dtype,
+                               const float* descale_q, const float* descale_k,
+                               const float* descale_v, int n_splits, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Backward pass (fp16 / bf16): the gradients of the attention above with
  * respect to q, k and v, given the forward's o and lse and the upstream
  * gradient dout:

@@ -236,3 +236,59 @@ def test_varlen_host_checks(cuda_lib):
                                 "bf16") == 1    # no block table
     assert binding.fa_fwd_paged(a, a, a, a, a, a, a, a, 1, 0, 64, 4, 4, 4, 2, 2, 64, 0.1, 0,
                                 "bf16") == 1    # max pages 0
+
+
+def _paged_setup(case):
+    seq_q, seq_k, page_size, H, H_kv, D, dtype, causal = PAGED_CASES[case]
+    g = np.random.default_rng(200 + case)
+    cu_q = np.concatenate([[0], np.cumsum(seq_q)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(seq_k)]).astype(np.int32)
+    tq, tk = int(cu_q[-1]), int(cu_k[-1])
+    q, dq = _rand((tq, H, D), dtype, g)
+    k, dk = _rand((tk, H_kv, D), dtype, g)
+    v, dv = _rand((tk, H_kv, D), dtype, g)
+
+    def junk(shape):
+        x = torch.from_numpy((g.standard_normal(shape) * 100).astype(np.float32))
+        if dtype == "e4m3":
+            return (x / dk).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+        return x.to(TORCH_DTYPE[dtype])
+
+    kc, table = _paged_cache(k, seq_k, cu_k, page_size, H_kv, D, np.random.default_rng(7), junk)
+    vc, _ = _paged_cache(v, seq_k, cu_k, page_size, H_kv, D, np.random.default_rng(7), junk)
+    return dict(seq_q=seq_q, seq_k=seq_k, page_size=page_size, H=H, H_kv=H_kv, D=D, dtype=dtype,
+                causal=causal, cu_q=cu_q, tq=tq, q=q, kc=kc, vc=vc, table=table,
+                descale=(dq, dk, dv))
+
+
+@pytest.mark.parametrize("n_splits", [1, 2, 3, 7])
+@pytest.mark.parametrize("case", range(len(PAGED_CASES)))
+def test_paged_split_parity(case, n_splits, cuda_lib):
+    c = _paged_setup(case)
+    scale = 1.0 / np.sqrt(c["D"])
+    O, L = ov.attention_paged(c["q"], c["kc"], c["vc"], cu_q=c["cu_q"],
+                              seqused_k=np.array(c["seq_k"]), block_table=c["table"],
+                              page_size=c["page_size"], H=c["H"], H_kv=c["H_kv"], D=c["D"],
+                              scale=scale, causal_mode=c["causal"], dtype=c["dtype"],
+                              descale=c["descale"])
+    out = Out(c["tq"], c["H"], c["D"], c["dtype"])
+    keep, ds = _descale_ptrs(c["descale"], c["dtype"])
+    st, nb = binding.fa_fwd_paged_split_workspace_size(c["H"], c["tq"], c["D"], n_splits)
+    assert st == 0
+    ws = torch.full((nb // 4 + 64,), float("nan"), device="cuda")   # contents must not matter
+    cq = torch.from_numpy(c["cu_q"]).cuda()
+    sk = torch.tensor(c["seq_k"], dtype=torch.int32, device="cuda")
+    tb = torch.from_numpy(c["table"]).cuda()
+    qd, kcd, vcd = c["q"].cuda(), c["kc"].cuda(), c["vc"].cuda()
+    st = binding.fa_fwd_paged_split(qd.data_ptr(), kcd.data_ptr(), vcd.data_ptr(),
+                                    out.o.data_ptr(), out.lse.data_ptr(), cq.data_ptr(),
+                                    sk.data_ptr(), tb.data_ptr(), len(c["seq_q"]),
+                                    c["table"].shape[1], c["page_size"], c["kc"].shape[0], c["tq"],
+                                    max(c["seq_q"]), c["H"], c["H_kv"], c["D"], scale, c["causal"],
+                                    c["dtype"], *ds, n_splits, ws.data_ptr(), ws.numel() * 4)
+    torch.cuda.synchronize()
+    assert st == 0, binding.FA_STATUS.get(st)
+    assert binding.fa_last_device_error() == 0
+    assert out.guards_intact()
+    eo, el = _compare(O, L, out, c["cu_q"], c["dtype"])
+    print(f"paged split case {case} n_splits={n_splits}: max|dO|={eo:.3g} max|dlse|={el:.3g}")

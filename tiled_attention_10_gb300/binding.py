@@ -18,7 +18,7 @@ FA_STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
              3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
 # Symbols the header declares; the library must export all of them.
-EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_splitkv_noalloc", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd_varlen", "fa_fwd_paged", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
+EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_splitkv_noalloc", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd_varlen", "fa_fwd_paged", "fa_fwd_paged_split", "fa_fwd_paged_split_workspace_size", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
            "fa_probe_wait_timeout", "fa_version")
 
 _lib = None
@@ -65,6 +65,11 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd_varlen.restype = ip
     lib.fa_fwd_paged.argtypes = [vp] * 8 + [i64] * 9 + [f32, ip, ip, vp, vp, vp, vp]
     lib.fa_fwd_paged.restype = ip
+    lib.fa_fwd_paged_split.argtypes = [vp] * 8 + [i64] * 9 + [f32, ip, ip, vp, vp, vp, ip, vp, sz,
+                                                               vp]
+    lib.fa_fwd_paged_split.restype = ip
+    lib.fa_fwd_paged_split_workspace_size.argtypes = [i64, i64, i64, ip, ctypes.POINTER(sz)]
+    lib.fa_fwd_paged_split_workspace_size.restype = ip
     lib.fa_status_string.argtypes = [ip]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_device_error.argtypes = [vp]
@@ -191,6 +196,31 @@ def fa_fwd_paged(q, k_cache, v_cache, o, lse, cu_q, seqused_k, block_table, n_se
                                 int(n_seqs), int(max_pages), int(page_size), int(num_pages),
                                 int(total_q), int(max_seqlen_q), int(H), int(H_kv), int(D),
                                 float(scale), c, dt, descale_q, descale_k, descale_v, stream))
+
+
+def fa_fwd_paged_split_workspace_size(H, total_q, D, n_splits):
+    """(status, bytes) of workspace fa_fwd_paged_split needs."""
+    lib = load()
+    n = ctypes.c_size_t(0)
+    st = int(lib.fa_fwd_paged_split_workspace_size(int(H), int(total_q), int(D), int(n_splits),
+                                                   ctypes.byref(n)))
+    return st, int(n.value)
+
+
+def fa_fwd_paged_split(q, k_cache, v_cache, o, lse, cu_q, seqused_k, block_table, n_seqs,
+                       max_pages, page_size, num_pages, total_q, max_seqlen_q, H, H_kv, D, scale,
+                       causal, dtype, descale_q, descale_k, descale_v, n_splits, workspace,
+                       workspace_bytes, stream=None) -> int:
+    """Paged K/V forward with the keys split n_splits ways and merged."""
+    lib = load()
+    dt = FA_DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
+    c = CAUSAL[causal] if isinstance(causal, str) else int(causal)
+    return int(lib.fa_fwd_paged_split(q, k_cache, v_cache, o, lse, cu_q, seqused_k, block_table,
+                                      int(n_seqs), int(max_pages), int(page_size),
+                                      int(num_pages), int(total_q), int(max_seqlen_q), int(H),
+                                      int(H_kv), int(D), float(scale), c, dt, descale_q,
+                                      descale_k, descale_v, int(n_splits), workspace,
+                                      int(workspace_bytes), stream))
 
 
 def fa_last_device_error(stream=None) -> int:

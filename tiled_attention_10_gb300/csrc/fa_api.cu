@@ -30,7 +30,8 @@
   FA_FWD_INSTANTIATE(extern, D, DT, fa::kModeDense)       \
   FA_FWD_INSTANTIATE(extern, D, DT, fa::kModeSplit)       \
   FA_FWD_INSTANTIATE(extern, D, DT, fa::kModeVarlen)      \
-  FA_FWD_INSTANTIATE(extern, D, DT, fa::kModePaged)
+  FA_FWD_INSTANTIATE(extern, D, DT, fa::kModePaged)      \
+  FA_FWD_INSTANTIATE(extern, D, DT, fa::kModePagedSplit)
 FA_FWD_EXTERN_ALL_MODES(64, fa::kDtF16)
 FA_FWD_EXTERN_ALL_MODES(128, fa::kDtF16)
 FA_FWD_EXTERN_ALL_MODES(64, fa::kDtBF16)
@@ -125,16 +126,17 @@ bool make_map(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, fa_layout_t lay
   return r == CUDA_SUCCESS;
 }
 
-// fp32 partial-O map: [n, H, S, D] with n = n_splits * B, boxes of 32 rows x
-// 32 columns (128 bytes), 128-byte swizzle.
-bool make_map_f32(CUtensorMap* m, const void* ptr, int64_t n, int64_t H, int64_t S, int64_t D) {
+// fp32 partial-O map: [n, H, S, D] with n = n_splits * B, boxes of `box_rows`
+// rows of `box_heads` heads x 32 columns (128 bytes), 128-byte swizzle.
+bool make_map_f32(CUtensorMap* m, const void* ptr, int64_t n, int64_t H, int64_t S, int64_t D,
+                  cuuint32_t box_rows = 32, cuuint32_t box_heads = 1) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
                         static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(n)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(D * 4), static_cast<cuuint64_t>(S * D * 4),
                            static_cast<cuuint64_t>(H * S * D * 4)};
-  cuuint32_t box[4] = {32, 32, 1, 1}, estr[4] = {1, 1, 1, 1};
+  cuuint32_t box[4] = {32, box_rows, box_heads, 1}, estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(ptr), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -569,7 +571,8 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
                     int64_t page_size, int64_t num_pages, int64_t total_q, int64_t total_k,
                     int64_t max_seqlen_q, int64_t H, int64_t H_kv, int64_t D, float scale,
                     int causal, fa_dtype_t dtype, const float* descale_q, const float* descale_k,
-                    const float* descale_v, cudaStream_t stream) {
+                    const float* descale_v, cudaStream_t stream, int n_splits = 1,
+                    void* workspace = nullptr, size_t workspace_bytes = 0) {
   const bool paged = block_table != nullptr;
   // ---- host-side checks: nothing below touches the device until they pass
   if (!q || !k || !v || !o || !lse || !cu_q) return FA_ERR_INVALID_ARG;
@@ -611,6 +614,15 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
   const int64_t toks = 128 >> shift;
   const int64_t n_pairs = ((max_seqlen_q + toks - 1) / toks + 1) / 2;
   if (n_seqs * (H >> shift) > INT32_MAX / n_pairs) return FA_ERR_UNSUPPORTED;
+  if (n_splits < 1) return FA_ERR_INVALID_ARG;
+  if (n_splits > kMaxSplits) return FA_ERR_UNSUPPORTED;
+  if (n_splits > 1) {
+    if (!workspace || workspace_bytes < split_workspace_bytes(1, H, total_q, D, n_splits))
+      return FA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+    if (static_cast<double>(n_splits) * n_seqs * (H >> shift) * n_pairs > 2e9)
+      return FA_ERR_UNSUPPORTED;
+  }
   if (total_q == 0) return FA_OK;  // no query rows: nothing to compute or write
 
   DeviceInfo dev;
@@ -627,6 +639,19 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
   else
     ok = ok && make_map(&mk, k, dtype, FA_LAYOUT_BSND, 1, H_kv, total_k > 0 ? total_k : 1, D) &&
          make_map(&mv, v, dtype, FA_LAYOUT_BSND, 1, H_kv, total_k > 0 ? total_k : 1, D);
+  // Split partials: fp32 O [n_splits, H, total_q, D] then fp32 lse
+  // [n_splits, H, total_q]; a partial box holds the packed tile's heads x
+  // tokens.
+  CUtensorMap mop = mo;
+  float* o_part = nullptr;
+  float* lse_part = nullptr;
+  if (n_splits > 1) {
+    o_part = static_cast<float*>(workspace);
+    const size_t rows = static_cast<size_t>(n_splits) * H * total_q;
+    lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * D * 4 + 255) / 256 * 256);
+    ok = ok && make_map_f32(&mop, o_part, n_splits, H, total_q, D,
+                            static_cast<cuuint32_t>(32 >> shift), static_cast<cuuint32_t>(1 << shift));
+  }
   if (!ok) return FA_ERR_CUDA;
 
   fa::KernelParams p = {};
@@ -634,7 +659,7 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
   p.kv_group = static_cast<int32_t>(H / H_kv);
   p.n_kv_blocks = 0;
   p.n_pairs = static_cast<int32_t>(n_pairs);
-  p.num_units = static_cast<int32_t>(n_seqs * (H >> shift) * n_pairs);
+  p.num_units = static_cast<int32_t>(n_seqs * (H >> shift) * n_pairs * n_splits);
   p.group_heads = 1;
   p.q_pack_log2 = shift;
   p.layout = 1;
@@ -648,8 +673,9 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
   p.lse = lse;
   p.err = dev.err_word;
   p.wait_limit_ns = g_wait_limit_ns.load();
-  p.n_splits = 1;
-  p.lse_part = nullptr;
+  p.n_splits = n_splits;
+  p.lse_part = lse_part;
+  p.o_part = o_part;
   p.cu_q = cu_q;
   p.cu_k = cu_k;
   p.seqused_k = seqused_k;
@@ -660,9 +686,10 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
 
   const int grid = static_cast<int>(p.num_units < dev.sm_count ? p.num_units : dev.sm_count);
   cudaError_t e;
-#define FA_LAUNCH_VAR(DD, DTY)                                                                \
-  (paged ? fa::launch_fa_fwd<DD, DTY, fa::kModePaged>(mq, mk, mv, mo, mo, p, grid, stream)     \
-         : fa::launch_fa_fwd<DD, DTY, fa::kModeVarlen>(mq, mk, mv, mo, mo, p, grid, stream))
+#define FA_LAUNCH_VAR(DD, DTY)                                                                  \
+  (n_splits > 1 ? fa::launch_fa_fwd<DD, DTY, fa::kModePagedSplit>(mq, mk, mv, mo, mop, p, grid, stream) \
+   : paged      ? fa::launch_fa_fwd<DD, DTY, fa::kModePaged>(mq, mk, mv, mo, mo, p, grid, stream)    \
+                : fa::launch_fa_fwd<DD, DTY, fa::kModeVarlen>(mq, mk, mv, mo, mo, p, grid, stream))
   if (dtype == FA_DTYPE_F16)
     e = (D == 64) ? FA_LAUNCH_VAR(64, fa::kDtF16) : FA_LAUNCH_VAR(128, fa::kDtF16);
   else if (dtype == FA_DTYPE_BF16)
@@ -670,7 +697,21 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
   else
     e = FA_LAUNCH_VAR(128, fa::kDtE4M3);
 #undef FA_LAUNCH_VAR
-  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if (n_splits > 1) {
+    fa::CombineParams c = {};
+    c.o_part = o_part;
+    c.lse_part = lse_part;
+    c.o = o;
+    c.lse = lse;
+    c.B = 1; c.H = H; c.S_q = total_q;
+    c.D = static_cast<int32_t>(D);
+    c.n_splits = n_splits;
+    c.layout = 1;  // o is [total_q, H, D]: BSND with B = 1
+    c.out_f16 = dtype == FA_DTYPE_F16 ? 1 : 0;
+    if (fa::launch_fa_combine(c, dev.sm_count, stream) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return FA_OK;
 }
 
 }  // namespace
@@ -699,6 +740,33 @@ fa_status_t fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache
   return run_var(q, k_cache, v_cache, o, lse, cu_seqlens_q, nullptr, seqused_k, block_table,
                  n_seqs, max_pages_per_seq, page_size, num_pages, total_q, 0, max_seqlen_q, H,
                  H_kv, D, scale, causal, dtype, descale_q, descale_k, descale_v, stream);
+}
+
+}  // extern "C"
+
+extern "C" {
+
+fa_status_t fa_fwd_paged_split_workspace_size(int64_t H, int64_t total_q, int64_t D, int n_splits,
+                                              size_t* workspace_bytes) {
+  if (!workspace_bytes || H < 1 || total_q < 0 || D < 1 || n_splits < 1) return FA_ERR_INVALID_ARG;
+  *workspace_bytes = n_splits > 1 ? split_workspace_bytes(1, H, total_q, D, n_splits) : 0;
+  return FA_OK;
+}
+
+fa_status_t fa_fwd_paged_split(const void* q, const void* k_cache, const void* v_cache, void* o,
+                               float* lse, const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                               const int32_t* block_table, int64_t n_seqs,
+                               int64_t max_pages_per_seq, int64_t page_size, int64_t num_pages,
+                               int64_t total_q, int64_t max_seqlen_q, int64_t H, int64_t H_kv,
+                               int64_t D, float scale, int causal, fa_dtype_t dtype,
+                               const float* descale_q, const float* descale_k,
+                               const float* descale_v, int n_splits, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  if (!block_table) return FA_ERR_INVALID_ARG;
+  return run_var(q, k_cache, v_cache, o, lse, cu_seqlens_q, nullptr, seqused_k, block_table,
+                 n_seqs, max_pages_per_seq, page_size, num_pages, total_q, 0, max_seqlen_q, H,
+                 H_kv, D, scale, causal, dtype, descale_q, descale_k, descale_v, stream, n_splits,
+                 workspace, workspace_bytes);
 }
 
 }  // extern "C"

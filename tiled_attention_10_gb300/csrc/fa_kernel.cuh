@@ -70,6 +70,9 @@ constexpr int kThreads = 384;
 // pass (partials in a workspace), packed variable-length sequences, and
 // packed queries against a paged K/V cache.
 constexpr int kModeDense = 0, kModeSplit = 1, kModeVarlen = 2, kModePaged = 3;
+// Paged K/V with each unit's keys split into n_splits chunks (fp32 partials,
+// merged by the combine kernel): the partition-and-reduce of paged decoding.
+constexpr int kModePagedSplit = 4;
 template <bool kWide>
 struct RegSplit {
   static constexpr uint32_t kSoftmax = kWide ? 200 : 216;
@@ -100,6 +103,7 @@ struct KernelParams {
   uint64_t wait_limit_ns;
   int32_t n_splits;     // K/V splits per unit (1: no split; outputs go to o / lse)
   float* lse_part;      // split > 1: fp32 [n_splits, B, H, S_q] partial log-sum-exp
+  float* o_part;        // paged split: fp32 [n_splits, H, S_q, D] partial O (row stores)
   // Varlen / paged modes (B = 1; S_q = total_q rows of q / o, lse is [H, total_q]).
   const int32_t* cu_q;         // [n_seqs + 1] query row offsets of each sequence
   const int32_t* cu_k;         // [n_seqs + 1] key row offsets (varlen)
@@ -203,9 +207,13 @@ __device__ __forceinline__ int var_tile_kv_blocks(const KernelParams& p, const I
 
 template <int kMode>
 __device__ __forceinline__ Item decode_item(const KernelParams& p, int u) {
+  static_assert(kMode >= kModeDense && kMode <= kModePagedSplit, "kernel mode");
   constexpr bool kSplit = kMode == kModeSplit;
   Item it;
   if constexpr (kMode >= kModeVarlen) {
+    constexpr bool kVarSplit = kMode == kModePagedSplit;
+    const int split = kVarSplit ? u % p.n_splits : 0;
+    u = kVarSplit ? u / p.n_splits : u;
     // unit = (query-tile pair, sequence, head group), pairs outermost and
     // the last pairs first: only long sequences have high pairs, and when
     // causal a sequence's last pairs see the most keys, so the costliest
@@ -239,6 +247,17 @@ __device__ __forceinline__ Item decode_item(const KernelParams& p, int u) {
     it.off = p.causal_br ? it.k_len - it.q_len : 0;
     it.n[0] = var_tile_kv_blocks(p, it, 2 * it.pair);
     it.n[1] = var_tile_kv_blocks(p, it, 2 * it.pair + 1);
+    if constexpr (kVarSplit) {
+      // This item: key blocks [lo, lo + chunk) of the unit; a split past the
+      // sequence's blocks is empty (its partials get zero weight).
+      const int nmax = max(it.n[0], it.n[1]);
+      const int chunk = (nmax + p.n_splits - 1) / p.n_splits;
+      it.split = split;
+      it.lo = split * chunk;
+      const int hi = min(nmax, it.lo + chunk);
+      it.n[0] = max(0, min(it.n[0], hi) - it.lo);
+      it.n[1] = max(0, min(it.n[1], hi) - it.lo);
+    }
     return it;
   }
   it.seq = 0;
@@ -357,8 +376,9 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
         if (!mbar_wait(bars.empty(slot), ((ring / C::kSlots) & 1u) ^ 1u, wc)) { ok = false; break; }
         mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
         const CUtensorMap* map = kv == 0 ? tmK : tmV;
-        if constexpr (kMode == kModePaged) {
-          paged_tile<D, DT>(sRing + slot * C::kTileBytes, map, bars.full(slot), p, item, j, hk);
+        if constexpr (kMode == kModePaged || kMode == kModePagedSplit) {
+          paged_tile<D, DT>(sRing + slot * C::kTileBytes, map, bars.full(slot), p, item,
+                            item.lo + j, hk);
         } else {
           for (int c = 0; c < C::kChunks; ++c)
             tma_tile(sRing + slot * C::kTileBytes + c * C::kChunkBytes, map, bars.full(slot),
@@ -663,8 +683,9 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t tS = tmem + lane_off + C::kTmemS + t * kBN;
   const uint32_t tO = tmem + lane_off + C::kTmemO + t * 128;
-  constexpr bool kSplit = kMode == kModeSplit;
-  constexpr bool split = kSplit;
+  constexpr bool kVarSplit = kMode == kModePagedSplit;
+  constexpr bool kSplit = kMode == kModeSplit;    // dense split: [n*B, H, S_q, D] partials
+  constexpr bool split = kSplit || kVarSplit;     // fp32 partial O and lse
   constexpr bool kVar = kMode >= kModeVarlen;
 
   float sl2 = p.scale_log2;
@@ -700,9 +721,13 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     if (n == 0) {
       // No key of this split is visible to this tile: an empty partial,
       // which the merge gives zero weight.
-      if (split && row < p.S_q) lse_row_base<kSplit>(p, item.split, bh)[row] = -CUDART_INF_F;
+      if (kSplit && row < p.S_q) lse_row_base<kSplit>(p, item.split, bh)[row] = -CUDART_INF_F;
+      if (kVarSplit && row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0)
+        p.lse_part[(static_cast<int64_t>(item.split) * p.H + hrow) * p.S_q + item.q_row0 + row] =
+            -CUDART_INF_F;
       // A varlen / paged tile whose rows see no key at all: O = 0, lse = -inf.
-      if (kVar && row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0) {
+      if (kVar && !kVarSplit && row < q_len && item.q_row0 + row < p.S_q &&
+          item.q_row0 + row >= 0) {
         const int64_t grow = item.q_row0 + row;
         uint8_t* orow = static_cast<uint8_t*>(p.o) + ((grow * p.H + hrow) * D) * 2;
         for (int c = 0; c < D / 8; ++c) st_global_v4(orow + 16 * c, 0u, 0u, 0u, 0u);
@@ -786,8 +811,12 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
         // the rows inside it (a TMA store would write the next sequence's).
         if (box_row0 + box_toks > q_len) {
           if (row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0) {
-            uint8_t* orow = static_cast<uint8_t*>(p.o) +
-                            (((item.q_row0 + row) * p.H + hrow) * D + 64 * bx) * 2;
+            uint8_t* orow =
+                kVarSplit ? reinterpret_cast<uint8_t*>(
+                                p.o_part + ((static_cast<int64_t>(item.split) * p.H + hrow) * p.S_q +
+                                            item.q_row0 + row) * D + 32 * bx)
+                          : static_cast<uint8_t*>(p.o) +
+                                (((item.q_row0 + row) * p.H + hrow) * D + 64 * bx) * 2;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
               st_global_v4(orow + 16 * q, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
@@ -798,9 +827,13 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
       // The previous TMA store from this staging box must have read it.
       if (lane == 0) bulk_wait_group_read0();
       __syncwarp();
+      // Staging row of this thread's row: the box's element order.  The
+      // head-major partial box of a packed tile (heads x tokens) takes row
+      // (head, token); every other box is in lane order.
+      const int srow = kVarSplit ? ((lane & ((1 << shift) - 1)) * box_toks + (lane >> shift)) : lane;
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        st_shared_v4(stage + lane * 128 + ((q ^ (lane & 7)) << 4), pk[4 * q], pk[4 * q + 1],
+        st_shared_v4(stage + srow * 128 + ((q ^ (srow & 7)) << 4), pk[4 * q], pk[4 * q + 1],
                      pk[4 * q + 2], pk[4 * q + 3]);
       fence_proxy_async_smem();
       __syncwarp();
@@ -808,7 +841,10 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
       // negative row.
       if (lane == 0 && (kVar ? (item.q_row0 + box_row0 >= 0 && item.q_row0 + box_row0 < p.S_q)
                              : box_row0 < p.S_q)) {
-        if (kVar)
+        if (kVarSplit)
+          tma_store_4d(tmOp, stage, 32 * bx, static_cast<int32_t>(item.q_row0) + box_row0,
+                       bh << shift, item.split);
+        else if (kVar)
           tma_store_4d(tmO, stage, 64 * bx, bh << shift, static_cast<int32_t>(item.q_row0) + box_row0, 0);
         else if (split)
           tma_store_4d(tmOp, stage, 32 * bx, box_row0, h, item.split * static_cast<int32_t>(p.B) + b);
@@ -820,8 +856,9 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
       }
     }
     if constexpr (kVar) {
+      float* lse_dst = kVarSplit ? p.lse_part + static_cast<int64_t>(item.split) * p.H * p.S_q : p.lse;
       if (row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0)
-        p.lse[static_cast<int64_t>(hrow) * p.S_q + item.q_row0 + row] =
+        lse_dst[static_cast<int64_t>(hrow) * p.S_q + item.q_row0 + row] =
             l > 0.0f ? (m_run + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
     } else if (row < p.S_q) {
       lse_row_base<kSplit>(p, item.split, bh)[row] = (m_run + log2f(l)) * 0.69314718055994531f;
