@@ -290,6 +290,12 @@ PACKED_WORKLOADS = {
         "bf16_paged_decode_128seq_1k-32k_p64_h32kv8", (1,) * 128,
         _log_uniform_lengths(128, 1024, 32768, 12), 32, 8, 128, "bf16", 2, page_size=64,
         n_splits=2),
+    # the same decode at a quarter of the cache (about 1 GB of K/V): the size
+    # the detailed profiler captures are taken on
+    "bf16_paged_decode_32seq_1k-32k_p64_h32kv8": PackedWorkload(
+        "bf16_paged_decode_32seq_1k-32k_p64_h32kv8", (1,) * 32,
+        _log_uniform_lengths(32, 1024, 32768, 12), 32, 8, 128, "bf16", 2, page_size=64,
+        n_splits=2),
 }
 
 
