@@ -315,6 +315,37 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
                    fa_layout_t layout, int causal, fa_dtype_t dtype, void* workspace,
                    size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * Strided tensors.  fa_strides_t gives a [B, H, S, D] tensor's element strides
+ * along batch, head and sequence; D is contiguous.  Any layout follows: BNSD,
+ * BSND, views of a fused QKV projection ([B, S, 3, H, D]: seq stride 3*H*D),
+ * padded rows, or K and V with different strides -- the Hygon retrospective's
+ * backward defect 13 came from stepping V by K's row stride, which passed
+ * every test in which the two were equal.  Each stride * element size must
+ * be a positive multiple of 16 bytes (a TMA requirement): FA_ERR_MISALIGNED
+ * otherwise, FA_ERR_INVALID_ARG for a stride < 1 or a NULL array,
+ * FA_ERR_UNSUPPORTED at or above 2^39 bytes.  lse stays dense [B, H, S_q].
+ *
+ * fa_fwd_strided -- fa_fwd_gqa with strides[0..3] = q, k, v, o.
+ * fa_bwd_strided -- fa_bwd with strides[0..7] = q, k, v, o, dout, dq, dk, dv.
+ */
+typedef struct {
+  int64_t batch, head, seq;
+} fa_strides_t;
+
+fa_status_t fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv,
+                           int64_t D, const fa_strides_t* strides, float scale, int causal,
+                           fa_dtype_t dtype, const float* descale_q, const float* descale_k,
+                           const float* descale_v, cudaStream_t stream);
+
+fa_status_t fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv,
+                           int64_t D, const fa_strides_t* strides, float scale, int causal,
+                           fa_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
 /* A static, human-readable name for a status code (never NULL). */
 const char* fa_status_string(fa_status_t s);
 

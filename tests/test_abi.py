@@ -143,3 +143,20 @@ def test_varlen_paged_host_checks(lib):
     assert binding.fa_fwd_paged(*pg[:7], None, *pg[8:]) == 1           # no block table
     assert binding.fa_fwd_paged(*pg[:9], 0, *pg[10:]) == 1             # max pages 0
     assert binding.fa_fwd_paged(*pg[:15], 3, *pg[16:]) == 1            # H % H_kv != 0
+
+
+def test_strided_host_checks(lib):
+    # fake pointers, never dereferenced: each case fails before any CUDA call
+    a = 4096
+    good = [(4 * 8 * 64, 64, 8 * 64)] * 4           # BSND-like, bf16: all 16-byte multiples
+    args = [a] * 5 + [2, 4, 4, 8, 8, 64]
+    assert binding.fa_fwd_strided(*args, None, 0.1, 0, "bf16") == 1          # no strides
+    assert binding.fa_fwd_strided(*args, good[:3] + [(0, 64, 512)], 0.1, 0, "bf16") == 1
+    assert binding.fa_fwd_strided(*args, good[:3] + [(2052, 64, 512)], 0.1, 0, "bf16") == 3
+    assert binding.fa_fwd_strided(*args, good[:3] + [(1 << 39, 64, 512)], 0.1, 0, "bf16") == 2
+    bargs = [a] * 9 + [2, 4, 4, 8, 8, 64]
+    assert binding.fa_bwd_strided(*bargs, good * 2, 0.1, 0, "bf16", None, 0) == 1  # no workspace
+    assert binding.fa_bwd_strided(*bargs, good * 2, 0.1, 0, "e4m3", a, 1 << 20) == 2  # no fp8 backward
+    bad = good * 2
+    bad[7] = (2052, 64, 512)                                                  # dv batch stride: 4104 bytes
+    assert binding.fa_bwd_strided(*bargs, bad, 0.1, 0, "bf16", a, 1 << 20) == 3

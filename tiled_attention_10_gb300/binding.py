@@ -18,8 +18,33 @@ FA_STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
              3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
 # Symbols the header declares; the library must export all of them.
-EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_splitkv_noalloc", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd_varlen", "fa_fwd_paged", "fa_fwd_paged_split", "fa_fwd_paged_split_workspace_size", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
+EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_splitkv_noalloc", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd_varlen", "fa_fwd_paged", "fa_fwd_paged_split", "fa_fwd_paged_split_workspace_size", "fa_fwd_strided", "fa_bwd_strided", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
            "fa_probe_wait_timeout", "fa_version")
+
+
+
+class Strides(ctypes.Structure):
+    """fa_strides_t: element strides of a [B, H, S, D] tensor (D contiguous)."""
+    _fields_ = [("batch", ctypes.c_int64), ("head", ctypes.c_int64), ("seq", ctypes.c_int64)]
+
+
+def strides_of(t, order="BNSD"):
+    """Strides of a torch tensor whose dims are [B, H, S, D] (order "BNSD") or
+    [B, S, H, D] (order "BSND"); D must be contiguous."""
+    st = t.stride()
+    if st[3] != 1:
+        raise ValueError("the head dimension must be contiguous")
+    if order == "BNSD":
+        return (st[0], st[1], st[2])
+    return (st[0], st[2], st[1])
+
+
+def _strides_array(triples):
+    arr = (Strides * len(triples))()
+    for i, (b, h, s_) in enumerate(triples):
+        arr[i] = Strides(int(b), int(h), int(s_))
+    return arr
+
 
 _lib = None
 
@@ -65,6 +90,10 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd_varlen.restype = ip
     lib.fa_fwd_paged.argtypes = [vp] * 8 + [i64] * 9 + [f32, ip, ip, vp, vp, vp, vp]
     lib.fa_fwd_paged.restype = ip
+    lib.fa_fwd_strided.argtypes = [vp] * 5 + [i64] * 6 + [vp, f32, ip, ip, vp, vp, vp, vp]
+    lib.fa_fwd_strided.restype = ip
+    lib.fa_bwd_strided.argtypes = [vp] * 9 + [i64] * 6 + [vp, f32, ip, ip, vp, sz, vp]
+    lib.fa_bwd_strided.restype = ip
     lib.fa_fwd_paged_split.argtypes = [vp] * 8 + [i64] * 9 + [f32, ip, ip, vp, vp, vp, ip, vp, sz,
                                                                vp]
     lib.fa_fwd_paged_split.restype = ip
@@ -221,6 +250,30 @@ def fa_fwd_paged_split(q, k_cache, v_cache, o, lse, cu_q, seqused_k, block_table
                                       int(H_kv), int(D), float(scale), c, dt, descale_q,
                                       descale_k, descale_v, int(n_splits), workspace,
                                       int(workspace_bytes), stream))
+
+
+def fa_fwd_strided(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, strides, scale, causal, dtype,
+                   descale_q=None, descale_k=None, descale_v=None, stream=None) -> int:
+    """Forward with explicit strides: `strides` = four (batch, head, seq) element
+    triples for q, k, v, o (e.g. from strides_of)."""
+    lib = load()
+    dt = FA_DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
+    arr = None if strides is None else _strides_array(strides)
+    return int(lib.fa_fwd_strided(q, k, v, o, lse, int(B), int(H), int(H_kv), int(S_q), int(S_kv),
+                                  int(D), arr, float(scale), int(bool(causal)), dt, descale_q,
+                                  descale_k, descale_v, stream))
+
+
+def fa_bwd_strided(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S_q, S_kv, D, strides, scale,
+                   causal, dtype, workspace, workspace_bytes, stream=None) -> int:
+    """Backward with explicit strides: eight (batch, head, seq) triples for q, k,
+    v, o, dout, dq, dk, dv."""
+    lib = load()
+    dt = FA_DTYPE[dtype] if isinstance(dtype, str) else int(dtype)
+    arr = None if strides is None else _strides_array(strides)
+    return int(lib.fa_bwd_strided(q, k, v, o, dout, lse, dq, dk, dv, int(B), int(H), int(H_kv),
+                                  int(S_q), int(S_kv), int(D), arr, float(scale),
+                                  int(bool(causal)), dt, workspace, int(workspace_bytes), stream))
 
 
 def fa_last_device_error(stream=None) -> int:

@@ -168,6 +168,50 @@ bool make_map_paged(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, int64_t n
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// A [B, H, S, D] tensor with element strides (batch, head, seq) and contiguous
+// D, as a 4-D map {D, S, H, B} (the BNSD coordinate order whatever the memory
+// order), boxes of `box_rows` rows x 128 bytes, 128-byte swizzle.
+bool make_map_strided(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, int64_t B, int64_t H,
+                      int64_t S, int64_t D, const fa_strides_t& st, cuuint32_t box_rows = 128) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const uint64_t eb = (dtype == FA_DTYPE_FP8E4M3) ? 1 : 2;
+  const CUtensorMapDataType t = dtype == FA_DTYPE_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                : dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.seq) * eb, static_cast<cuuint64_t>(st.head) * eb,
+                           static_cast<cuuint64_t>(st.batch) * eb};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, t, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The element strides of a dense tensor in one of the two layouts.
+fa_strides_t dense_strides(fa_layout_t layout, int64_t H, int64_t S, int64_t D) {
+  if (layout == FA_LAYOUT_BNSD) return fa_strides_t{H * S * D, S * D, D};
+  return fa_strides_t{S * H * D, D, H * D};
+}
+
+// Strides a TMA map can use: positive, 16-byte multiples, below 2^40 bytes.
+fa_status_t check_strides(const fa_strides_t* st, int n, fa_dtype_t dtype) {
+  if (!st) return FA_ERR_INVALID_ARG;
+  const int64_t eb = (dtype == FA_DTYPE_FP8E4M3) ? 1 : 2;
+  for (int i = 0; i < n; ++i) {
+    const int64_t v[3] = {st[i].batch, st[i].head, st[i].seq};
+    for (int64_t x : v) {
+      if (x < 1) return FA_ERR_INVALID_ARG;
+      if ((x * eb) % 16 != 0) return FA_ERR_MISALIGNED;
+      if (x > (int64_t(1) << 39) / eb) return FA_ERR_UNSUPPORTED;
+    }
+  }
+  return FA_OK;
+}
+
 __global__ void fa_wait_probe_kernel(uint32_t* err, uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -265,7 +309,8 @@ fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, fl
                         int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv, int64_t D,
                         float scale, fa_layout_t layout, int causal, fa_dtype_t dtype,
                         const float* descale_q, const float* descale_k, const float* descale_v,
-                        int n_splits, void* workspace, cudaStream_t stream) {
+                        int n_splits, void* workspace, cudaStream_t stream,
+                        const fa_strides_t* strides = nullptr) {
   const int64_t eb = (dtype == FA_DTYPE_FP8E4M3) ? 1 : 2;
   const int64_t n_pairs = ((S_q + 127) / 128 + 1) / 2;
   DeviceInfo dev;
@@ -275,10 +320,19 @@ fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, fl
   // warp's rows) x 128 bytes, written by TMA stores.
   CUtensorMap mq, mk, mv, mo;
   const fa_dtype_t odt = (dtype == FA_DTYPE_F16) ? FA_DTYPE_F16 : FA_DTYPE_BF16;
-  if (!make_map(&mq, q, dtype, layout, B, H, S_q, D) || !make_map(&mk, k, dtype, layout, B, H_kv, S_kv, D) ||
-      !make_map(&mv, v, dtype, layout, B, H_kv, S_kv, D) ||
-      !make_map(&mo, o, odt, layout, B, H, S_q, D, 32))
+  if (strides) {  // q, k, v, o with their own strides: BNSD coordinate order
+    if (!make_map_strided(&mq, q, dtype, B, H, S_q, D, strides[0]) ||
+        !make_map_strided(&mk, k, dtype, B, H_kv, S_kv, D, strides[1]) ||
+        !make_map_strided(&mv, v, dtype, B, H_kv, S_kv, D, strides[2]) ||
+        !make_map_strided(&mo, o, odt, B, H, S_q, D, strides[3], 32))
+      return FA_ERR_CUDA;
+    layout = FA_LAYOUT_BNSD;
+  } else if (!make_map(&mq, q, dtype, layout, B, H, S_q, D) ||
+             !make_map(&mk, k, dtype, layout, B, H_kv, S_kv, D) ||
+             !make_map(&mv, v, dtype, layout, B, H_kv, S_kv, D) ||
+             !make_map(&mo, o, odt, layout, B, H, S_q, D, 32)) {
     return FA_ERR_CUDA;
+  }
   // Split partials: fp32 [n_splits * B, H, S_q, D] (BNSD), boxes of 32 rows x
   // 32 fp32 columns.
   CUtensorMap mop = mo;
@@ -415,6 +469,20 @@ fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
                      descale_q, descale_k, descale_v, n_splits, workspace, stream);
 }
 
+fa_status_t fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv,
+                           int64_t D, const fa_strides_t* strides, float scale, int causal,
+                           fa_dtype_t dtype, const float* descale_q, const float* descale_k,
+                           const float* descale_v, cudaStream_t stream) {
+  fa_status_t st = check_args(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, FA_LAYOUT_BNSD,
+                              dtype, descale_q, descale_k, descale_v);
+  if (st != FA_OK) return st;
+  st = check_strides(strides, 4, dtype);
+  if (st != FA_OK) return st;
+  return run_forward(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, FA_LAYOUT_BNSD, causal,
+                     dtype, descale_q, descale_k, descale_v, 1, nullptr, stream, strides);
+}
+
 fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
                    int64_t H, int64_t S_q, int64_t S_kv, int64_t D, float scale,
                    fa_layout_t layout, int causal, fa_dtype_t dtype, const float* descale_q,
@@ -457,19 +525,16 @@ size_t bwd_workspace_bytes(int64_t B, int64_t H, int64_t S_q) {
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-fa_status_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t S_q, size_t* workspace_bytes) {
-  if (!workspace_bytes || B < 1 || H < 1 || S_q < 1) return FA_ERR_INVALID_ARG;
-  *workspace_bytes = bwd_workspace_bytes(B, H, S_q);
-  return FA_OK;
-}
-
-fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                   const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H,
-                   int64_t H_kv, int64_t S_q, int64_t S_kv, int64_t D, float scale,
-                   fa_layout_t layout, int causal, fa_dtype_t dtype, void* workspace,
-                   size_t workspace_bytes, cudaStream_t stream) {
+// The backward pass; strides (q, k, v, o, dout, dq, dk, dv) or NULL for the
+// dense layout.
+fa_status_t run_backward(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv, int64_t D,
+                         float scale, fa_layout_t layout, int causal, fa_dtype_t dtype,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                         const fa_strides_t* strides) {
   fa_status_t st = check_args(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout, dtype,
                               nullptr, nullptr, nullptr);
   if (st != FA_OK) return st;
@@ -485,13 +550,29 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
   DeviceInfo dev;
   if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
   CUtensorMap mq, mk, mv, mdo, mdk, mdv;
-  if (!make_map(&mq, q, dtype, layout, B, H, S_q, D) ||
-      !make_map(&mk, k, dtype, layout, B, H_kv, S_kv, D) ||
-      !make_map(&mv, v, dtype, layout, B, H_kv, S_kv, D) ||
-      !make_map(&mdo, dout, dtype, layout, B, H, S_q, D) ||
-      !make_map(&mdk, dk, dtype, layout, B, H_kv, S_kv, D, 32) ||
-      !make_map(&mdv, dv, dtype, layout, B, H_kv, S_kv, D, 32))
-    return FA_ERR_CUDA;
+  fa_strides_t ts[8];  // q, k, v, o, dout, dq, dk, dv
+  if (strides) {
+    for (int i = 0; i < 8; ++i) ts[i] = strides[i];
+    if (!make_map_strided(&mq, q, dtype, B, H, S_q, D, ts[0]) ||
+        !make_map_strided(&mk, k, dtype, B, H_kv, S_kv, D, ts[1]) ||
+        !make_map_strided(&mv, v, dtype, B, H_kv, S_kv, D, ts[2]) ||
+        !make_map_strided(&mdo, dout, dtype, B, H, S_q, D, ts[4]) ||
+        !make_map_strided(&mdk, dk, dtype, B, H_kv, S_kv, D, ts[6], 32) ||
+        !make_map_strided(&mdv, dv, dtype, B, H_kv, S_kv, D, ts[7], 32))
+      return FA_ERR_CUDA;
+    layout = FA_LAYOUT_BNSD;  // the maps take BNSD coordinates
+  } else {
+    const fa_strides_t sq = dense_strides(layout, H, S_q, D), sk = dense_strides(layout, H_kv, S_kv, D);
+    const fa_strides_t dense[8] = {sq, sk, sk, sq, sq, sq, sk, sk};
+    for (int i = 0; i < 8; ++i) ts[i] = dense[i];
+    if (!make_map(&mq, q, dtype, layout, B, H, S_q, D) ||
+        !make_map(&mk, k, dtype, layout, B, H_kv, S_kv, D) ||
+        !make_map(&mv, v, dtype, layout, B, H_kv, S_kv, D) ||
+        !make_map(&mdo, dout, dtype, layout, B, H, S_q, D) ||
+        !make_map(&mdk, dk, dtype, layout, B, H_kv, S_kv, D, 32) ||
+        !make_map(&mdv, dv, dtype, layout, B, H_kv, S_kv, D, 32))
+      return FA_ERR_CUDA;
+  }
 
   const int64_t S_q_pad = n_q * 128;
   const size_t half_ws = bwd_workspace_bytes(B, H, S_q) / 2;
@@ -512,6 +593,13 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
   p.dsum = dsum;
   p.err = dev.err_word;
   p.wait_limit_ns = g_wait_limit_ns.load();
+  const fa_strides_t* sp3[3] = {&ts[3], &ts[4], &ts[5]};
+  int64_t* dst3[3] = {p.o_st, p.do_st, p.dq_st};
+  for (int i = 0; i < 3; ++i) {
+    dst3[i][0] = sp3[i]->batch;
+    dst3[i][1] = sp3[i]->head;
+    dst3[i][2] = sp3[i]->seq;
+  }
 
   // dQ: one unit per (query head, query tile); causal runs group heads so
   // that the K/V in flight fit in about 48 MB of L2 (as the forward).
@@ -557,6 +645,37 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
                                                                 dout, lse, lse2, dsum, pq, pk,
                                                                 grid_q, grid_k, grid_p, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_bwd_workspace_size(int64_t B, int64_t H, int64_t S_q, size_t* workspace_bytes) {
+  if (!workspace_bytes || B < 1 || H < 1 || S_q < 1) return FA_ERR_INVALID_ARG;
+  *workspace_bytes = bwd_workspace_bytes(B, H, S_q);
+  return FA_OK;
+}
+
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int64_t B, int64_t H,
+                   int64_t H_kv, int64_t S_q, int64_t S_kv, int64_t D, float scale,
+                   fa_layout_t layout, int causal, fa_dtype_t dtype, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream) {
+  return run_backward(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S_q, S_kv, D, scale, layout,
+                      causal, dtype, workspace, workspace_bytes, stream, nullptr);
+}
+
+fa_status_t fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           int64_t B, int64_t H, int64_t H_kv, int64_t S_q, int64_t S_kv,
+                           int64_t D, const fa_strides_t* strides, float scale, int causal,
+                           fa_dtype_t dtype, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  const fa_status_t st = check_strides(strides, 8, dtype);
+  if (st != FA_OK) return st;
+  return run_backward(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, S_q, S_kv, D, scale,
+                      FA_LAYOUT_BNSD, causal, dtype, workspace, workspace_bytes, stream, strides);
 }
 
 }  // extern "C"

@@ -67,6 +67,10 @@ struct BwdParams {
   const float* dsum;      // [B*H, S_q_pad]: rowsum(dO * O); 0 for rows >= S_q
   uint32_t* err;
   uint64_t wait_limit_ns;
+  // Element strides (batch, head, seq) of the tensors read or written
+  // without a tensor map: O and dO by the row-statistics pass, dQ by the dQ
+  // epilogue.  D is contiguous.
+  int64_t o_st[3], do_st[3], dq_st[3];
 };
 
 template <int D>
@@ -241,10 +245,10 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __rest
     float acc = 0.0f;
     if (active && s < p.S_q) {
       const int64_t b = bh / p.H, h = bh - b * p.H;
-      const int64_t off = (p.layout == 0 ? ((bh * p.S_q + s) * D) : (((b * p.S_q + s) * p.H + h) * D)) +
-                          sub * 8;
-      const uint4 ov = *reinterpret_cast<const uint4*>(o + off);
-      const uint4 dv = *reinterpret_cast<const uint4*>(dout + off);
+      const int64_t off_o = b * p.o_st[0] + h * p.o_st[1] + s * p.o_st[2] + sub * 8;
+      const int64_t off_do = b * p.do_st[0] + h * p.do_st[1] + s * p.do_st[2] + sub * 8;
+      const uint4 ov = *reinterpret_cast<const uint4*>(o + off_o);
+      const uint4 dv = *reinterpret_cast<const uint4*>(dout + off_do);
       const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
       const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
 #pragma unroll
@@ -593,8 +597,7 @@ __device__ void dq_softmax(const BwdParams& p, void* dq_out, uint32_t tmem, int 
       reg_dep_x32(a1);
       if (qi < p.S_q) {
         const int64_t b = bh / p.H, h = bh - b * p.H;
-        const int64_t off = (p.layout == 0 ? ((bh * p.S_q + qi) * D) : (((b * p.S_q + qi) * p.H + h) * D)) +
-                            64 * half;
+        const int64_t off = b * p.dq_st[0] + h * p.dq_st[1] + qi * p.dq_st[2] + 64 * half;
         uint8_t* dst = static_cast<uint8_t*>(dq_out) + off * 2;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
