@@ -143,3 +143,26 @@ def test_bwd_fused_qkv_into_fused_grads(causal, H_kv, cuda_lib):
     for got, ref in ((dq, dQ), (dk, dK), (dv, dV)):
         gg = got.float().permute(0, 2, 1, 3).cpu().double().numpy()
         assert np.linalg.norm(gg - ref) <= 2e-2 * np.linalg.norm(ref)
+
+
+@pytest.mark.parametrize("layout", ["BNSD", "BSND"])
+def test_autograd_function_matches_direct_calls(layout, cuda_lib):
+    # flash_attention (torch.autograd) = fa_fwd_strided + fa_bwd_strided: its
+    # output and gradients equal the direct calls' bits.
+    from tiled_attention_10_gb300 import flash_attention
+    B, H, H_kv, S, D = 2, 4, 2, 257, 64
+    g = torch.Generator(device="cuda").manual_seed(5)
+    shp = (lambda n: (B, n, S, D)) if layout == "BNSD" else (lambda n: (B, S, n, D))
+    q = torch.randn(*shp(H), generator=g, device="cuda").half().requires_grad_()
+    k = torch.randn(*shp(H_kv), generator=g, device="cuda").half().requires_grad_()
+    v = torch.randn(*shp(H_kv), generator=g, device="cuda").half().requires_grad_()
+    do = torch.randn(*shp(H), generator=g, device="cuda").half()
+    out = flash_attention(q, k, v, causal=True, layout=layout)
+    out.backward(do)
+    o_ref, lse_ref = binding.attention(q.detach(), k.detach(), v.detach(), causal=True,
+                                       layout=layout)
+    assert torch.equal(out.detach().view(torch.int16), o_ref.view(torch.int16))
+    dq, dk, dv = binding.attention_backward(q.detach(), k.detach(), v.detach(), o_ref, lse_ref,
+                                            do, causal=True, layout=layout)
+    for got, ref in ((q.grad, dq), (k.grad, dk), (v.grad, dv)):
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))

@@ -329,3 +329,93 @@ def attention(q, k, v, *, causal=False, scale=None, layout="BNSD", descale=None,
     if st != 0:
         raise FaError(st, "fa_fwd")
     return out, lse
+
+
+def attention_backward(q, k, v, out, lse, dout, *, causal=False, scale=None, layout="BNSD",
+                       dq=None, dk=None, dv=None, stream=None):
+    """dq, dk, dv = attention_backward(...): gradients through fa_bwd_strided
+    for torch CUDA tensors in `layout` ([B, H, S, D] or [B, S, H, D] dims,
+    any strides with D contiguous); `out`, `lse` from attention()."""
+    import torch
+    dmap = {torch.float16: "f16", torch.bfloat16: "bf16"}
+    if q.dtype not in dmap:
+        raise TypeError(f"no backward for {q.dtype}")
+    dtype = dmap[q.dtype]
+    if layout == "BNSD":
+        B, H, S_q, D = q.shape
+        H_kv, S_kv = k.shape[1], k.shape[2]
+    else:
+        B, S_q, H, D = q.shape
+        S_kv, H_kv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q, memory_format=torch.contiguous_format) if dq is None else dq
+    dk = torch.empty_like(k, memory_format=torch.contiguous_format) if dk is None else dk
+    dv = torch.empty_like(v, memory_format=torch.contiguous_format) if dv is None else dv
+    st, nbytes = fa_bwd_workspace_size(B, H, S_q)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    strides = [strides_of(t, layout) for t in (q, k, v, out, dout, dq, dk, dv)]
+    st = fa_bwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(),
+                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, H_kv,
+                        S_q, S_kv, D, strides, scale, causal, dtype, ws.data_ptr(), ws.numel(),
+                        stream)
+    if st != 0:
+        raise FaError(st, "fa_bwd_strided")
+    return dq, dk, dv
+
+
+def _autograd_function():
+    import torch
+
+    class FlashAttention(torch.autograd.Function):
+        """Autograd wrapper: forward through fa_fwd_strided, backward through
+        fa_bwd_strided (fp16 / bf16)."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, causal, scale, layout):
+            if layout == "BNSD":
+                B, H, S_q, D = q.shape
+                H_kv, S_kv = k.shape[1], k.shape[2]
+            else:
+                B, S_q, H, D = q.shape
+                S_kv, H_kv = k.shape[1], k.shape[2]
+            sc = 1.0 / math.sqrt(D) if scale is None else scale
+            out = torch.empty_like(q, memory_format=torch.contiguous_format)
+            lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device)
+            dt = {torch.float16: "f16", torch.bfloat16: "bf16"}[q.dtype]
+            stream = torch.cuda.current_stream(q.device).cuda_stream
+            st = fa_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), B, H, H_kv, S_q, S_kv, D,
+                                [strides_of(t, layout) for t in (q, k, v, out)], sc, causal, dt,
+                                None, None, None, stream)
+            if st != 0:
+                raise FaError(st, "fa_fwd_strided")
+            ctx.save_for_backward(q, k, v, out, lse)
+            ctx.causal, ctx.scale, ctx.layout = causal, sc, layout
+            return out
+
+        @staticmethod
+        def backward(ctx, dout):
+            q, k, v, out, lse = ctx.saved_tensors
+            if dout.stride(-1) != 1:
+                dout = dout.contiguous()
+            dq, dk, dv = attention_backward(q, k, v, out, lse, dout, causal=ctx.causal,
+                                            scale=ctx.scale, layout=ctx.layout)
+            return dq, dk, dv, None, None, None
+
+    return FlashAttention
+
+
+_FLASH_FN = None
+
+
+def flash_attention(q, k, v, causal=False, scale=None, layout="BNSD"):
+    """Differentiable attention (torch.autograd): O = softmax(scale q k^T) v
+    with this library's forward and backward kernels (fp16 / bf16; k and v may
+    have fewer heads than q; any strides with the head dim contiguous)."""
+    global _FLASH_FN
+    if _FLASH_FN is None:
+        _FLASH_FN = _autograd_function()
+    return _FLASH_FN.apply(q, k, v, causal, scale, layout)
