@@ -62,10 +62,22 @@ struct DeviceInfo {
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
 
+// The device whose primary context this thread has made current.  Tensor-map
+// encoding is a driver call that needs a current context; a thread on which
+// no CUDA runtime call has touched the device yet (a framework's worker
+// thread, say) has none, so it is made current once per thread and device
+// (cudaSetDevice on the device the thread already reports, which changes
+// nothing the caller chose).
+thread_local int t_ctx_dev = -1;
+
 // Per-device facts, looked up once with that device current.
 fa_status_t device_info(DeviceInfo* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  if (t_ctx_dev != dev) {
+    if (cudaSetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
+    t_ctx_dev = dev;
+  }
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   DeviceInfo& d = g_dev[dev];
   if (!d.ready) {
@@ -507,8 +519,13 @@ fa_status_t fa_last_device_error(cudaStream_t stream) {
 fa_status_t fa_probe_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
   DeviceInfo dev;
   if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
-  fa_wait_probe_kernel<<<1, 32, 0, stream>>>(dev.err_word, limit_ns ? limit_ns : 1000000ull);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = stream;
+  if (cudaLaunchKernelEx(&cfg, fa_wait_probe_kernel, dev.err_word,
+                         static_cast<uint64_t>(limit_ns ? limit_ns : 1000000ull)) != cudaSuccess)
+    return FA_ERR_CUDA;
   return fa_last_device_error(stream);
 }
 

@@ -1084,11 +1084,18 @@ cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
                           const float* lse, float* lse2, float* dsum, const BwdParams& p_dq,
                           const BwdParams& p_kv, int grid_dq, int grid_kv, int grid_prep,
                           cudaStream_t stream) {
-  fa_bwd_prep_kernel<D, DT><<<grid_prep, 256, 0, stream>>>(
-      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout_ptr), lse, p_dq, lse2,
-      dsum);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  // Every launch reports its own status (cudaLaunchKernelEx), so an error
+  // left pending by other code on this thread is never taken for ours.
+  cudaError_t e;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_prep);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    e = cudaLaunchKernelEx(&cfg, fa_bwd_prep_kernel<D, DT>, static_cast<const uint16_t*>(o),
+                           static_cast<const uint16_t*>(dout_ptr), lse, p_dq, lse2, dsum);
+    if (e != cudaSuccess) return e;
+  }
   {
     auto kern = fa_bwd_dq_kernel<D, DT>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kLaunchSmem);

@@ -64,11 +64,14 @@ cudaError_t launch_fa_combine(const CombineParams& c, int sm_count, cudaStream_t
   int64_t blocks = (rows + 7) / 8;
   const int64_t cap = static_cast<int64_t>(sm_count) * 16;
   if (blocks > cap) blocks = cap;
-  if (c.D == 64)
-    fa_combine_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(c);
-  else
-    fa_combine_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(c);
-  return cudaGetLastError();
+  // cudaLaunchKernelEx reports this launch's own status (not an error left
+  // pending by other code on the thread).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  if (c.D == 64) return cudaLaunchKernelEx(&cfg, fa_combine_kernel<64>, c);
+  return cudaLaunchKernelEx(&cfg, fa_combine_kernel<128>, c);
 }
 
 }  // namespace fa
