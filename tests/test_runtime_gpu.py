@@ -78,3 +78,24 @@ def test_torch_tensor_wrapper(cuda_lib):
     og = out.float().cpu().double().permute(0, 2, 1, 3).numpy()
     assert np.abs(og - O).max() <= 1.6e-2
     assert np.abs(lse.cpu().double().numpy() - L).max() <= 1e-3
+
+
+def test_calls_from_a_thread_that_never_touched_the_device(cuda_lib):
+    # The first CUDA call of a new thread is the library's own: it must make
+    # the device's context current itself (tensor-map encoding needs one).
+    import threading
+    from tiled_attention_10_gb300.inputs import Workload, make_inputs
+    w = Workload("t", 1, 2, 300, 300, 128, "bf16", "BNSD", True, seed=3)
+    x = make_inputs(w, device="cuda")
+    o1, o2 = torch.empty_like(x.q), torch.empty_like(x.q)
+    l1, l2 = (torch.empty(1, 2, 300, device="cuda") for _ in range(2))
+    args = lambda o, l: (x.q.data_ptr(), x.k.data_ptr(), x.v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                         1, 2, 300, 300, 128, w.softmax_scale, "BNSD", True, "bf16", None, None, None)
+    assert binding.fa_fwd(*args(o1, l1)) == 0
+    res = {}
+    t = threading.Thread(target=lambda: res.setdefault("st", binding.fa_fwd(*args(o2, l2))))
+    t.start()
+    t.join()
+    torch.cuda.synchronize()
+    assert res["st"] == 0
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
