@@ -624,7 +624,8 @@ def run_ours_packed(args, w, world, rank, local):
 
     ws, ws_bytes = None, 0
     if w.page_size and w.n_splits > 1:   # workspace allocated outside the timed region
-        st, ws_bytes = binding.fa_fwd_paged_split_workspace_size(w.H, tq, w.D, w.n_splits)
+        st, ws_bytes = binding.fa_fwd_paged_split_workspace_size(w.H, tq, w.D, w.n_splits,
+                                                                 len(w.seq_q))
         ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
 
     def step(qq=x.q, kk=x.k, vv=x.v):
@@ -739,7 +740,8 @@ def run_ours_packed(args, w, world, rank, local):
         "roofline": roof,
         "e2e": {"value": round(e2e_val, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (2 if (w.page_size and w.n_splits > 1) else 1),
+        # paged split: sequence-order pre-pass, forward, merge
+        "gpu_launches": args.steps * (3 if (w.page_size and w.n_splits > 1) else 1),
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

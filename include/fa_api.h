@@ -253,18 +253,27 @@ fa_status_t fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache
  *   of the paged-decode kernels in the Hygon retrospective (defect 7).  For
  *   decoding, where a few long sequences would otherwise leave most SMs
  *   idle.  Splits past a sequence's last key block are empty and get zero
- *   weight.  n_splits 1..32 (1: exactly fa_fwd_paged, workspace unused);
- *   workspace: caller-owned device memory of at least
- *   fa_fwd_paged_split_workspace_size bytes (fp32 [n_splits, H, total_q, D],
- *   then fp32 [n_splits, H, total_q], each 256-byte aligned), 256-byte
- *   aligned, contents on entry irrelevant.  Statuses as fa_fwd_paged plus
- *   FA_ERR_INVALID_ARG (n_splits < 1, workspace missing or small),
- *   FA_ERR_MISALIGNED (workspace off 256 bytes), FA_ERR_UNSUPPORTED
- *   (n_splits > 32).  Two launches on `stream`; calls sharing a workspace
- *   must not overlap.
+ *   weight.  With a workspace the sequences are also taken longest first
+ *   (a pre-pass ranks them by seqused_k; up to 16384 sequences, more keep
+ *   their given order), so that the static hand-out of work items stays
+ *   balanced when key lengths vary widely; the results do not depend on the
+ *   order.  n_splits 1..32 (1: fa_fwd_paged, plus the ordering when a
+ *   workspace is given); workspace: caller-owned device memory of at least
+ *   fa_fwd_paged_split_workspace_size bytes (int32 [n_seqs] sequence order
+ *   when n_seqs <= 16384, then for n_splits > 1 fp32 [n_splits, H, total_q,
+ *   D] and fp32 [n_splits, H, total_q]; each part 256-byte aligned),
+ *   256-byte aligned, contents on entry irrelevant; may be NULL only when
+ *   n_splits is 1.  Statuses as fa_fwd_paged plus FA_ERR_INVALID_ARG
+ *   (n_splits < 1, workspace missing or small), FA_ERR_MISALIGNED (workspace
+ *   off 256 bytes), FA_ERR_UNSUPPORTED (n_splits > 32).  Up to three launches
+ *   on `stream` (order, forward, merge); calls sharing a workspace must not
+ *   overlap.
+ *
+ * fa_fwd_paged_split_workspace_size -- that workspace size for n_seqs
+ *   sequences.  Host only; FA_ERR_INVALID_ARG on bad sizes or a NULL output.
  */
 fa_status_t fa_fwd_paged_split_workspace_size(int64_t H, int64_t total_q, int64_t D, int n_splits,
-                                              size_t* workspace_bytes);
+                                              int64_t n_seqs, size_t* workspace_bytes);
 
 fa_status_t fa_fwd_paged_split(const void* q, const void* k_cache, const void* v_cache, void* o,
                                float* lse, const int32_t* cu_seqlens_q, const int32_t* seqused_k,

@@ -145,6 +145,27 @@ def test_varlen_paged_host_checks(lib):
     assert binding.fa_fwd_paged(*pg[:15], 3, *pg[16:]) == 1            # H % H_kv != 0
 
 
+def test_paged_split_workspace_size(lib):
+    # the sequence order (int32 per sequence, up to 16384 sequences) then, for
+    # n_splits > 1, fp32 partial O and lse; each part rounded up to 256 bytes
+    r = lambda n: -(-n // 256) * 256
+    H, tq, D = 32, 128, 128
+    assert binding.fa_fwd_paged_split_workspace_size(H, tq, D, 1, 128) == (0, r(128 * 4))
+    assert binding.fa_fwd_paged_split_workspace_size(H, tq, D, 1, 1) == (0, 256)
+    part = r(2 * H * tq * D * 4) + r(2 * H * tq * 4)
+    assert binding.fa_fwd_paged_split_workspace_size(H, tq, D, 2, 128) == (0, r(512) + part)
+    assert binding.fa_fwd_paged_split_workspace_size(H, tq, D, 1, 16384) == (0, 65536)
+    assert binding.fa_fwd_paged_split_workspace_size(H, tq, D, 1, 16385) == (0, 0)   # given order
+    assert binding.fa_fwd_paged_split_workspace_size(H, tq, D, 1, 0)[0] == 1
+    assert binding.fa_fwd_paged_split_workspace_size(H, tq, D, 0, 4)[0] == 1
+    # a workspace smaller than that is rejected before any CUDA call
+    a = 4096
+    ps = [a] * 8 + [4, 8, 64, 100, 4, 1, 32, 8, 128, 0.1, 2, "bf16", None, None, None]
+    assert binding.fa_fwd_paged_split(*ps, 1, a, 255) == 1             # order needs 256
+    assert binding.fa_fwd_paged_split(*ps, 2, None, 0) == 1            # n_splits > 1 needs one
+    assert binding.fa_fwd_paged_split(*ps, 2, a + 16, 1 << 30) == 3    # workspace off 256 bytes
+
+
 def test_strided_host_checks(lib):
     # fake pointers, never dereferenced: each case fails before any CUDA call
     a = 4096

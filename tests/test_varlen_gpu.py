@@ -273,7 +273,8 @@ def test_paged_split_parity(case, n_splits, cuda_lib):
                               descale=c["descale"])
     out = Out(c["tq"], c["H"], c["D"], c["dtype"])
     keep, ds = _descale_ptrs(c["descale"], c["dtype"])
-    st, nb = binding.fa_fwd_paged_split_workspace_size(c["H"], c["tq"], c["D"], n_splits)
+    st, nb = binding.fa_fwd_paged_split_workspace_size(c["H"], c["tq"], c["D"], n_splits,
+                                                       len(c["seq_q"]))
     assert st == 0
     ws = torch.full((nb // 4 + 64,), float("nan"), device="cuda")   # contents must not matter
     cq = torch.from_numpy(c["cu_q"]).cuda()
@@ -292,3 +293,48 @@ def test_paged_split_parity(case, n_splits, cuda_lib):
     assert out.guards_intact()
     eo, el = _compare(O, L, out, c["cu_q"], c["dtype"])
     print(f"paged split case {case} n_splits={n_splits}: max|dO|={eo:.3g} max|dlse|={el:.3g}")
+
+
+def test_paged_sequence_order(cuda_lib):
+    # fa_fwd_paged_split with a workspace first ranks the sequences longest
+    # first (int32 [n_seqs] at the workspace's start) and hands out work in
+    # that order; the order moves work between CTAs but not its arithmetic, so
+    # the outputs equal fa_fwd_paged's bits.  Ties keep the given order.
+    c = _paged_setup(0)
+    seq_k = [1000, 17, 128, 257]
+    assert list(c["seq_k"]) == seq_k
+    scale = 1.0 / np.sqrt(c["D"])
+    cq = torch.from_numpy(c["cu_q"]).cuda()
+    sk = torch.tensor(seq_k, dtype=torch.int32, device="cuda")
+    tb = torch.from_numpy(c["table"]).cuda()
+    qd, kcd, vcd = c["q"].cuda(), c["kc"].cuda(), c["vc"].cuda()
+    keep, ds = _descale_ptrs(c["descale"], c["dtype"])
+    args = (len(c["seq_q"]), c["table"].shape[1], c["page_size"], c["kc"].shape[0], c["tq"],
+            max(c["seq_q"]), c["H"], c["H_kv"], c["D"], scale, c["causal"], c["dtype"], *ds)
+    ref = Out(c["tq"], c["H"], c["D"], c["dtype"])
+    assert binding.fa_fwd_paged(qd.data_ptr(), kcd.data_ptr(), vcd.data_ptr(), ref.o.data_ptr(),
+                                ref.lse.data_ptr(), cq.data_ptr(), sk.data_ptr(), tb.data_ptr(),
+                                *args) == 0
+    st, nb = binding.fa_fwd_paged_split_workspace_size(c["H"], c["tq"], c["D"], 1, len(seq_k))
+    assert st == 0 and nb == 256                       # the order alone, one aligned block
+    ws = torch.full((nb // 4,), -7, dtype=torch.int32, device="cuda")
+    out = Out(c["tq"], c["H"], c["D"], c["dtype"])
+    assert binding.fa_fwd_paged_split(qd.data_ptr(), kcd.data_ptr(), vcd.data_ptr(),
+                                      out.o.data_ptr(), out.lse.data_ptr(), cq.data_ptr(),
+                                      sk.data_ptr(), tb.data_ptr(), *args, 1, ws.data_ptr(),
+                                      nb) == 0
+    torch.cuda.synchronize()
+    assert binding.fa_last_device_error() == 0
+    assert ws[:4].tolist() == [0, 3, 2, 1]             # 1000, 257, 128, 17 keys
+    assert torch.equal(out.o.view(torch.int16), ref.o.view(torch.int16))
+    assert torch.equal(out.lse, ref.lse)
+    # equal lengths keep their index order; lengths past the cache are clamped
+    sk2 = torch.tensor([128, 9999999, 128, 17], dtype=torch.int32, device="cuda")
+    out2 = Out(c["tq"], c["H"], c["D"], c["dtype"])
+    assert binding.fa_fwd_paged_split(qd.data_ptr(), kcd.data_ptr(), vcd.data_ptr(),
+                                      out2.o.data_ptr(), out2.lse.data_ptr(), cq.data_ptr(),
+                                      sk2.data_ptr(), tb.data_ptr(), *args, 1, ws.data_ptr(),
+                                      nb) == 0
+    torch.cuda.synchronize()
+    assert binding.fa_last_device_error() == 0
+    assert ws[:4].tolist() == [1, 0, 2, 3]

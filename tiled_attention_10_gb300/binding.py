@@ -97,7 +97,7 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd_paged_split.argtypes = [vp] * 8 + [i64] * 9 + [f32, ip, ip, vp, vp, vp, ip, vp, sz,
                                                                vp]
     lib.fa_fwd_paged_split.restype = ip
-    lib.fa_fwd_paged_split_workspace_size.argtypes = [i64, i64, i64, ip, ctypes.POINTER(sz)]
+    lib.fa_fwd_paged_split_workspace_size.argtypes = [i64, i64, i64, ip, i64, ctypes.POINTER(sz)]
     lib.fa_fwd_paged_split_workspace_size.restype = ip
     lib.fa_status_string.argtypes = [ip]
     lib.fa_status_string.restype = ctypes.c_char_p
@@ -227,12 +227,12 @@ def fa_fwd_paged(q, k_cache, v_cache, o, lse, cu_q, seqused_k, block_table, n_se
                                 float(scale), c, dt, descale_q, descale_k, descale_v, stream))
 
 
-def fa_fwd_paged_split_workspace_size(H, total_q, D, n_splits):
+def fa_fwd_paged_split_workspace_size(H, total_q, D, n_splits, n_seqs):
     """(status, bytes) of workspace fa_fwd_paged_split needs."""
     lib = load()
     n = ctypes.c_size_t(0)
     st = int(lib.fa_fwd_paged_split_workspace_size(int(H), int(total_q), int(D), int(n_splits),
-                                                   ctypes.byref(n)))
+                                                   int(n_seqs), ctypes.byref(n)))
     return st, int(n.value)
 
 

@@ -24,6 +24,7 @@
 #include "fa_bwd.cuh"
 #include "fa_combine.cuh"
 #include "fa_kernel.cuh"
+#include "fa_seq_order.cuh"
 
 // Explicit instantiations live in fa_inst_*.cu (compiled in parallel).
 #define FA_FWD_EXTERN_ALL_MODES(D, DT)                    \
@@ -272,6 +273,16 @@ size_t split_workspace_bytes(int64_t B, int64_t H, int64_t S_q, int64_t D, int n
   const size_t rows = static_cast<size_t>(n_splits) * B * H * S_q;
   const size_t o_bytes = (rows * D * 4 + 255) / 256 * 256;
   return o_bytes + (rows * 4 + 255) / 256 * 256;
+}
+// fa_fwd_paged_split's workspace: the sequence order (int32 [n_seqs], when
+// n_seqs <= kMaxOrderedSeqs), then the split partials (n_splits > 1); each
+// part 256-byte aligned.
+size_t order_bytes(int64_t n_seqs) {
+  return n_seqs <= kMaxOrderedSeqs ? (static_cast<size_t>(n_seqs) * 4 + 255) / 256 * 256 : 0;
+}
+size_t paged_split_workspace_bytes(int64_t H, int64_t total_q, int64_t D, int n_splits,
+                                   int64_t n_seqs) {
+  return order_bytes(n_seqs) + (n_splits > 1 ? split_workspace_bytes(1, H, total_q, D, n_splits) : 0);
 }
 }  // namespace fa
 using fa::split_workspace_bytes;
@@ -752,13 +763,14 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
   if (n_seqs * (H >> shift) > INT32_MAX / n_pairs) return FA_ERR_UNSUPPORTED;
   if (n_splits < 1) return FA_ERR_INVALID_ARG;
   if (n_splits > kMaxSplits) return FA_ERR_UNSUPPORTED;
-  if (n_splits > 1) {
-    if (!workspace || workspace_bytes < split_workspace_bytes(1, H, total_q, D, n_splits))
+  if (n_splits > 1 && !workspace) return FA_ERR_INVALID_ARG;
+  if (workspace) {  // fa_fwd_paged_split: sequence order, then split partials
+    if (workspace_bytes < fa::paged_split_workspace_bytes(H, total_q, D, n_splits, n_seqs))
       return FA_ERR_INVALID_ARG;
     if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
-    if (static_cast<double>(n_splits) * n_seqs * (H >> shift) * n_pairs > 2e9)
-      return FA_ERR_UNSUPPORTED;
   }
+  if (n_splits > 1 && static_cast<double>(n_splits) * n_seqs * (H >> shift) * n_pairs > 2e9)
+    return FA_ERR_UNSUPPORTED;
   if (total_q == 0) return FA_OK;  // no query rows: nothing to compute or write
 
   DeviceInfo dev;
@@ -781,10 +793,12 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
   CUtensorMap mop = mo;
   float* o_part = nullptr;
   float* lse_part = nullptr;
+  int32_t* seq_order = nullptr;
+  if (workspace && n_seqs <= fa::kMaxOrderedSeqs) seq_order = static_cast<int32_t*>(workspace);
   if (n_splits > 1) {
-    o_part = static_cast<float*>(workspace);
+    o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + fa::order_bytes(n_seqs));
     const size_t rows = static_cast<size_t>(n_splits) * H * total_q;
-    lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + (rows * D * 4 + 255) / 256 * 256);
+    lse_part = reinterpret_cast<float*>(reinterpret_cast<char*>(o_part) + (rows * D * 4 + 255) / 256 * 256);
     ok = ok && make_map_f32(&mop, o_part, n_splits, H, total_q, D,
                             static_cast<cuuint32_t>(32 >> shift), static_cast<cuuint32_t>(1 << shift));
   }
@@ -819,6 +833,11 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
   p.n_seqs = static_cast<int32_t>(n_seqs);
   p.max_pages = static_cast<int32_t>(paged ? max_pages : 0);
   p.page_size = static_cast<int32_t>(paged ? page_size : 0);
+  p.seq_order = seq_order;
+  if (seq_order &&
+      fa::launch_seq_order(seqused_k, static_cast<int>(n_seqs), max_pages * page_size, seq_order,
+                           stream) != cudaSuccess)
+    return FA_ERR_CUDA;
 
   const int grid = static_cast<int>(p.num_units < dev.sm_count ? p.num_units : dev.sm_count);
   cudaError_t e;
@@ -883,9 +902,10 @@ fa_status_t fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache
 extern "C" {
 
 fa_status_t fa_fwd_paged_split_workspace_size(int64_t H, int64_t total_q, int64_t D, int n_splits,
-                                              size_t* workspace_bytes) {
-  if (!workspace_bytes || H < 1 || total_q < 0 || D < 1 || n_splits < 1) return FA_ERR_INVALID_ARG;
-  *workspace_bytes = n_splits > 1 ? split_workspace_bytes(1, H, total_q, D, n_splits) : 0;
+                                              int64_t n_seqs, size_t* workspace_bytes) {
+  if (!workspace_bytes || H < 1 || total_q < 0 || D < 1 || n_splits < 1 || n_seqs < 1)
+    return FA_ERR_INVALID_ARG;
+  *workspace_bytes = fa::paged_split_workspace_bytes(H, total_q, D, n_splits, n_seqs);
   return FA_OK;
 }
 

@@ -114,6 +114,7 @@ struct KernelParams {
                                // each of 128 >> q_pack_log2 tokens (row = token * 2^.. + head)
   int32_t causal_br;           // causal mask aligned bottom-right (key j visible to
                                // query i iff j <= i + S_kv - S_q)
+  const int32_t* seq_order;    // paged: sequence of each rank (longest first), or null
 };
 
 template <int D, int DT>
@@ -217,15 +218,17 @@ __device__ __forceinline__ Item decode_item(const KernelParams& p, int u) {
     // unit = (query-tile pair, sequence, head group), pairs outermost and
     // the last pairs first: only long sequences have high pairs, and when
     // causal a sequence's last pairs see the most keys, so the costliest
-    // units start early (longest-first order).  Pairs past a sequence's
-    // length are empty.  A head group is 2^q_pack_log2 query heads (those of
+    // units start early (longest-first order).  Within a pair the sequences
+    // follow seq_order when given (longest keys first).  Pairs past a
+    // sequence's length are empty.  A head group is 2^q_pack_log2 query heads (those of
     // one key/value head when packed, else one head); bh is its index.
     const int groups = static_cast<int>(p.H) >> p.q_pack_log2;
     const int per_rank = p.n_seqs * groups;
     const int rank = u / per_rank;
     const int rem = u - rank * per_rank;
-    it.seq = rem / groups;
-    it.bh = rem - it.seq * groups;
+    const int si = rem / groups;  // the sequence's place in the order
+    it.seq = p.seq_order ? min(max(p.seq_order[si], 0), p.n_seqs - 1) : si;
+    it.bh = rem - si * groups;
     it.pair = p.n_pairs - 1 - rank;
     it.split = 0;
     it.lo = 0;
