@@ -296,6 +296,74 @@ def run_reference(args, w, world, rank):
     return 0
 
 
+E2E_STREAMED = ("streamed: each step's inputs host->device on one copy stream and its results "
+                "device->host on another, through one of two device buffer sets, so the copies "
+                "of neighbouring steps overlap a step's compute; every step copies all of its "
+                "inputs in and all of its results out inside the timed region")
+E2E_SERIAL = ("serial: each step copies its inputs host->device, computes and copies its results "
+              "device->host on one stream (steps this small are bound by the host's per-call "
+              "overhead, which streaming only adds to)")
+E2E_STREAM_MIN_BYTES = 16 << 20   # stream the steps whose inputs are at least this large
+
+
+def e2e_ms_per_step(torch, stream, host_in, dev_in, run, dev_out, host_out, steps, world):
+    """End to end through the public call with pinned host buffers, fed the way a caller
+    streams batches: E2E_STREAMED when a step's inputs are at least E2E_STREAM_MIN_BYTES,
+    else E2E_SERIAL.  dev_in / dev_out: two lists of device tensors (one per buffer set);
+    run(b) computes from dev_in[b] into dev_out[b] on `stream`.  Returns (mean ms per step
+    over `steps` steps by CUDA events, max over ranks; the description of the scheme)."""
+    streamed = sum(t.numel() * t.element_size() for t in host_in) >= E2E_STREAM_MIN_BYTES
+    h2d, d2h = (torch.cuda.Stream(), torch.cuda.Stream()) if streamed else (stream, stream)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    out_home = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+
+    def one(i):
+        if not streamed:
+            for d_, h_ in zip(dev_in[0], host_in):
+                d_.copy_(h_, non_blocking=True)
+            run(0)
+            for h_, d_ in zip(host_out, dev_out[0]):
+                h_.copy_(d_, non_blocking=True)
+            return
+        b = i % 2
+        with torch.cuda.stream(h2d):
+            if used[b]:
+                h2d.wait_event(computed[b])        # step i-2 has read this set's inputs
+            for d_, h_ in zip(dev_in[b], host_in):
+                d_.copy_(h_, non_blocking=True)
+            in_ready[b].record(h2d)
+        stream.wait_event(in_ready[b])
+        if used[b]:
+            stream.wait_event(out_home[b])         # step i-2's results have left this set
+        run(b)
+        computed[b].record(stream)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(computed[b])
+            for h_, d_ in zip(host_out, dev_out[b]):
+                h_.copy_(d_, non_blocking=True)
+            out_home[b].record(d2h)
+        used[b] = True
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    if streamed:
+        h2d.wait_stream(stream)                    # no copy starts before e0
+    for i in range(steps):
+        one(i)
+    if streamed:
+        stream.wait_stream(d2h)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return (max_over_ranks(e0.elapsed_time(e1) / steps, world),
+            E2E_STREAMED if streamed else E2E_SERIAL)
+
+
 def run_ours(args, w, world, rank, local):
     import torch
     from tiled_attention_10_gb300 import binding
@@ -323,15 +391,15 @@ def run_ours(args, w, world, rank, local):
         ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     launches_per_step = 2 if n_splits > 1 else 1
 
-    def step(qq=q, kk=k, vv=v):
+    def step(qq=q, kk=k, vv=v, oo=o, ll=lse):
         if w.split:
-            st = binding.fa_fwd_splitkv(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
-                                        lse.data_ptr(), w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D,
+            st = binding.fa_fwd_splitkv(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(),
+                                        ll.data_ptr(), w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D,
                                         w.softmax_scale, w.layout, w.causal, w.dtype, ds[0],
                                         ds[1], ds[2], n_splits, ws.data_ptr(), ws_bytes, sp)
         else:
-            st = binding.fa_fwd_gqa(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
-                                    lse.data_ptr(), w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D,
+            st = binding.fa_fwd_gqa(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(),
+                                    ll.data_ptr(), w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D,
                                     w.softmax_scale, w.layout, w.causal, w.dtype, ds[0], ds[1],
                                     ds[2], sp)
         if st != 0:
@@ -362,31 +430,13 @@ def run_ours(args, w, world, rank, local):
         raise RuntimeError("device-side error during the timed steps")
 
     # End to end through the public call: pinned host inputs in, O and lse out.
-    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-
-    def e2e_step():
-        qd.copy_(hq, non_blocking=True)
-        kd.copy_(hk, non_blocking=True)
-        vd.copy_(hv, non_blocking=True)
-        step(qd, kd, vd)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-
-    e2e_steps = max(1, min(args.steps, 50))
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    host_in = [t.cpu().pin_memory() for t in (q, k, v)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
+    dev_in = [[torch.empty_like(t) for t in (q, k, v)] for _ in range(2)]
+    dev_out = [[o, lse], [torch.empty_like(o), torch.empty_like(lse)]]
+    e2e_ms, e2e_how = e2e_ms_per_step(torch, stream, host_in, dev_in,
+                             lambda b: step(*dev_in[b], *dev_out[b]), dev_out, host_out,
+                             max(1, min(args.steps, 50)), world)
     h2d = (q.numel() * q.element_size()) + (k.numel() * k.element_size()) + (v.numel() * v.element_size())
     d2h = o.numel() * o.element_size() + lse.numel() * 4
 
@@ -416,7 +466,7 @@ def run_ours(args, w, world, rank, local):
                      "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} bf16 GEMM"
                                     f"{' x2 (fp8 nominal ratio)' if w.dtype == 'e4m3' else ''}"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "how": e2e_how},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
     }
@@ -453,10 +503,10 @@ def run_ours_bwd(args, w, world, rank, local):
     st, ws_bytes = binding.fa_bwd_workspace_size(w.B, w.H, w.S_q)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
-    def step(qq=q, kk=k, vv=v, oo=o, dd=do, ll=lse):
+    def step(qq=q, kk=k, vv=v, oo=o, dd=do, ll=lse, gq=dq, gk=dk, gv=dv):
         st = binding.fa_bwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(),
-                            dd.data_ptr(), ll.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                            dv.data_ptr(), w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D,
+                            dd.data_ptr(), ll.data_ptr(), gq.data_ptr(), gk.data_ptr(),
+                            gv.data_ptr(), w.B, w.H, w.kv_heads, w.S_q, w.S_kv, w.D,
                             w.softmax_scale, w.layout, w.causal, w.dtype, ws.data_ptr(), ws_bytes,
                             sp)
         if st != 0:
@@ -486,29 +536,13 @@ def run_ours_bwd(args, w, world, rank, local):
 
     # End to end: pinned host Q, K, V, O, dO, lse in; dQ, dK, dV out.
     ins = (q, k, v, o, do, lse)
-    hins = [t.cpu().pin_memory() for t in ins]
-    dins = [torch.empty_like(t) for t in ins]
-    houts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
-
-    def e2e_step():
-        for d_, h_ in zip(dins, hins):
-            d_.copy_(h_, non_blocking=True)
-        step(*dins)
-        for h_, d_ in zip(houts, (dq, dk, dv)):
-            h_.copy_(d_, non_blocking=True)
-
-    e2e_steps = max(1, min(args.steps, 30))
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    host_in = [t.cpu().pin_memory() for t in ins]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+    dev_in = [[torch.empty_like(t) for t in ins] for _ in range(2)]
+    dev_out = [[dq, dk, dv], [torch.empty_like(t) for t in (dq, dk, dv)]]
+    e2e_ms, e2e_how = e2e_ms_per_step(torch, stream, host_in, dev_in,
+                             lambda b: step(*dev_in[b], *dev_out[b]), dev_out, host_out,
+                             max(1, min(args.steps, 30)), world)
     h2d = sum(t.numel() * t.element_size() for t in ins)
     d2h = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
     if rank != 0:
@@ -538,7 +572,7 @@ def run_ours_bwd(args, w, world, rank, local):
                      "executed_frac": round(executed / peak, 4),
                      "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} bf16 GEMM"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "how": e2e_how},
         "gpu_launches": args.steps * 3,
         "clocks": clocks,
     }
@@ -628,24 +662,24 @@ def run_ours_packed(args, w, world, rank, local):
                                                                  len(w.seq_q))
         ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
 
-    def step(qq=x.q, kk=x.k, vv=x.v):
+    def step(qq=x.q, kk=x.k, vv=x.v, oo=o, ll=lse):
         if w.page_size and w.n_splits > 1:
             st = binding.fa_fwd_paged_split(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(),
-                                            o.data_ptr(), lse.data_ptr(), x.cu_q.data_ptr(),
+                                            oo.data_ptr(), ll.data_ptr(), x.cu_q.data_ptr(),
                                             x.seqused_k.data_ptr(), x.block_table.data_ptr(),
                                             len(w.seq_q), x.block_table.shape[1], w.page_size,
                                             kk.shape[0], tq, max(w.seq_q), w.H, w.H_kv, w.D,
                                             w.softmax_scale, w.causal, w.dtype, *ds, w.n_splits,
                                             ws.data_ptr(), ws_bytes, sp)
         elif w.page_size:
-            st = binding.fa_fwd_paged(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
-                                      lse.data_ptr(), x.cu_q.data_ptr(), x.seqused_k.data_ptr(),
+            st = binding.fa_fwd_paged(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(),
+                                      ll.data_ptr(), x.cu_q.data_ptr(), x.seqused_k.data_ptr(),
                                       x.block_table.data_ptr(), len(w.seq_q), x.block_table.shape[1],
                                       w.page_size, kk.shape[0], tq, max(w.seq_q), w.H, w.H_kv, w.D,
                                       w.softmax_scale, w.causal, w.dtype, *ds, sp)
         else:
-            st = binding.fa_fwd_varlen(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
-                                       lse.data_ptr(), x.cu_q.data_ptr(), x.cu_k.data_ptr(),
+            st = binding.fa_fwd_varlen(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(),
+                                       ll.data_ptr(), x.cu_q.data_ptr(), x.cu_k.data_ptr(),
                                        len(w.seq_q), tq, sum(w.seq_k), max(w.seq_q), w.H, w.H_kv,
                                        w.D, w.softmax_scale, w.causal, w.dtype, *ds, sp)
         if st != 0:
@@ -674,31 +708,13 @@ def run_ours_packed(args, w, world, rank, local):
         raise RuntimeError("device-side error during the timed steps")
 
     # End to end: pinned host Q and K / V (or caches) in, O and lse out.
-    hq, hk, hv = (t.cpu().pin_memory() for t in (x.q, x.k, x.v))
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    qd, kd, vd = torch.empty_like(x.q), torch.empty_like(x.k), torch.empty_like(x.v)
-
-    def e2e_step():
-        qd.copy_(hq, non_blocking=True)
-        kd.copy_(hk, non_blocking=True)
-        vd.copy_(hv, non_blocking=True)
-        step(qd, kd, vd)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
-
-    e2e_steps = max(1, min(args.steps, 20))
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    host_in = [t.cpu().pin_memory() for t in (x.q, x.k, x.v)]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
+    dev_in = [[torch.empty_like(t) for t in (x.q, x.k, x.v)] for _ in range(2)]
+    dev_out = [[o, lse], [torch.empty_like(o), torch.empty_like(lse)]]
+    e2e_ms, e2e_how = e2e_ms_per_step(torch, stream, host_in, dev_in,
+                             lambda b: step(*dev_in[b], *dev_out[b]), dev_out, host_out,
+                             max(1, min(args.steps, 20)), world)
     h2d = sum(t.numel() * t.element_size() for t in (x.q, x.k, x.v))
     d2h = o.numel() * o.element_size() + lse.numel() * 4
     if rank != 0:
@@ -739,7 +755,7 @@ def run_ours_packed(args, w, world, rank, local):
                    "parallelism": f"{world} independent shard(s), one per GPU"},
         "roofline": roof,
         "e2e": {"value": round(e2e_val, 3), "unit": unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "how": e2e_how},
         # paged split: sequence-order pre-pass, forward, merge
         "gpu_launches": args.steps * (3 if (w.page_size and w.n_splits > 1) else 1),
         "clocks": clocks,
