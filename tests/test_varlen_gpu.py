@@ -338,3 +338,55 @@ def test_paged_sequence_order(cuda_lib):
     torch.cuda.synchronize()
     assert binding.fa_last_device_error() == 0
     assert ws[:4].tolist() == [1, 0, 2, 3]
+
+
+@pytest.mark.parametrize("n_seqs", [16384, 16385])
+def test_paged_split_many_sequences(n_seqs, cuda_lib):
+    # Decode over the largest batch that is still ordered (16384 sequences) and
+    # one past it (given order, no order in the workspace: the partials start at
+    # its beginning).  Sampled sequences against the oracle; the written order
+    # against a host sort.
+    H, H_kv, D, page_size, dtype = 8, 2, 64, 16, "bf16"
+    g = np.random.default_rng(n_seqs)
+    seq_q = [1] * n_seqs
+    seq_k = [int(x) for x in g.integers(1, 41, n_seqs)]
+    cu_q = np.arange(n_seqs + 1, dtype=np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(seq_k)]).astype(np.int32)
+    q, _ = _rand((n_seqs, H, D), dtype, g)
+    k, _ = _rand((int(cu_k[-1]), H_kv, D), dtype, g)
+    v, _ = _rand((int(cu_k[-1]), H_kv, D), dtype, g)
+    junk = lambda shape: torch.from_numpy(g.standard_normal(shape).astype(np.float32)).to(
+        TORCH_DTYPE[dtype])
+    kc, table = _paged_cache(k, seq_k, cu_k, page_size, H_kv, D, np.random.default_rng(1), junk)
+    vc, _ = _paged_cache(v, seq_k, cu_k, page_size, H_kv, D, np.random.default_rng(1), junk)
+    scale = 1.0 / np.sqrt(D)
+    n_splits = 2
+    st, nb = binding.fa_fwd_paged_split_workspace_size(H, n_seqs, D, n_splits, n_seqs)
+    assert st == 0
+    ws = torch.full((nb // 4 + 64,), float("nan"), device="cuda")
+    out = Out(n_seqs, H, D, dtype)
+    cq = torch.from_numpy(cu_q).cuda()
+    sk = torch.tensor(seq_k, dtype=torch.int32, device="cuda")
+    tb = torch.from_numpy(table).cuda()
+    qd, kcd, vcd = q.cuda(), kc.cuda(), vc.cuda()   # held until the call has run
+    st = binding.fa_fwd_paged_split(qd.data_ptr(), kcd.data_ptr(),
+                                    vcd.data_ptr(), out.o.data_ptr(), out.lse.data_ptr(),
+                                    cq.data_ptr(), sk.data_ptr(), tb.data_ptr(), n_seqs,
+                                    table.shape[1], page_size, kc.shape[0], n_seqs, 1, H, H_kv, D,
+                                    scale, 2, dtype, None, None, None, n_splits, ws.data_ptr(),
+                                    ws.numel() * 4)
+    torch.cuda.synchronize()
+    assert st == 0, binding.FA_STATUS.get(st)
+    assert binding.fa_last_device_error() == 0
+    assert out.guards_intact()
+    if n_seqs <= 16384:
+        want = np.lexsort((np.arange(n_seqs), -np.array(seq_k)))   # longest first, then index
+        assert np.array_equal(ws.view(torch.int32)[:n_seqs].cpu().numpy(), want)
+    pick = np.sort(np.concatenate([[0, n_seqs - 1], g.choice(n_seqs, 30, replace=False)]))
+    O, L = ov.attention_paged(q[torch.from_numpy(pick)], kc, vc, cu_q=np.arange(len(pick) + 1, dtype=np.int32),
+                              seqused_k=np.array(seq_k)[pick], block_table=table[pick],
+                              page_size=page_size, H=H, H_kv=H_kv, D=D, scale=scale,
+                              causal_mode=2, dtype=dtype, descale=(1.0, 1.0, 1.0))
+    og = out.o[torch.from_numpy(pick).cuda()].float().cpu().double().numpy()
+    lg = out.lse[:, torch.from_numpy(pick).cuda()].cpu().double().numpy()
+    assert np.abs(og - O).max() <= TOL_O[dtype] and np.abs(lg - L).max() <= TOL_LSE
