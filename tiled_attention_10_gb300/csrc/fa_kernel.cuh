@@ -145,6 +145,10 @@ struct Cfg {
   static constexpr uint32_t kIdescQK = umma_idesc(kFmt, false, kBM, kBN);
   static constexpr uint32_t kIdescPV = umma_idesc(kFmt, true, kBM, D);
   static constexpr float kRescaleThreshold = kFp8 ? 0.0f : 8.0f;
+  // log2 of P's scale: e4m3 P holds 256 * p (= 2^(x + 8)), so that weights
+  // down to 2^-17 of the row max stay representable; the row sum l then
+  // carries the same factor, which O / l cancels and the LSE subtracts.
+  static constexpr float kPLog2Scale = kFp8 ? 8.0f : 0.0f;
   static constexpr uint32_t kTmemS = 0, kTmemO = 256;
 };
 
@@ -617,7 +621,8 @@ __device__ __forceinline__ void softmax_block(float (&s)[128], int lim, int j, f
   // product of the first 64 keys runs while the second half is computed.
   // The loops are straight-line code (no branch inside) so the scheduler
   // can hide MUFU latency across columns.
-  const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_sub, -m_sub);
+  const float negm = C::kFp8 ? C::kPLog2Scale - m_sub : -m_sub;
+  const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(negm, negm);
   uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -638,7 +643,7 @@ __device__ __forceinline__ void softmax_block(float (&s)[128], int lim, int j, f
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int c = 64 * h + 4 * i;
-        pk[i] = pack_e4m3x4(s[c] * 256.f, s[c + 1] * 256.f, s[c + 2] * 256.f, s[c + 3] * 256.f);
+        pk[i] = pack_e4m3x4(s[c], s[c + 1], s[c + 2], s[c + 3]);
       }
       tmem_st_x16(tS + 16 * h, pk);
     } else {
@@ -698,7 +703,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     const float dk = p.descale_k ? *p.descale_k : 1.0f;
     const float dv = p.descale_v ? *p.descale_v : 1.0f;
     sl2 *= dq * dk;
-    o_mul = dv * (1.0f / 256.0f);  // P is stored as 256 * p in e4m3
+    o_mul = dv;  // (P's factor 256 is in l too: O / l cancels it)
   }
   // A masked score is -inf and must give p = 0: keep the base-2 scale
   // strictly positive (a zero scale or descale becomes 1e-30, which changes
@@ -862,9 +867,10 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
       float* lse_dst = kVarSplit ? p.lse_part + static_cast<int64_t>(item.split) * p.H * p.S_q : p.lse;
       if (row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0)
         lse_dst[static_cast<int64_t>(hrow) * p.S_q + item.q_row0 + row] =
-            l > 0.0f ? (m_run + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+            l > 0.0f ? (m_run + log2f(l) - C::kPLog2Scale) * 0.69314718055994531f : -CUDART_INF_F;
     } else if (row < p.S_q) {
-      lse_row_base<kSplit>(p, item.split, bh)[row] = (m_run + log2f(l)) * 0.69314718055994531f;
+      lse_row_base<kSplit>(p, item.split, bh)[row] =
+          (m_run + log2f(l) - C::kPLog2Scale) * 0.69314718055994531f;
     }
     tc_fence_before();
   }
