@@ -378,6 +378,10 @@ fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, fl
   p.lse_part = lse_part;
   // Causal: group heads so that the K/V of the heads in flight together fit
   // comfortably in L2 (about 48 MB); longest pairs first inside each group.
+  // When the K/V of all heads is about the size of L2 (<= 192 MB) grouping
+  // buys little locality, and with few groups the longest-first order that
+  // restarts in each group leaves CTAs unevenly loaded (1 x 32 heads x 8192
+  // bf16: 429 us grouped by 12 heads, 382 us as one group): one group then.
   int64_t group = 1;
   if (causal) {
     // K/V bytes one query head brings into L2 (a key/value head is shared
@@ -385,6 +389,7 @@ fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, fl
     const int64_t kv_bytes = 2 * S_kv * D * eb * H_kv / H;
     group = (48ll << 20) / (kv_bytes > 0 ? kv_bytes : 1);
     if (group < 1) group = 1;
+    if (B * H * kv_bytes <= (192ll << 20)) group = B * H;
     if (group > B * H) group = B * H;
   }
   p.group_heads = static_cast<int32_t>(group);
