@@ -403,6 +403,18 @@ fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, fl
   p.lse = lse;
   p.err = dev.err_word;
   p.wait_limit_ns = g_wait_limit_ns.load();
+  // Without a mask all units cost the same, and a last round of T < SMs / 2
+  // units leaves the other SMs idle for a whole unit: its units become 2T
+  // single-tile units whose key blocks are split over both tile slots, so
+  // that round takes about half as long (4 x 32 x 4096: 2048 units, T = 72).
+  p.solo_base = p.num_units;
+  if (!causal && n_splits == 1) {
+    const int64_t units = p.num_units, tail = units % dev.sm_count;
+    if (tail > 0 && 2 * tail <= dev.sm_count && units + tail < INT32_MAX - 2 * dev.sm_count) {
+      p.solo_base = static_cast<int32_t>(units - tail);
+      p.num_units = static_cast<int32_t>(units + tail);
+    }
+  }
 
   const int grid = static_cast<int>(p.num_units < dev.sm_count ? p.num_units : dev.sm_count);
   const bool sp = n_splits > 1;

@@ -115,6 +115,10 @@ struct KernelParams {
   int32_t causal_br;           // causal mask aligned bottom-right (key j visible to
                                // query i iff j <= i + S_kv - S_q)
   const int32_t* seq_order;    // paged: sequence of each rank (longest first), or null
+  // Dense mode: units u >= solo_base are single query tiles whose key blocks
+  // are split over both tile slots (see Item); the pair units they come from
+  // are solo_base + (u - solo_base) / 2.
+  int32_t solo_base;
 };
 
 template <int D, int DT>
@@ -138,7 +142,7 @@ struct Cfg {
   static constexpr int kEpiBoxBytes = 32 * 128;
   static constexpr int kEpiOffset = kQBytes + kSlots * kTileBytes;
   static constexpr int kBarOffset = kEpiOffset + 8 * kEpiBoxBytes;
-  static constexpr int kNumBars = 2 * kSlots + 11;
+  static constexpr int kNumBars = 2 * kSlots + 13;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;  // + align slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr uint32_t kFmt = kFp8 ? 0u : (DT == kDtBF16 ? 1u : 0u);
@@ -191,6 +195,13 @@ __device__ __forceinline__ int tile_kv_blocks(const KernelParams& p, int q_tile)
 struct Item {
   int bh, pair, split, lo;
   int n[2];
+  // A solo item (dense mode, the last round of a schedule that would leave
+  // SMs idle) is one query tile, qt, whose key blocks are split over both
+  // tile slots: slot t takes blocks [b[t], b[t] + n[t]); the epilogue merges
+  // the two halves.  Otherwise b[0] = b[1] = lo.
+  bool solo;
+  int qt;
+  int b[2];
   // Varlen / paged modes: the unit's sequence, its query / key lengths, the
   // packed row of its first query / key, and the causal offset (0 top-left,
   // S_kv - S_q bottom-right).
@@ -254,6 +265,8 @@ __device__ __forceinline__ Item decode_item(const KernelParams& p, int u) {
     it.off = p.causal_br ? it.k_len - it.q_len : 0;
     it.n[0] = var_tile_kv_blocks(p, it, 2 * it.pair);
     it.n[1] = var_tile_kv_blocks(p, it, 2 * it.pair + 1);
+    it.solo = false;
+    it.qt = 2 * it.pair;
     if constexpr (kVarSplit) {
       // This item: key blocks [lo, lo + chunk) of the unit; a split past the
       // sequence's blocks is empty (its partials get zero weight).
@@ -265,6 +278,7 @@ __device__ __forceinline__ Item decode_item(const KernelParams& p, int u) {
       it.n[0] = max(0, min(it.n[0], hi) - it.lo);
       it.n[1] = max(0, min(it.n[1], hi) - it.lo);
     }
+    it.b[0] = it.b[1] = it.lo;
     return it;
   }
   it.seq = 0;
@@ -273,16 +287,37 @@ __device__ __forceinline__ Item decode_item(const KernelParams& p, int u) {
   it.q_row0 = 0;
   it.k_row0 = 0;
   it.off = 0;
-  const int unit = kSplit ? u / p.n_splits : u;
+  int unit = kSplit ? u / p.n_splits : u;
   it.split = kSplit ? u - unit * p.n_splits : 0;
+  it.solo = false;
+  int solo_tile = 0;
+  if constexpr (kMode == kModeDense) {
+    if (u >= p.solo_base) {
+      unit = p.solo_base + ((u - p.solo_base) >> 1);
+      solo_tile = (u - p.solo_base) & 1;
+      it.solo = true;
+    }
+  }
   decode_unit(p, unit, it.bh, it.pair);
   const int f0 = tile_kv_blocks(p, 2 * it.pair), f1 = tile_kv_blocks(p, 2 * it.pair + 1);
+  if (it.solo) {
+    const int f = solo_tile ? f1 : f0;  // 0: a tile with no row
+    it.qt = 2 * it.pair + solo_tile;
+    it.lo = 0;
+    it.n[0] = (f + 1) >> 1;
+    it.n[1] = f - it.n[0];
+    it.b[0] = 0;
+    it.b[1] = it.n[0];
+    return it;
+  }
   const int nmax = max(f0, f1);
   const int chunk = kSplit ? (nmax + p.n_splits - 1) / p.n_splits : nmax;
   it.lo = it.split * chunk;
   const int hi = min(nmax, it.lo + chunk);
   it.n[0] = max(0, min(f0, hi) - it.lo);
   it.n[1] = max(0, min(f1, hi) - it.lo);
+  it.qt = 2 * it.pair;
+  it.b[0] = it.b[1] = it.lo;
   return it;
 }
 
@@ -307,6 +342,10 @@ struct Bars {
   __device__ uint32_t p_half(int t, int h) const { return base + 8u * (2 * ns + 4 + 2 * t + h); }
   __device__ uint32_t o_done(int t) const { return base + 8u * (2 * ns + 8 + t); }
   __device__ uint32_t drain() const { return base + 8u * (2 * ns + 10); }
+  // Solo items: slot 1's row state is in shared memory / slot 0 has read
+  // slot 1's O (one arrival per thread of the warpgroup).
+  __device__ uint32_t solo_ml() const { return base + 8u * (2 * ns + 11); }
+  __device__ uint32_t solo_read() const { return base + 8u * (2 * ns + 12); }
 };
 
 // Short bounded wait used only while tearing down after an abort: it ignores
@@ -368,6 +407,33 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
     const int nmax = max(n0, n1);
     if (nmax == 0) continue;            // an empty split: no MMA work
     if (!mbar_wait(bars.q_empty(), (it & 1u) ^ 1u, wc)) { ok = false; break; }
+    if constexpr (kMode == kModeDense) {
+      if (item.solo) {
+        // One Q tile (into slot 0's buffer), then K of each slot's first
+        // block, then per step: V of each slot's block, K of each slot's next.
+        mbar_arrive_expect_tx(bars.q_full(), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_tile(sQ + c * C::kChunkBytes, tmQ, bars.q_full(), p.layout, c * C::kBoxElems,
+                   item.qt * kBM, h, b);
+        ++it;
+        auto load = [&](int kv, int blk) -> bool {
+          const int slot = static_cast<int>(ring % C::kSlots);
+          if (!mbar_wait(bars.empty(slot), ((ring / C::kSlots) & 1u) ^ 1u, wc)) return false;
+          mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_tile(sRing + slot * C::kTileBytes + c * C::kChunkBytes, kv == 0 ? tmK : tmV,
+                     bars.full(slot), p.layout, c * C::kBoxElems, blk * kBN, hk, b);
+          ++ring;
+          return true;
+        };
+        ok = load(0, item.b[0]) && (n1 == 0 || load(0, item.b[1]));
+        for (int j = 0; j < n0 && ok; ++j) {
+          ok = load(1, item.b[0] + j) && (j >= n1 || load(1, item.b[1] + j));
+          if (ok && j + 1 < n0) ok = load(0, item.b[0] + j + 1) && (j + 1 >= n1 || load(0, item.b[1] + j + 1));
+        }
+        continue;
+      }
+    }
     mbar_arrive_expect_tx(bars.q_full(), (n0 > 0 ? C::kTileBytes : 0) + (n1 > 0 ? C::kTileBytes : 0));
     for (int t = 0; t < 2; ++t) {
       if ((t == 0 ? n0 : n1) == 0) continue;
@@ -454,6 +520,81 @@ struct RingPos {
   }
 };
 
+// The products of a solo item (see Item): both tile slots multiply the one
+// Q tile (slot 0's buffer), slot t over its own key blocks, in the ring
+// order the producer loads them.  Returns false if a wait gave up.
+template <int D, int DT>
+__device__ bool mma_solo_unit(const Item& item, RingPos& rp, uint32_t (&p_phase)[2], uint32_t q_lo,
+                              uint32_t k_lo0, uint32_t v_lo0, const uint32_t (&tS)[2],
+                              const uint32_t (&tO)[2], const Bars& bars, const WaitCtl& wc) {
+  using C = Cfg<D, DT>;
+  constexpr uint32_t kTileW = C::kTileBytes >> 4;
+  const int n[2] = {item.n[0], item.n[1]};  // n[0] >= n[1], n[0] >= 1
+  RingPos k[2], v[2];
+  k[0] = rp;
+  rp.advance<C::kSlots>();
+  k[1] = k[0];
+  if (n[1] > 0) {
+    k[1] = rp;
+    rp.advance<C::kSlots>();
+  }
+  if (!mbar_wait(bars.full(k[0].slot), k[0].phase, wc)) return false;
+  if (n[1] > 0 && !mbar_wait(bars.full(k[1].slot), k[1].phase, wc)) return false;
+  tc_fence_after();
+  issue_qk<D, DT>(tS[0], q_lo, k_lo0 + k[0].slot * kTileW);
+  umma_commit(bars.s_full(0));
+  if (n[1] > 0) {
+    issue_qk<D, DT>(tS[1], q_lo, k_lo0 + k[1].slot * kTileW);
+    umma_commit(bars.s_full(1));
+    umma_commit(bars.empty(k[1].slot));
+  }
+  umma_commit(bars.empty(k[0].slot));
+  if (n[0] == 1) umma_commit(bars.q_empty());
+  for (int j = 0; j < n[0]; ++j) {
+    v[0] = rp;
+    rp.advance<C::kSlots>();
+    if (j < n[1]) {
+      v[1] = rp;
+      rp.advance<C::kSlots>();
+    }
+    if (j + 1 < n[0]) {
+      k[0] = rp;
+      rp.advance<C::kSlots>();
+    }
+    if (j + 1 < n[1]) {
+      k[1] = rp;
+      rp.advance<C::kSlots>();
+    }
+    for (int t = 0; t < 2; ++t) {
+      if (j >= n[t]) continue;
+      const RingPos& vt = t ? v[1] : v[0];
+      const RingPos& kt = t ? k[1] : k[0];
+      if (!mbar_wait(bars.p_half(t, 0), p_phase[t], wc)) return false;
+      if (!mbar_wait(bars.full(vt.slot), vt.phase, wc)) return false;
+      tc_fence_after();
+      issue_pv_half<D, DT, 0>(tO[t], tS[t], v_lo0 + vt.slot * kTileW, j > 0 ? 1u : 0u);
+      if (!mbar_wait(bars.p_half(t, 1), p_phase[t], wc)) return false;
+      p_phase[t] ^= 1u;
+      tc_fence_after();
+      issue_pv_half<D, DT, 1>(tO[t], tS[t], v_lo0 + vt.slot * kTileW, 1u);
+      if (j + 1 < n[t]) {
+        if (!mbar_wait(bars.full(kt.slot), kt.phase, wc)) return false;
+        tc_fence_after();
+        issue_qk<D, DT>(tS[t], q_lo, k_lo0 + kt.slot * kTileW);
+        umma_commit(bars.s_full(t));
+      } else {
+        umma_commit(bars.o_done(t));
+      }
+    }
+    umma_commit(bars.empty(v[0].slot));
+    if (j < n[1]) umma_commit(bars.empty(v[1].slot));
+    if (j + 1 < n[0]) umma_commit(bars.empty(k[0].slot));
+    if (j + 1 < n[1]) umma_commit(bars.empty(k[1].slot));
+    if (j + 2 == n[0]) umma_commit(bars.q_empty());
+  }
+  return true;
+}
+
 template <int D, int DT, int kMode>
 __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint32_t sRing,
                          const Bars& bars, const WaitCtl& wc) {
@@ -478,6 +619,15 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
     if (nmax == 0) continue;
     if (!mbar_wait(bars.q_full(), it & 1u, wc)) { ok = false; break; }
     ++it;
+    if constexpr (kMode == kModeDense) {
+      if (item.solo) {
+        if (!mma_solo_unit<D, DT>(item, rp, p_phase, q_lo[0], k_lo0, v_lo0, tS, tO, bars, wc)) {
+          ok = false;
+          break;
+        }
+        continue;
+      }
+    }
     // Prologue: S_t = Q_t K_0^T for both tiles.
     int slotK = rp.slot;
     if (!mbar_wait(bars.full(slotK), rp.phase, wc)) { ok = false; break; }
@@ -554,6 +704,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
+}
+
+__device__ __forceinline__ void st_shared_f2(uint32_t addr, float a, float b) {
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ void ld_shared_f2(uint32_t addr, float& a, float& b) {
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(a), "=f"(b) : "r"(addr) : "memory");
 }
 
 // One K/V block of the softmax for one query row (the thread's TMEM lane):
@@ -710,15 +867,17 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
   // no unmasked exponent by more than ~1e-29 relative).
   sl2 = fmaxf(sl2, 1e-30f);
 
-  uint32_t s_phase = 0u, o_phase = 0u;
+  uint32_t s_phase = 0u, o_phase = 0u, solo_phase = 0u;
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0;; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
     const Item item = decode_item<kMode>(p, u);
     const int bh = item.bh;
-    const int q_tile = 2 * item.pair + t;
+    // A solo item's two slots work on the same tile, qt.
+    const int q_tile = item.solo ? item.qt : 2 * item.pair + t;
     const int n = t ? item.n[1] : item.n[0];
+    const int blk0 = t ? item.b[1] : item.b[0];  // this slot's first key block
     // Tile rows are tokens (dense, split: 128 of one head); varlen / paged
     // with GQA packing: 2^shift heads of each of 128 >> shift tokens.
     const int shift = kVar ? p.q_pack_log2 : 0;
@@ -763,7 +922,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
 #pragma unroll
       for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
 
-      const int64_t col0 = static_cast<int64_t>(item.lo + j) * kBN;
+      const int64_t col0 = static_cast<int64_t>(blk0 + j) * kBN;
       // Block-uniform: does any column of this block need a mask?
       const bool masked = (col0 + kBN > k_len) || (p.causal && col0 + (kBN - 1) > tile_row0 + item.off);
       const int lim = static_cast<int>(max(min(col_end - col0, static_cast<int64_t>(kBN)), int64_t(0)));
@@ -781,8 +940,40 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     if (!mbar_wait(bars.o_done(t), o_phase, wc)) break;
     o_phase ^= 1u;
     tc_fence_after();
+    // Solo item with both slots busy: slot 1 hands its row state (m, l) to
+    // slot 0 through its own staging box and waits until slot 0 has read its
+    // O from TMEM; slot 0 merges the halves, O = (a0 O0 + a1 O1) / (a0 l0 +
+    // a1 l1) with a_i = 2^(m_i - max(m0, m1)), and writes the tile.
+    const bool merge = item.solo && item.n[1] > 0;
+    float a0 = 1.0f, a1 = 0.0f;
+    if (merge) {
+      const uint32_t ml = sEpi + static_cast<uint32_t>(4 + wq) * C::kEpiBoxBytes + lane * 8;
+      const uint32_t ph = solo_phase;
+      solo_phase ^= 1u;
+      if (t == 1) {
+        if (lane == 0) bulk_wait_group_read0();  // this box's last store has read it
+        __syncwarp();
+        st_shared_f2(ml, m_run, l);
+        tc_fence_before();
+        mbar_arrive(bars.solo_ml());
+        if (!mbar_wait(bars.solo_read(), ph, wc)) break;
+        tc_fence_after();
+        continue;
+      }
+      if (!mbar_wait(bars.solo_ml(), ph, wc)) break;
+      tc_fence_after();
+      float m1, l1;
+      ld_shared_f2(ml, m1, l1);
+      const float mm = fmaxf(m_run, m1);
+      a0 = (m_run == -CUDART_INF_F) ? 0.0f : ex2(m_run - mm);
+      a1 = (m1 == -CUDART_INF_F) ? 0.0f : ex2(m1 - mm);
+      l = a0 * l + a1 * l1;
+      m_run = mm;
+    }
     // (A varlen / paged row that saw no key has l = 0: O = 0.)
     const float inv = (kVar && l == 0.0f) ? 0.0f : o_mul / l;
+    const float c0 = a0 * inv, c1 = a1 * inv;  // O = c0 O0 (+ c1 O1 when merging)
+    const uint32_t tO1 = tO + 128;               // slot 1's O (read when merging)
     // This warp's 32 rows: tokens [box_row0, box_row0 + box_toks).
     const int box_toks = 32 >> shift;
     const int32_t box_row0 = static_cast<int32_t>(tile_row0) + wq * box_toks;
@@ -799,6 +990,22 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
         reg_dep_x32(o0);
 #pragma unroll
         for (int i = 0; i < 32; ++i) pk[i] = __float_as_uint(__uint_as_float(o0[i]) * inv);
+      } else if (merge) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t o0[32], o1[32];
+          tmem_ld_x32(tO + 64 * bx + 32 * hf, o0);
+          tmem_ld_x32(tO1 + 64 * bx + 32 * hf, o1);
+          tmem_wait_ld();
+          reg_dep_x32(o0);
+          reg_dep_x32(o1);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float x0 = fmaf(__uint_as_float(o1[2 * i]), c1, __uint_as_float(o0[2 * i]) * c0);
+            const float x1 = fmaf(__uint_as_float(o1[2 * i + 1]), c1, __uint_as_float(o0[2 * i + 1]) * c0);
+            pk[16 * hf + i] = (DT == kDtF16) ? pack_f16x2(x0, x1) : pack_bf16x2(x0, x1);
+          }
+        }
       } else {
         uint32_t o0[32], o1[32];
         tmem_ld_x32(tO + 64 * bx, o0);
@@ -863,6 +1070,11 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
         bulk_commit_group();
       }
     }
+    if (merge) {
+      // Every read of slot 1's O has completed (each load above was waited).
+      tc_fence_before();
+      mbar_arrive(bars.solo_read());
+    }
     if constexpr (kVar) {
       float* lse_dst = kVarSplit ? p.lse_part + static_cast<int64_t>(item.split) * p.H * p.S_q : p.lse;
       if (row < q_len && item.q_row0 + row < p.S_q && item.q_row0 + row >= 0)
@@ -914,6 +1126,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.o_done(t), 1);
     }
     mbar_init(bars.drain(), 1);
+    mbar_init(bars.solo_ml(), 128);
+    mbar_init(bars.solo_read(), 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
