@@ -13,6 +13,9 @@ template <int D>
 __global__ void __launch_bounds__(256) fa_combine_kernel(const CombineParams c) {
   constexpr int kPer = D / 32;  // head-dim elements per lane
   const int lane = threadIdx.x & 31;
+  // Launched as a programmatic dependent of the split forward pass: nothing
+  // is read before that pass has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t rows = c.B * c.H * c.S_q;
   const int64_t split_stride = rows;  // rows per split
   for (int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5); row < rows;
@@ -70,6 +73,14 @@ cudaError_t launch_fa_combine(const CombineParams& c, int sm_count, cudaStream_t
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
+  // Programmatic dependent launch: the merge grid is scheduled while the
+  // forward pass drains and waits on the device for it (griddepcontrol.wait)
+  // instead of on the launch path.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (c.D == 64) return cudaLaunchKernelEx(&cfg, fa_combine_kernel<64>, c);
   return cudaLaunchKernelEx(&cfg, fa_combine_kernel<128>, c);
 }

@@ -1159,6 +1159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncwarp();
+  // This CTA's work is issued: a dependent grid (the split merge) may start.
+  if (threadIdx.x == 0) griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
