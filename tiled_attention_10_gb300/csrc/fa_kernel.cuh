@@ -507,6 +507,36 @@ __device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, 
   }
 }
 
+// e4m3: whether tile slot t's keys are one block that takes the softmax's
+// masked path (the same test as the softmax's) -- the first tile under a
+// causal mask, keys shorter than a block: rows there may see only a few
+// keys, and P's residual is added for them.
+template <int kMode>
+__device__ __forceinline__ bool refine_tile(const KernelParams& p, const Item& it, int t) {
+  const int n = t ? it.n[1] : it.n[0];
+  if (n != 1) return false;
+  const int q_tile = it.solo ? it.qt : 2 * it.pair + t;
+  const int shift = kMode >= kModeVarlen ? p.q_pack_log2 : 0;
+  const int64_t tile_row0 = static_cast<int64_t>(q_tile) * (kBM >> shift);
+  const int64_t col0 = static_cast<int64_t>((t ? it.b[1] : it.b[0]) + n - 1) * kBN;
+  return (col0 + kBN > it.k_len) || (p.causal && col0 + (kBN - 1) > tile_row0 + it.off);
+}
+
+// e4m3: O_t += P_lo V, P_lo = the residual of P's rounding that the softmax
+// writes in the 32 columns after P for a tile refine_tile selects.
+template <int D, int DT>
+__device__ __forceinline__ void issue_pv_residual(uint32_t o_tmem, uint32_t p_tmem, uint32_t vlo) {
+  using C = Cfg<D, DT>;
+  if constexpr (C::kFp8) {
+    constexpr uint32_t hi = umma_desc_hi_sw128(1024);
+#pragma unroll
+    for (int kk = 0; kk < C::kPVSteps; ++kk) {
+      const uint32_t off = static_cast<uint32_t>((kk * C::kUK * 128) >> 4);
+      umma_ts_w<true>(o_tmem, p_tmem + 32 + kk * 8, vlo + off, hi, C::kIdescPV, 1u);
+    }
+  }
+}
+
 // Ring position: slot index and the parity of its current use.
 struct RingPos {
   int slot = 0;
@@ -526,7 +556,8 @@ struct RingPos {
 template <int D, int DT>
 __device__ bool mma_solo_unit(const Item& item, RingPos& rp, uint32_t (&p_phase)[2], uint32_t q_lo,
                               uint32_t k_lo0, uint32_t v_lo0, const uint32_t (&tS)[2],
-                              const uint32_t (&tO)[2], const Bars& bars, const WaitCtl& wc) {
+                              const uint32_t (&tO)[2], const bool (&rf)[2], const Bars& bars,
+                              const WaitCtl& wc) {
   using C = Cfg<D, DT>;
   constexpr uint32_t kTileW = C::kTileBytes >> 4;
   const int n[2] = {item.n[0], item.n[1]};  // n[0] >= n[1], n[0] >= 1
@@ -583,6 +614,7 @@ __device__ bool mma_solo_unit(const Item& item, RingPos& rp, uint32_t (&p_phase)
         issue_qk<D, DT>(tS[t], q_lo, k_lo0 + kt.slot * kTileW);
         umma_commit(bars.s_full(t));
       } else {
+        if (t ? rf[1] : rf[0]) issue_pv_residual<D, DT>(tO[t], tS[t], v_lo0 + vt.slot * kTileW);
         umma_commit(bars.o_done(t));
       }
     }
@@ -619,9 +651,13 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
     if (nmax == 0) continue;
     if (!mbar_wait(bars.q_full(), it & 1u, wc)) { ok = false; break; }
     ++it;
+    // e4m3: tiles whose last block adds P's rounding residual.
+    const bool rf0 = C::kFp8 && refine_tile<kMode>(p, item, 0);
+    const bool rf1 = C::kFp8 && refine_tile<kMode>(p, item, 1);
     if constexpr (kMode == kModeDense) {
       if (item.solo) {
-        if (!mma_solo_unit<D, DT>(item, rp, p_phase, q_lo[0], k_lo0, v_lo0, tS, tO, bars, wc)) {
+        const bool rf[2] = {rf0, rf1};
+        if (!mma_solo_unit<D, DT>(item, rp, p_phase, q_lo[0], k_lo0, v_lo0, tS, tO, rf, bars, wc)) {
           ok = false;
           break;
         }
@@ -675,6 +711,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
           issue_qk<D, DT>(tS[t], q_lo[t], k_lo0 + slotKn * kTileW);
           umma_commit(bars.s_full(t));
         } else {
+          if (t ? rf1 : rf0) issue_pv_residual<D, DT>(tO[t], tS[t], v_lo0 + slotV * kTileW);
           umma_commit(bars.o_done(t));
         }
       }
@@ -796,13 +833,36 @@ __device__ __forceinline__ void softmax_block(float (&s)[128], int lim, int j, f
       if (i & 1) acc1 = f2_add(acc1, f2_pack(x0, x1)); else acc0 = f2_add(acc0, f2_pack(x0, x1));
     }
     if constexpr (C::kFp8) {
-      uint32_t pk[16];
+      // Masked blocks also write the residual P - e4m3(P), in e4m3, to the
+      // next 32 columns; for a tile whose keys are that one block (see
+      // refine_tile) the PV product adds it: P then reaches O to 2^-8 instead
+      // of 2^-4 -- for rows that see only a few keys, whose weights are not
+      // averaged.  (Computing it in every masked block keeps the flag out of
+      // the loop: a runtime flag there cost registers.)
+      if constexpr (kMasked) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int c = 64 * h + 4 * i;
-        pk[i] = pack_e4m3x4(s[c], s[c + 1], s[c + 2], s[c + 3]);
+        for (int g = 0; g < 2; ++g) {  // in groups of 8 columns (fewer live registers)
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int c = 64 * h + 32 * g + 4 * i;
+            hi[i] = pack_e4m3x4(s[c], s[c + 1], s[c + 2], s[c + 3]);
+            float q0, q1, q2, q3;
+            e4m3x4_unpack(hi[i], q0, q1, q2, q3);
+            lo[i] = pack_e4m3x4(s[c] - q0, s[c + 1] - q1, s[c + 2] - q2, s[c + 3] - q3);
+          }
+          tmem_st_x8(tS + 16 * h + 8 * g, hi);
+          tmem_st_x8(tS + 32 + 16 * h + 8 * g, lo);
+        }
+      } else {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = 64 * h + 4 * i;
+          pk[i] = pack_e4m3x4(s[c], s[c + 1], s[c + 2], s[c + 3]);
+        }
+        tmem_st_x16(tS + 16 * h, pk);
       }
-      tmem_st_x16(tS + 16 * h, pk);
     } else {
       uint32_t pk[32];
 #pragma unroll

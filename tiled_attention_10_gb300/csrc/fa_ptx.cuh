@@ -363,6 +363,22 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// The four e4m3 values packed in v (byte 0 first) as floats: each is exact
+// in f16, then in f32.
+__device__ __forceinline__ void e4m3x4_unpack(uint32_t v, float& x0, float& x1, float& x2,
+                                              float& x3) {
+  uint32_t h01, h23;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(h01), "=r"(h23)
+      : "r"(v));
+  asm("{\n\t.reg .b16 x, y;\n\tmov.b32 {x, y}, %2;\n\tcvt.f32.f16 %0, x;\n\tcvt.f32.f16 %1, y;\n\t}"
+      : "=f"(x0), "=f"(x1)
+      : "r"(h01));
+  asm("{\n\t.reg .b16 x, y;\n\tmov.b32 {x, y}, %2;\n\tcvt.f32.f16 %0, x;\n\tcvt.f32.f16 %1, y;\n\t}"
+      : "=f"(x2), "=f"(x3)
+      : "r"(h23));
+}
 // Four floats -> four e4m3 bytes (x0 in the lowest byte), RN, saturating.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
   uint32_t r;
