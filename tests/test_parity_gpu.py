@@ -83,3 +83,16 @@ def test_parity_gqa(H, H_kv, causal, layout, dtype, cuda_lib):
     w = Workload("t", 2, H, 300, 257, D, dtype, layout, causal, seed=H * 7 + H_kv, H_kv=H_kv,
                  poison=(layout == "BSND"))
     run_small(w)
+
+
+@pytest.mark.parametrize("B,H,H_kv,S_q,S_kv,causal,seed", [
+    (1, 6, 6, 385, 562, True, 1024), (3, 4, 4, 751, 625, True, 1117),
+    (2, 2, 2, 898, 7, False, 1068), (3, 4, 1, 153, 187, True, 1003)])
+def test_fp8_rows_with_few_keys(B, H, H_kv, S_q, S_kv, causal, seed, cuda_lib):
+    """e4m3 P rounds each weight by up to 2^-4; rows that see only a few keys
+    (the first query tile under a causal mask, keys shorter than a block) get
+    P's rounding residual added too.  These shapes reached |dO| 0.052-0.062
+    without it; the bound here is well inside the 6e-2 tolerance."""
+    w = Workload("t", B, H, S_q, S_kv, 128, "e4m3", "BNSD", causal, seed=seed, H_kv=H_kv)
+    eo, el = run_small(w)
+    assert eo <= 0.035, eo
