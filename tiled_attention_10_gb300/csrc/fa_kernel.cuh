@@ -363,24 +363,40 @@ __device__ __forceinline__ void mbar_wait_teardown(uint32_t bar, uint32_t parity
 // Paged K/V: the 128 keys of block j of sequence `seq` come from one page
 // (page_size >= 128) or from 128 / page_size pages, one TMA box each.  Page
 // indices past the sequence's last page are clamped to it (their keys are
-// masked); the block table is read only within the sequence's pages.
+// masked); the block table is read only within the sequence's pages.  The
+// producer looks a block's pages up once for its K and V tiles, one block
+// ahead of their loads, in 32-bit arithmetic (keys < 2^31): the lookups of a
+// single thread would otherwise hold up the ring.
+struct PagedBlock {
+  int32_t page[8];   // the pages of the block's sub-blocks (128 / rows of them)
+  int32_t in_page;   // first key of the block inside its page (page_size >= 128)
+};
+
+__device__ __forceinline__ void paged_lookup(const KernelParams& p, const int32_t* table,
+                                             uint32_t last_page, int j, PagedBlock& pb) {
+  const uint32_t ps = static_cast<uint32_t>(p.page_size);
+  const uint32_t key0 = static_cast<uint32_t>(j) * kBN;
+  const uint32_t pidx0 = key0 / ps;
+  pb.in_page = ps >= kBN ? static_cast<int32_t>(key0 - pidx0 * ps) : 0;
+  const int nsub = ps >= kBN ? 1 : static_cast<int>(kBN / ps);  // 1, 2, 4 or 8
+#pragma unroll
+  for (int sub = 0; sub < 8; ++sub)
+    if (sub < nsub) pb.page[sub] = table[min(pidx0 + sub, last_page)];
+}
+
 template <int D, int DT>
 __device__ __forceinline__ void paged_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                           const KernelParams& p, const Item& item, int j,
+                                           const KernelParams& p, const PagedBlock& pb,
                                            int32_t hk) {
   using C = Cfg<D, DT>;
-  const int64_t key0 = static_cast<int64_t>(j) * kBN;
-  const int64_t n_pages = max((item.k_len + p.page_size - 1) / p.page_size, int64_t(1));
-  const int32_t* table = p.block_table + static_cast<int64_t>(item.seq) * p.max_pages;
   const int rows = p.page_size < kBN ? p.page_size : kBN;
-  for (int sub = 0; sub < kBN / rows; ++sub) {
-    const int64_t key = key0 + static_cast<int64_t>(sub) * rows;
-    const int64_t pidx = min(min(key / p.page_size, n_pages - 1), int64_t(p.max_pages - 1));
-    const int32_t page = table[pidx];
-    const int32_t in_page = static_cast<int32_t>(key % p.page_size);
+  const int nsub = kBN / rows;
+#pragma unroll
+  for (int sub = 0; sub < 8; ++sub) {
+    if (sub >= nsub) break;
     for (int c = 0; c < C::kChunks; ++c)
       tma_load_4d(dst + c * C::kChunkBytes + sub * rows * 128, map, bar, c * C::kBoxElems, hk,
-                  in_page, page);
+                  pb.in_page, pb.page[sub]);
   }
 }
 
@@ -443,15 +459,28 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
                  h, b);
     }
     ++it;
+    // Paged: the sequence's block-table row and last page; block j + 1's
+    // pages are looked up while block j's tiles are in flight.
+    constexpr bool kPagedMode = kMode == kModePaged || kMode == kModePagedSplit;
+    const int32_t* table = kPagedMode ? p.block_table + static_cast<int64_t>(item.seq) * p.max_pages
+                                      : nullptr;
+    uint32_t last_page = 0;
+    PagedBlock pb;
+    if constexpr (kPagedMode) {
+      const uint32_t n_pages = static_cast<uint32_t>(
+          max((item.k_len + p.page_size - 1) / p.page_size, int64_t(1)));
+      last_page = min(n_pages, static_cast<uint32_t>(p.max_pages)) - 1u;
+      paged_lookup(p, table, last_page, item.lo, pb);
+    }
     for (int j = 0; j < nmax && ok; ++j) {
       for (int kv = 0; kv < 2; ++kv) {
         const int slot = static_cast<int>(ring % C::kSlots);
         if (!mbar_wait(bars.empty(slot), ((ring / C::kSlots) & 1u) ^ 1u, wc)) { ok = false; break; }
         mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
         const CUtensorMap* map = kv == 0 ? tmK : tmV;
-        if constexpr (kMode == kModePaged || kMode == kModePagedSplit) {
-          paged_tile<D, DT>(sRing + slot * C::kTileBytes, map, bars.full(slot), p, item,
-                            item.lo + j, hk);
+        if constexpr (kPagedMode) {
+          paged_tile<D, DT>(sRing + slot * C::kTileBytes, map, bars.full(slot), p, pb, hk);
+          if (kv == 1 && j + 1 < nmax) paged_lookup(p, table, last_page, item.lo + j + 1, pb);
         } else {
           for (int c = 0; c < C::kChunks; ++c)
             tma_tile(sRing + slot * C::kTileBytes + c * C::kChunkBytes, map, bars.full(slot),
