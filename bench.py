@@ -656,20 +656,32 @@ def run_ours_packed(args, w, world, rank, local):
         dst = [torch.tensor([d], dtype=torch.float32, device=dev) for d in x.descale]
         ds = [t.data_ptr() for t in dst]
 
-    ws, ws_bytes = None, 0
-    if w.page_size and w.n_splits > 1:   # workspace allocated outside the timed region
-        st, ws_bytes = binding.fa_fwd_paged_split_workspace_size(w.H, tq, w.D, w.n_splits,
+    # paged split: n_splits given, or (0) planned from the host-known sizes;
+    # the workspace is allocated outside the timed region
+    ws, ws_bytes, n_splits = None, 0, w.n_splits
+    use_split = bool(w.page_size) and n_splits != 1
+    if use_split:
+        if n_splits == 0:
+            st, n_splits, _ = binding.fa_fwd_paged_split_plan(len(w.seq_q), tq, max(w.seq_q),
+                                                              sum(w.seq_k), max(w.seq_k), w.H,
+                                                              w.H_kv, w.D)
+            if st != 0:
+                raise RuntimeError(f"paged split plan: {binding.fa_status_string(st)}")
+        st, ws_bytes = binding.fa_fwd_paged_split_workspace_size(w.H, tq, w.D, n_splits,
                                                                  len(w.seq_q))
         ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    # launches per step: paged split = sequence-order pre-pass (up to 16384
+    # sequences), forward, and the merge when the keys are split
+    launches_per_step = (1 + (len(w.seq_q) <= 16384) + (n_splits > 1)) if use_split else 1
 
     def step(qq=x.q, kk=x.k, vv=x.v, oo=o, ll=lse):
-        if w.page_size and w.n_splits > 1:
+        if use_split:
             st = binding.fa_fwd_paged_split(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(),
                                             oo.data_ptr(), ll.data_ptr(), x.cu_q.data_ptr(),
                                             x.seqused_k.data_ptr(), x.block_table.data_ptr(),
                                             len(w.seq_q), x.block_table.shape[1], w.page_size,
                                             kk.shape[0], tq, max(w.seq_q), w.H, w.H_kv, w.D,
-                                            w.softmax_scale, w.causal, w.dtype, *ds, w.n_splits,
+                                            w.softmax_scale, w.causal, w.dtype, *ds, n_splits,
                                             ws.data_ptr(), ws_bytes, sp)
         elif w.page_size:
             st = binding.fa_fwd_paged(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(),
@@ -752,12 +764,12 @@ def run_ours_packed(args, w, world, rank, local):
                    "flops": "4*D*H per visible (query, key) pair",
                    "l2": ("no flush: K/V exceed the 129 MB L2" if w.kv_bytes > (129 << 20)
                           else "no flush: inputs fit in L2"),
+                   **({"n_splits": n_splits} if use_split else {}),
                    "parallelism": f"{world} independent shard(s), one per GPU"},
         "roofline": roof,
         "e2e": {"value": round(e2e_val, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "how": e2e_how},
-        # paged split: sequence-order pre-pass, forward, merge
-        "gpu_launches": args.steps * (3 if (w.page_size and w.n_splits > 1) else 1),
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:

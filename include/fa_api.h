@@ -271,9 +271,25 @@ fa_status_t fa_fwd_paged(const void* q, const void* k_cache, const void* v_cache
  *
  * fa_fwd_paged_split_workspace_size -- that workspace size for n_seqs
  *   sequences.  Host only; FA_ERR_INVALID_ARG on bad sizes or a NULL output.
+ *
+ * fa_fwd_paged_split_plan -- picks n_splits from sizes the host knows: the
+ *   smallest count (1..32, at most half the longest sequence's 128-key
+ *   blocks) at which the longest work item -- a split of the longest
+ *   sequence, max_seqlen_k keys, plus about three blocks of fixed cost -- is
+ *   at most half of one SM's share of all the work (total_k keys over the
+ *   sequences, per group of query heads packed into a tile); and the
+ *   workspace that count needs.  sm_count: the SMs to plan for, 0 for the
+ *   current device's.  Host only; FA_ERR_INVALID_ARG on bad sizes
+ *   (max_seqlen_k > total_k, H % H_kv != 0, ...) or NULL outputs, FA_ERR_CUDA
+ *   if sm_count is 0 and the device cannot be queried.
  */
 fa_status_t fa_fwd_paged_split_workspace_size(int64_t H, int64_t total_q, int64_t D, int n_splits,
                                               int64_t n_seqs, size_t* workspace_bytes);
+
+fa_status_t fa_fwd_paged_split_plan(int64_t n_seqs, int64_t total_q, int64_t max_seqlen_q,
+                                    int64_t total_k, int64_t max_seqlen_k, int64_t H,
+                                    int64_t H_kv, int64_t D, int sm_count, int* n_splits,
+                                    size_t* workspace_bytes);
 
 fa_status_t fa_fwd_paged_split(const void* q, const void* k_cache, const void* v_cache, void* o,
                                float* lse, const int32_t* cu_seqlens_q, const int32_t* seqused_k,

@@ -166,6 +166,36 @@ def test_paged_split_workspace_size(lib):
     assert binding.fa_fwd_paged_split(*ps, 2, a + 16, 1 << 30) == 3    # workspace off 256 bytes
 
 
+def test_paged_split_plan(lib):
+    # host arithmetic only (sm_count given): decode over 1K-32K keys, 8 key/value
+    # heads with 4 query heads each (one packed tile per sequence and head)
+    plan = lambda n, tk, mk, sm=152, tq=None, mq=1, H=32, H_kv=8: binding.fa_fwd_paged_split_plan(
+        n, n if tq is None else tq, mq, tk, mk, H, H_kv, 128, sm)
+    # 128 sequences, 1.03M keys: a two-way split of the longest (255 blocks)
+    # is within half an SM's share (428 blocks)
+    st, n, ws = plan(128, 1033533, 32623)
+    assert (st, n) == (0, 2)
+    assert ws == binding.fa_fwd_paged_split_workspace_size(32, 128, 128, 2, 128)[1]
+    # 32 sequences, 265K keys: share 110 blocks, longest 232 -> five ways
+    assert plan(32, 265332, 29592)[:2] == (0, 5)
+    # the same keys with 4x the SMs need more splits, never fewer
+    ns = [plan(32, 265332, 29592, sm=sm)[1] for sm in (38, 76, 152, 304, 608)]
+    assert ns == sorted(ns) and ns[-1] <= 32
+    # a lone short sequence: at least two key blocks per split (8 blocks -> 4)
+    assert plan(1, 1000, 1000)[:2] == (0, 4)
+    assert plan(1, 128, 128)[:2] == (0, 1)
+    # prefill that fills the GPU on its own: no split, and the workspace is
+    # then the sequence order alone
+    st, n, ws = plan(64, 64 * 8192, 8192, tq=64 * 4096, mq=4096)
+    assert (st, n, ws) == (0, 1, 256)
+    # the cap: 32 splits
+    assert plan(1, 1 << 20, 1 << 20, sm=100000)[:2] == (0, 32)
+    for bad in ((0, 10, 10), (4, 10, 11), (4, -1, 0)):
+        assert plan(*bad)[0] == 1
+    assert plan(4, 100, 10, H=32, H_kv=6)[0] == 1     # H % H_kv != 0
+    assert plan(4, 100, 10, sm=-1)[0] == 1
+
+
 def test_strided_host_checks(lib):
     # fake pointers, never dereferenced: each case fails before any CUDA call
     a = 4096

@@ -18,7 +18,7 @@ FA_STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED",
              3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
 
 # Symbols the header declares; the library must export all of them.
-EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_splitkv_noalloc", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd_varlen", "fa_fwd_paged", "fa_fwd_paged_split", "fa_fwd_paged_split_workspace_size", "fa_fwd_strided", "fa_bwd_strided", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
+EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_fwd_splitkv_plan", "fa_fwd_splitkv_noalloc", "fa_bwd", "fa_bwd_workspace_size", "fa_fwd_varlen", "fa_fwd_paged", "fa_fwd_paged_split", "fa_fwd_paged_split_workspace_size", "fa_fwd_paged_split_plan", "fa_fwd_strided", "fa_bwd_strided", "fa_status_string", "fa_last_device_error", "fa_set_wait_limit_ns",
            "fa_probe_wait_timeout", "fa_version")
 
 
@@ -99,6 +99,8 @@ def load(path: str = LIB_PATH):
     lib.fa_fwd_paged_split.restype = ip
     lib.fa_fwd_paged_split_workspace_size.argtypes = [i64, i64, i64, ip, i64, ctypes.POINTER(sz)]
     lib.fa_fwd_paged_split_workspace_size.restype = ip
+    lib.fa_fwd_paged_split_plan.argtypes = [i64] * 8 + [ip, ctypes.POINTER(ip), ctypes.POINTER(sz)]
+    lib.fa_fwd_paged_split_plan.restype = ip
     lib.fa_status_string.argtypes = [ip]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_last_device_error.argtypes = [vp]
@@ -234,6 +236,18 @@ def fa_fwd_paged_split_workspace_size(H, total_q, D, n_splits, n_seqs):
     st = int(lib.fa_fwd_paged_split_workspace_size(int(H), int(total_q), int(D), int(n_splits),
                                                    int(n_seqs), ctypes.byref(n)))
     return st, int(n.value)
+
+
+def fa_fwd_paged_split_plan(n_seqs, total_q, max_seqlen_q, total_k, max_seqlen_k, H, H_kv, D,
+                            sm_count=0):
+    """(status, n_splits, workspace bytes) for fa_fwd_paged_split; sm_count 0: this device."""
+    lib = load()
+    n = ctypes.c_int(0)
+    b = ctypes.c_size_t(0)
+    st = int(lib.fa_fwd_paged_split_plan(int(n_seqs), int(total_q), int(max_seqlen_q),
+                                         int(total_k), int(max_seqlen_k), int(H), int(H_kv),
+                                         int(D), int(sm_count), ctypes.byref(n), ctypes.byref(b)))
+    return st, int(n.value), int(b.value)
 
 
 def fa_fwd_paged_split(q, k_cache, v_cache, o, lse, cu_q, seqused_k, block_table, n_seqs,

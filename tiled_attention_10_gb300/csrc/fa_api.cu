@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -727,6 +728,18 @@ fa_status_t fa_bwd_strided(const void* q, const void* k, const void* v, const vo
 
 namespace {
 
+// GQA packing: the query heads that share a key/value head fill one tile
+// together (2^shift heads x 128 >> shift tokens), so a K/V block is read
+// once for all of them -- what makes decoding (one token per sequence) use
+// more than one row of the 128.
+int q_pack_shift(int64_t H, int64_t H_kv) {
+  const int64_t g = H / H_kv;
+  int shift = 0;
+  if (g > 1 && g <= 32 && (g & (g - 1)) == 0)
+    while ((int64_t(1) << shift) < g) ++shift;
+  return shift;
+}
+
 // Varlen and paged forward passes: packed queries [total_q, H, D], one unit
 // per (sequence, head, pair of 128-row query tiles up to max_seqlen_q).
 fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -767,14 +780,7 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
       n_seqs > INT32_MAX - 1 || max_pages > INT32_MAX || num_pages > INT32_MAX ||
       page_size > 65536 || max_pages * page_size > kMaxRows)
     return FA_ERR_UNSUPPORTED;
-  // GQA packing: the query heads that share a key/value head fill one tile
-  // together (2^shift heads x 128 >> shift tokens), so a K/V block is read
-  // once for all of them -- what makes decoding (one token per sequence)
-  // use more than one row of the 128.
-  const int64_t g = H / H_kv;
-  int shift = 0;
-  if (g > 1 && g <= 32 && (g & (g - 1)) == 0)
-    while ((int64_t(1) << shift) < g) ++shift;
+  const int shift = q_pack_shift(H, H_kv);
   const int64_t toks = 128 >> shift;
   const int64_t n_pairs = ((max_seqlen_q + toks - 1) / toks + 1) / 2;
   if (n_seqs * (H >> shift) > INT32_MAX / n_pairs) return FA_ERR_UNSUPPORTED;
@@ -923,6 +929,42 @@ fa_status_t fa_fwd_paged_split_workspace_size(int64_t H, int64_t total_q, int64_
   if (!workspace_bytes || H < 1 || total_q < 0 || D < 1 || n_splits < 1 || n_seqs < 1)
     return FA_ERR_INVALID_ARG;
   *workspace_bytes = fa::paged_split_workspace_bytes(H, total_q, D, n_splits, n_seqs);
+  return FA_OK;
+}
+
+fa_status_t fa_fwd_paged_split_plan(int64_t n_seqs, int64_t total_q, int64_t max_seqlen_q,
+                                    int64_t total_k, int64_t max_seqlen_k, int64_t H,
+                                    int64_t H_kv, int64_t D, int sm_count, int* n_splits,
+                                    size_t* workspace_bytes) {
+  if (!n_splits || !workspace_bytes) return FA_ERR_INVALID_ARG;
+  if (n_seqs < 1 || total_q < 0 || max_seqlen_q < 1 || total_k < 0 || max_seqlen_k < 0 ||
+      max_seqlen_k > total_k || H < 1 || H_kv < 1 || H % H_kv != 0 || D < 1 || sm_count < 0)
+    return FA_ERR_INVALID_ARG;
+  if (sm_count == 0) {
+    DeviceInfo dev;
+    if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
+    sm_count = dev.sm_count;
+  }
+  // Work in 128-key blocks per head group (the query heads packed into one
+  // tile), times the query-tile pairs a sequence has on average.  Sequences
+  // are taken longest first, so the static hand-out stays balanced while the
+  // longest work item (a split of the longest sequence, plus about three
+  // blocks of fixed cost) is at most half of one SM's share; measured on the
+  // paged decode workloads (32 and 128 sequences, 1K-32K keys), that rule
+  // picks the fastest count or one within 2 % of it.
+  const int shift = q_pack_shift(H, H_kv);
+  const int64_t toks = 128 >> shift;
+  const int64_t groups = H >> shift;
+  const int64_t pairs = std::max<int64_t>(1, (total_q + n_seqs * 2 * toks - 1) / (n_seqs * 2 * toks));
+  const double share = (static_cast<double>(total_k) / 128.0 + 0.5 * static_cast<double>(n_seqs)) *
+                       static_cast<double>(groups * pairs) / sm_count;
+  const int64_t longest = (max_seqlen_k + 127) / 128;
+  const int64_t cap = std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, longest / 2));
+  int64_t splits = 1;
+  while (splits < cap && static_cast<double>((longest + splits - 1) / splits + 3) > 0.5 * share)
+    ++splits;
+  *n_splits = static_cast<int>(splits);
+  *workspace_bytes = fa::paged_split_workspace_bytes(H, total_q, D, static_cast<int>(splits), n_seqs);
   return FA_OK;
 }
 

@@ -224,7 +224,8 @@ class PackedWorkload:
     page_size: int = 0      # 0: contiguous packed K/V
     seed: int = 0
     std: float = 1.0
-    n_splits: int = 1       # paged: keys of each unit split this many ways, then merged
+    n_splits: int = 1       # paged: keys of each unit split this many ways, then merged;
+                            # 0: as many as fa_fwd_paged_split_plan picks
 
     @property
     def softmax_scale(self) -> float:
@@ -263,7 +264,7 @@ class PackedWorkload:
                 "H_kv": self.H_kv, "D": self.D, "dtype": self.dtype,
                 "causal": ["none", "top-left", "bottom-right"][self.causal],
                 "page_size": self.page_size or "contiguous",
-                **({"n_splits": self.n_splits} if self.n_splits > 1 else {}),
+                **({"n_splits": self.n_splits or "planned"} if self.n_splits != 1 else {}),
                 "values": f"iid N(0,{self.std}^2), seed {self.seed}"}
 
 
@@ -285,17 +286,18 @@ PACKED_WORKLOADS = {
         "bf16_paged_prefill_8x1024of8192_p64_h32kv8", (1024,) * 8, (8192,) * 8, 32, 8, 128,
         "bf16", 2, page_size=64),
     # decode: one new token per sequence, cached lengths log-uniform in [1K, 32K];
-    # keys split two ways per sequence and merged (fa_fwd_paged_split)
+    # keys split per sequence and merged (fa_fwd_paged_split), as many ways as
+    # fa_fwd_paged_split_plan picks (2 here)
     "bf16_paged_decode_128seq_1k-32k_p64_h32kv8": PackedWorkload(
         "bf16_paged_decode_128seq_1k-32k_p64_h32kv8", (1,) * 128,
         _log_uniform_lengths(128, 1024, 32768, 12), 32, 8, 128, "bf16", 2, page_size=64,
-        n_splits=2),
+        n_splits=0),
     # the same decode at a quarter of the cache (about 1 GB of K/V): the size
-    # the detailed profiler captures are taken on
+    # the detailed profiler captures are taken on (5 splits planned)
     "bf16_paged_decode_32seq_1k-32k_p64_h32kv8": PackedWorkload(
         "bf16_paged_decode_32seq_1k-32k_p64_h32kv8", (1,) * 32,
         _log_uniform_lengths(32, 1024, 32768, 12), 32, 8, 128, "bf16", 2, page_size=64,
-        n_splits=2),
+        n_splits=0),
 }
 
 
