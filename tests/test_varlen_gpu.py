@@ -390,3 +390,60 @@ def test_paged_split_many_sequences(n_seqs, cuda_lib):
     og = out.o[torch.from_numpy(pick).cuda()].float().cpu().double().numpy()
     lg = out.lse[:, torch.from_numpy(pick).cuda()].cpu().double().numpy()
     assert np.abs(og - O).max() <= TOL_O[dtype] and np.abs(lg - L).max() <= TOL_LSE
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_paged_split_planned(dtype, cuda_lib):
+    # Decode with the split count fa_fwd_paged_split_plan picks for this
+    # device: a few sequences of very different lengths leave most SMs idle,
+    # so it splits many ways (up to half the longest sequence's blocks).
+    H, H_kv, D, page_size = 8, 2, 128, 64
+    g = np.random.default_rng(5)
+    seq_k = [5000, 37, 1200, 129, 3100, 640]
+    n_seqs = len(seq_k)
+    cu_q = np.arange(n_seqs + 1, dtype=np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(seq_k)]).astype(np.int32)
+    q, dq = _rand((n_seqs, H, D), dtype, g)
+    k, dk = _rand((int(cu_k[-1]), H_kv, D), dtype, g)
+    v, dv = _rand((int(cu_k[-1]), H_kv, D), dtype, g)
+
+    def junk(shape):
+        x = torch.from_numpy((g.standard_normal(shape) * 100).astype(np.float32))
+        if dtype == "e4m3":
+            return (x / dk).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+        return x.to(TORCH_DTYPE[dtype])
+
+    kc, table = _paged_cache(k, seq_k, cu_k, page_size, H_kv, D, np.random.default_rng(2), junk)
+    vc, _ = _paged_cache(v, seq_k, cu_k, page_size, H_kv, D, np.random.default_rng(2), junk)
+    st, n_splits, nb = binding.fa_fwd_paged_split_plan(n_seqs, n_seqs, 1, sum(seq_k), max(seq_k),
+                                                       H, H_kv, D)
+    assert st == 0 and 2 <= n_splits <= 32
+    assert nb == binding.fa_fwd_paged_split_workspace_size(H, n_seqs, D, n_splits, n_seqs)[1]
+    ws = torch.full((nb // 4 + 64,), float("nan"), device="cuda")
+    out = Out(n_seqs, H, D, dtype)
+    scale = 1.0 / np.sqrt(D)
+    ds, dst = [None] * 3, []
+    if dtype == "e4m3":
+        dst = [torch.tensor([d], dtype=torch.float32, device="cuda") for d in (dq, dk, dv)]
+        ds = [t.data_ptr() for t in dst]
+    cq = torch.from_numpy(cu_q).cuda()
+    sk = torch.tensor(seq_k, dtype=torch.int32, device="cuda")
+    tb = torch.from_numpy(table).cuda()
+    qd, kcd, vcd = q.cuda(), kc.cuda(), vc.cuda()   # held until the call has run
+    st = binding.fa_fwd_paged_split(qd.data_ptr(), kcd.data_ptr(), vcd.data_ptr(),
+                                    out.o.data_ptr(), out.lse.data_ptr(), cq.data_ptr(),
+                                    sk.data_ptr(), tb.data_ptr(), n_seqs, table.shape[1],
+                                    page_size, kc.shape[0], n_seqs, 1, H, H_kv, D, scale, 2,
+                                    dtype, *ds, n_splits, ws.data_ptr(), ws.numel() * 4)
+    torch.cuda.synchronize()
+    assert st == 0, binding.FA_STATUS.get(st)
+    assert binding.fa_last_device_error() == 0
+    assert out.guards_intact()
+    O, L = ov.attention_paged(q, kc, vc, cu_q=cu_q, seqused_k=np.array(seq_k), block_table=table,
+                              page_size=page_size, H=H, H_kv=H_kv, D=D, scale=scale,
+                              causal_mode=2, dtype=dtype, descale=(dq, dk, dv))
+    eo = np.abs(out.o.float().cpu().double().numpy() - O).max()
+    el = np.abs(out.lse.cpu().double().numpy() - L).max()
+    print(f"planned paged split ({dtype}): n_splits={n_splits} max|dO|={eo:.3g} max|dlse|={el:.3g}")
+    assert eo <= TOL_O[dtype] and el <= TOL_LSE

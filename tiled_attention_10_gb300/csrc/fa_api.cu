@@ -16,10 +16,14 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <array>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <map>
 #include <mutex>
+#include <numeric>
+#include <vector>
 
 #include "../../include/fa_api.h"
 #include "fa_bwd.cuh"
@@ -327,6 +331,76 @@ fa_status_t check_args(const void* q, const void* k, const void* v, const void* 
 
 constexpr int kMaxSplits = 32;
 
+// Causal units (query-tile pairs) as the kernel hands them out: heads taken g
+// at a time, the longest pairs first inside each group, unit w * grid + b to
+// CTA b in even rounds and to CTA grid - 1 - b in odd ones.  Returns the
+// busiest CTA's load in key blocks, plus one per unit for its fixed cost.
+int64_t causal_makespan(int64_t BH, int64_t S_q, int64_t S_kv, int64_t g, int grid,
+                        std::vector<int64_t>& load) {
+  const int64_t n_tiles = (S_q + 127) / 128, n_pairs = (n_tiles + 1) / 2;
+  auto blocks = [&](int64_t t) -> int64_t {
+    if (t >= n_tiles) return 0;
+    return std::min(std::min(t * 128 + 127, S_q - 1), S_kv - 1) / 128 + 1;
+  };
+  load.assign(static_cast<size_t>(grid), 0);
+  const int64_t per_group = g * n_pairs, units = BH * n_pairs;
+  for (int64_t u = 0; u < units; ++u) {
+    const int64_t gi = u / per_group, r = u - gi * per_group;
+    const int64_t heads = std::min(g, BH - gi * g);
+    const int64_t pair = n_pairs - 1 - r / heads;
+    const int64_t w = u / grid, b = u - w * grid;
+    load[static_cast<size_t>((w & 1) ? grid - 1 - b : b)] +=
+        std::max(blocks(2 * pair), blocks(2 * pair + 1)) + 1;
+  }
+  return *std::max_element(load.begin(), load.end());
+}
+
+// Heads per scheduling group for a causal pass (see the kernel's static
+// schedule).  The K/V of the heads in flight together should fit in L2:
+// about 48 MB a group.  When the K/V of all heads is at most 192 MB (about
+// the size of L2) grouping buys little locality, and with few groups the
+// longest-first order that restarts in each group leaves CTAs unevenly
+// loaded (1 x 32 heads x 8192 bf16: 429 us grouped by 12 heads, 382 us as
+// one group): one group then.  Otherwise a group that is a whole number of
+// snake round pairs (g * pairs a multiple of 2 * grid) keeps every CTA's
+// share even, and is taken, up to 96 MB a group, when the modelled busiest
+// CTA is lighter than with the 48 MB group (bf16, D = 128: 4 x 32 x 4096
+// takes 19 heads, 455 -> 414 us; 2 x 32 x 8192 19 heads, 828 -> 761 us;
+// 8 x 32 x 4096 38 heads, 851-864 -> 809-812 us).  Choices are cached per
+// shape.
+int64_t causal_group(int64_t BH, int64_t S_q, int64_t S_kv, int64_t kv_bytes, int grid,
+                     bool balance) {
+  if (BH * kv_bytes <= (192ll << 20)) return BH;
+  const int64_t kv = kv_bytes > 0 ? kv_bytes : 1;
+  int64_t group = std::min(std::max<int64_t>((48ll << 20) / kv, 1), BH);
+  if (!balance || grid < 1) return group;
+  const int64_t g_max = std::min(std::max<int64_t>((96ll << 20) / kv, 1), BH);
+  const int64_t n_pairs = ((S_q + 127) / 128 + 1) / 2;
+  const int64_t g0 = 2 * grid / std::gcd<int64_t>(2 * grid, n_pairs);
+  if (g0 > g_max) return group;
+  static std::mutex mu;
+  static std::map<std::array<int64_t, 5>, int64_t> cache;
+  const std::array<int64_t, 5> key = {BH, S_q, S_kv, kv_bytes, grid};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  std::vector<int64_t> load;
+  int64_t best = causal_makespan(BH, S_q, S_kv, group, grid, load);
+  for (int64_t g = g0, tries = 0; g <= g_max && tries < 8; g += g0, ++tries) {
+    const int64_t m = causal_makespan(BH, S_q, S_kv, g, grid, load);
+    if (m < best) {
+      best = m;
+      group = g;
+    }
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() >= 1024) cache.clear();
+  cache[key] = group;
+  return group;
+}
+
 // The forward pass, whole (n_splits = 1: o / lse written directly) or split
 // over the keys (n_splits > 1: partials in `workspace`, then the merge).
 fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -377,21 +451,14 @@ fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, fl
   p.num_units = static_cast<int32_t>(B * H * n_pairs * n_splits);
   p.n_splits = n_splits;
   p.lse_part = lse_part;
-  // Causal: group heads so that the K/V of the heads in flight together fit
-  // comfortably in L2 (about 48 MB); longest pairs first inside each group.
-  // When the K/V of all heads is about the size of L2 (<= 192 MB) grouping
-  // buys little locality, and with few groups the longest-first order that
-  // restarts in each group leaves CTAs unevenly loaded (1 x 32 heads x 8192
-  // bf16: 429 us grouped by 12 heads, 382 us as one group): one group then.
+  // Causal: heads in scheduling groups, longest pairs first inside each.
+  // (K/V bytes one query head brings into L2: a key/value head is shared by
+  // H / H_kv consecutive query heads.)
   int64_t group = 1;
   if (causal) {
-    // K/V bytes one query head brings into L2 (a key/value head is shared
-    // by H / H_kv consecutive query heads).
-    const int64_t kv_bytes = 2 * S_kv * D * eb * H_kv / H;
-    group = (48ll << 20) / (kv_bytes > 0 ? kv_bytes : 1);
-    if (group < 1) group = 1;
-    if (B * H * kv_bytes <= (192ll << 20)) group = B * H;
-    if (group > B * H) group = B * H;
+    const int64_t sched_grid = std::min<int64_t>(B * H * n_pairs, dev.sm_count);
+    group = causal_group(B * H, S_q, S_kv, 2 * S_kv * D * eb * H_kv / H,
+                         static_cast<int>(sched_grid), n_splits == 1);
   }
   p.group_heads = static_cast<int32_t>(group);
   p.layout = static_cast<int32_t>(layout);

@@ -100,6 +100,10 @@ EXTRA_WORKLOADS = {
                                           "bf16", "BNSD", False, H_kv=8),
     "bf16_gqa_causal_1x64kv8x8192x128": Workload("bf16_gqa_causal_1x64kv8x8192x128", 1, 64, 8192,
                                                  8192, 128, "bf16", "BSND", True, H_kv=8),
+    # the forward of the training configuration (32 heads, head dim 128,
+    # causal, bf16) at 4 x 4096 tokens: the pass the backward workload follows
+    "bf16_causal_4x32x4096x128": Workload("bf16_causal_4x32x4096x128", 4, 32, 4096, 4096, 128,
+                                          "bf16", "BNSD", True),
     # few heads, short queries, long keys: split-KV fills the GPU
     "bf16_splitkv_1x8x512x16384x128": Workload("bf16_splitkv_1x8x512x16384x128", 1, 8, 512, 16384,
                                                128, "bf16", "BNSD", False, split=True),
