@@ -16,7 +16,6 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <array>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -331,65 +330,60 @@ fa_status_t check_args(const void* q, const void* k, const void* v, const void* 
 
 constexpr int kMaxSplits = 32;
 
-// Causal units (query-tile pairs) as the kernel hands them out: heads taken g
-// at a time, the longest pairs first inside each group, unit w * grid + b to
-// CTA b in even rounds and to CTA grid - 1 - b in odd ones.  Returns the
-// busiest CTA's load in key blocks, plus one per unit for its fixed cost.
-int64_t causal_makespan(int64_t BH, int64_t S_q, int64_t S_kv, int64_t g, int grid,
-                        std::vector<int64_t>& load) {
-  const int64_t n_tiles = (S_q + 127) / 128, n_pairs = (n_tiles + 1) / 2;
-  auto blocks = [&](int64_t t) -> int64_t {
-    if (t >= n_tiles) return 0;
-    return std::min(std::min(t * 128 + 127, S_q - 1), S_kv - 1) / 128 + 1;
-  };
+// The busiest CTA's load under the kernels' static schedule: units in groups
+// of g heads, rank-major inside a group (heads vary fastest; rank r costs
+// cost[r] key blocks -- or query tiles -- plus one for the unit's fixed
+// cost), unit w * grid + b to CTA b in even rounds and to CTA grid - 1 - b in
+// odd ones.
+int64_t snake_makespan(int64_t n_heads, const std::vector<int64_t>& cost, int64_t g, int grid,
+                       std::vector<int64_t>& load) {
+  const int64_t n_ranks = static_cast<int64_t>(cost.size());
   load.assign(static_cast<size_t>(grid), 0);
-  const int64_t per_group = g * n_pairs, units = BH * n_pairs;
+  const int64_t per_group = g * n_ranks, units = n_heads * n_ranks;
   for (int64_t u = 0; u < units; ++u) {
     const int64_t gi = u / per_group, r = u - gi * per_group;
-    const int64_t heads = std::min(g, BH - gi * g);
-    const int64_t pair = n_pairs - 1 - r / heads;
+    const int64_t heads = std::min(g, n_heads - gi * g);
     const int64_t w = u / grid, b = u - w * grid;
-    load[static_cast<size_t>((w & 1) ? grid - 1 - b : b)] +=
-        std::max(blocks(2 * pair), blocks(2 * pair + 1)) + 1;
+    load[static_cast<size_t>((w & 1) ? grid - 1 - b : b)] += cost[static_cast<size_t>(r / heads)] + 1;
   }
   return *std::max_element(load.begin(), load.end());
 }
 
-// Heads per scheduling group for a causal pass (see the kernel's static
-// schedule).  The K/V of the heads in flight together should fit in L2:
-// about 48 MB a group.  When the K/V of all heads is at most 192 MB (about
-// the size of L2) grouping buys little locality, and with few groups the
-// longest-first order that restarts in each group leaves CTAs unevenly
-// loaded (1 x 32 heads x 8192 bf16: 429 us grouped by 12 heads, 382 us as
-// one group): one group then.  Otherwise a group that is a whole number of
-// snake round pairs (g * pairs a multiple of 2 * grid) keeps every CTA's
-// share even, and is taken, up to 96 MB a group, when the modelled busiest
-// CTA is lighter than with the 48 MB group (bf16, D = 128: 4 x 32 x 4096
-// takes 19 heads, 455 -> 414 us; 2 x 32 x 8192 19 heads, 828 -> 761 us;
-// 8 x 32 x 4096 38 heads, 851-864 -> 809-812 us).  Choices are cached per
-// shape.
-int64_t causal_group(int64_t BH, int64_t S_q, int64_t S_kv, int64_t kv_bytes, int grid,
-                     bool balance) {
-  if (BH * kv_bytes <= (192ll << 20)) return BH;
-  const int64_t kv = kv_bytes > 0 ? kv_bytes : 1;
-  int64_t group = std::min(std::max<int64_t>((48ll << 20) / kv, 1), BH);
-  if (!balance || grid < 1) return group;
-  const int64_t g_max = std::min(std::max<int64_t>((96ll << 20) / kv, 1), BH);
-  const int64_t n_pairs = ((S_q + 127) / 128 + 1) / 2;
-  const int64_t g0 = 2 * grid / std::gcd<int64_t>(2 * grid, n_pairs);
+// Heads per scheduling group of a causal pass (forward, or one of the
+// backward's kernels).  The data the heads in flight together share should
+// fit in L2: about 48 MB a group (bytes_per_head each).  The longest units
+// come first inside each group, so a group whose units are not a whole
+// number of snake round pairs (g * ranks a multiple of 2 * grid) leaves the
+// rounds that straddle a group boundary uneven.  Such groups -- multiples of
+// g0 = 2 * grid / gcd(2 * grid, ranks), up to 96 MB -- are weighed against
+// the 48 MB group with the schedule above and taken when the busiest CTA is
+// lighter.  Measured on bf16, D = 128 causal passes against the 48 MB rule:
+// forward 4 x 32 x 4096 455 -> 414 us (19 heads), 2 x 32 x 8192 828 -> 761 us
+// (19), 8 x 32 x 4096 851-864 -> 809-812 us (38); backward 4 x 32 x 4096
+// 1542-1573 -> 1479-1499 us, 8 x 32 x 4096 3249-3340 -> 3028-3094 us (19).
+// Choices are cached per shape.
+int64_t balanced_group(int64_t n_heads, const std::vector<int64_t>& cost, int64_t bytes_per_head,
+                       int grid, bool balance) {
+  const int64_t per_head = bytes_per_head > 0 ? bytes_per_head : 1;
+  int64_t group = std::min(std::max<int64_t>((48ll << 20) / per_head, 1), n_heads);
+  const int64_t n_ranks = static_cast<int64_t>(cost.size());
+  if (!balance || grid < 1 || n_ranks < 1) return group;
+  const int64_t g_max = std::min(std::max<int64_t>((96ll << 20) / per_head, 1), n_heads);
+  const int64_t g0 = 2 * grid / std::gcd<int64_t>(2 * grid, n_ranks);
   if (g0 > g_max) return group;
   static std::mutex mu;
-  static std::map<std::array<int64_t, 5>, int64_t> cache;
-  const std::array<int64_t, 5> key = {BH, S_q, S_kv, kv_bytes, grid};
+  static std::map<std::vector<int64_t>, int64_t> cache;
+  std::vector<int64_t> key = {n_heads, per_head, grid};
+  key.insert(key.end(), cost.begin(), cost.end());
   {
     std::lock_guard<std::mutex> lock(mu);
     const auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
   std::vector<int64_t> load;
-  int64_t best = causal_makespan(BH, S_q, S_kv, group, grid, load);
+  int64_t best = snake_makespan(n_heads, cost, group, grid, load);
   for (int64_t g = g0, tries = 0; g <= g_max && tries < 8; g += g0, ++tries) {
-    const int64_t m = causal_makespan(BH, S_q, S_kv, g, grid, load);
+    const int64_t m = snake_makespan(n_heads, cost, g, grid, load);
     if (m < best) {
       best = m;
       group = g;
@@ -399,6 +393,13 @@ int64_t causal_group(int64_t BH, int64_t S_q, int64_t S_kv, int64_t kv_bytes, in
   if (cache.size() >= 1024) cache.clear();
   cache[key] = group;
   return group;
+}
+
+// Key blocks that query tile t needs under the top-left causal mask (0 for a
+// tile past S_q).
+int64_t causal_tile_blocks(int64_t t, int64_t S_q, int64_t S_kv) {
+  if (t * 128 >= S_q) return 0;
+  return std::min(std::min(t * 128 + 127, S_q - 1), S_kv - 1) / 128 + 1;
 }
 
 // The forward pass, whole (n_splits = 1: o / lse written directly) or split
@@ -454,11 +455,26 @@ fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, fl
   // Causal: heads in scheduling groups, longest pairs first inside each.
   // (K/V bytes one query head brings into L2: a key/value head is shared by
   // H / H_kv consecutive query heads.)
+  // When the K/V of all heads is at most 192 MB (about the size of L2)
+  // grouping buys little locality, and with few groups the longest-first
+  // order that restarts in each group leaves CTAs unevenly loaded (1 x 32
+  // heads x 8192 bf16: 429 us grouped by 12 heads, 382 us as one group): one
+  // group then.  Split passes keep the 48 MB rule.
   int64_t group = 1;
   if (causal) {
-    const int64_t sched_grid = std::min<int64_t>(B * H * n_pairs, dev.sm_count);
-    group = causal_group(B * H, S_q, S_kv, 2 * S_kv * D * eb * H_kv / H,
-                         static_cast<int>(sched_grid), n_splits == 1);
+    const int64_t kv_bytes = 2 * S_kv * D * eb * H_kv / H;
+    if (B * H * kv_bytes <= (192ll << 20)) {
+      group = B * H;
+    } else {
+      std::vector<int64_t> cost(static_cast<size_t>(n_pairs));
+      for (int64_t r = 0; r < n_pairs; ++r) {
+        const int64_t pair = n_pairs - 1 - r;
+        cost[static_cast<size_t>(r)] = std::max(causal_tile_blocks(2 * pair, S_q, S_kv),
+                                                causal_tile_blocks(2 * pair + 1, S_q, S_kv));
+      }
+      const int64_t sched_grid = std::min<int64_t>(B * H * n_pairs, dev.sm_count);
+      group = balanced_group(B * H, cost, kv_bytes, static_cast<int>(sched_grid), n_splits == 1);
+    }
   }
   p.group_heads = static_cast<int32_t>(group);
   p.layout = static_cast<int32_t>(layout);
@@ -715,25 +731,31 @@ fa_status_t run_backward(const void* q, const void* k, const void* v, const void
   }
 
   // dQ: one unit per (query head, query tile); causal runs group heads so
-  // that the K/V in flight fit in about 48 MB of L2 (as the forward).
+  // that the K/V in flight fit in L2, at a size that keeps the static
+  // schedule balanced (balanced_group, as the forward).
   fa::bwd::BwdParams pq = p;
   pq.num_units = static_cast<int32_t>(B * H * n_q);
   int64_t gq = 1;
   if (causal) {
-    const int64_t kv_bytes = 2 * S_kv * D * 2 * H_kv / H;
-    gq = (48ll << 20) / (kv_bytes > 0 ? kv_bytes : 1);
-    gq = gq < 1 ? 1 : (gq > B * H ? B * H : gq);
+    std::vector<int64_t> cost(static_cast<size_t>(n_q));
+    for (int64_t r = 0; r < n_q; ++r)
+      cost[static_cast<size_t>(r)] = causal_tile_blocks(n_q - 1 - r, S_q, S_kv);
+    gq = balanced_group(B * H, cost, 2 * S_kv * D * 2 * H_kv / H,
+                        static_cast<int>(std::min<int64_t>(B * H * n_q, dev.sm_count)), true);
   }
   pq.group_heads = static_cast<int32_t>(gq);
   // dK / dV: one unit per (key/value head, key tile); heads grouped so that
-  // the Q / dO their query heads stream fit in about 48 MB of L2.
+  // the Q / dO their query heads stream fit in L2 (balanced_group).
   fa::bwd::BwdParams pk = p;
   pk.num_units = static_cast<int32_t>(B * H_kv * n_kv);
   int64_t gk = 1;
   if (causal) {
-    const int64_t qdo_bytes = 2 * S_q * D * 2 * (H / H_kv);
-    gk = (48ll << 20) / (qdo_bytes > 0 ? qdo_bytes : 1);
-    gk = gk < 1 ? 1 : (gk > B * H_kv ? B * H_kv : gk);
+    // key tile j is seen by query tiles j .. n_q - 1 of each of its query heads
+    std::vector<int64_t> cost(static_cast<size_t>(n_kv));
+    for (int64_t j = 0; j < n_kv; ++j)
+      cost[static_cast<size_t>(j)] = std::max<int64_t>(0, n_q - j) * (H / H_kv);
+    gk = balanced_group(B * H_kv, cost, 2 * S_q * D * 2 * (H / H_kv),
+                        static_cast<int>(std::min<int64_t>(B * H_kv * n_kv, dev.sm_count)), true);
   }
   pk.group_heads = static_cast<int32_t>(gk);
 
