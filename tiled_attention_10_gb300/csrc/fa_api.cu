@@ -357,7 +357,8 @@ int64_t snake_makespan(int64_t n_heads, const std::vector<int64_t>& cost, int64_
 // rounds that straddle a group boundary uneven.  Such groups -- multiples of
 // g0 = 2 * grid / gcd(2 * grid, ranks), up to 96 MB -- are weighed against
 // the 48 MB group with the schedule above and taken when the busiest CTA is
-// lighter.  Measured on bf16, D = 128 causal passes against the 48 MB rule:
+// lighter (up to a million units).  Measured on bf16, D = 128 causal passes
+// against the 48 MB rule:
 // forward 4 x 32 x 4096 455 -> 414 us (19 heads), 2 x 32 x 8192 828 -> 761 us
 // (19), 8 x 32 x 4096 851-864 -> 809-812 us (38); backward 4 x 32 x 4096
 // 1542-1573 -> 1479-1499 us, 8 x 32 x 4096 3249-3340 -> 3028-3094 us (19).
@@ -370,7 +371,9 @@ int64_t balanced_group(int64_t n_heads, const std::vector<int64_t>& cost, int64_
   if (!balance || grid < 1 || n_ranks < 1) return group;
   const int64_t g_max = std::min(std::max<int64_t>((96ll << 20) / per_head, 1), n_heads);
   const int64_t g0 = 2 * grid / std::gcd<int64_t>(2 * grid, n_ranks);
-  if (g0 > g_max) return group;
+  // (The model walks every unit: beyond a million units the first call of a
+  // shape would spend milliseconds on it, so those keep the 48 MB group.)
+  if (g0 > g_max || n_heads * n_ranks > (int64_t(1) << 20)) return group;
   static std::mutex mu;
   static std::map<std::vector<int64_t>, int64_t> cache;
   std::vector<int64_t> key = {n_heads, per_head, grid};
