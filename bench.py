@@ -2,7 +2,7 @@
 """Benchmark of the FlashAttention forward pass (libfa_b200) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline]
+                    [--workload NAME] [--no-cpu-baseline] [--oracle-full]
 
 One step = one fa_fwd call over the whole workload (default: bf16
 B=4, H=32, S_q=S_kv=4096, D=128, BNSD, non-causal), inputs resident in HBM.
@@ -240,6 +240,113 @@ def cpu_baseline_bwd(w, x, do):
                       f"query head(s) x {w.S_q} x {w.S_kv}, float64 numpy, {t:.1f} s"}
 
 
+def visible_pairs(w) -> int:
+    """(query, key) pairs the mask leaves visible over the whole workload:
+    one exponential each in the softmax (top-left causal: row i sees keys
+    0..min(i, S_kv - 1))."""
+    if not w.causal:
+        per_head = w.S_q * w.S_kv
+    else:
+        n = min(w.S_q, w.S_kv)            # rows 0..n-1 see i + 1 keys
+        per_head = n * (n + 1) // 2 + max(0, w.S_q - n) * w.S_kv
+    return w.B * w.H * per_head
+
+
+def secondary_ceilings(pairs: int, launch_s: float, sms: int, sm_mhz: float, clock_src: str):
+    """The softmax's own ceilings beside the tensor roofline: the MUFU unit's
+    exponentials (one ex2 per visible pair, 32 per clock per SM, measured with
+    a microbenchmark) and the FP32 pipe's softmax arithmetic (three operations
+    per visible pair -- the scale-and-subtract FMA, the max and the row-sum add
+    -- at 128 per clock per SM)."""
+    hz = sm_mhz * 1e6
+    out = {}
+    for name, per_pair, per_clk in (("mufu_ex2", 1, 32), ("fp32_softmax", 3, 128)):
+        ops = per_pair * pairs
+        peak = per_clk * sms * hz
+        out[name] = {"ops_per_launch": ops, "achieved_per_s": round(ops / launch_s, 1),
+                     "peak_per_s": round(peak, 1), "frac": round(ops / launch_s / peak, 4),
+                     "peak_source": f"{per_clk} per clock per SM x {sms} SMs x {sm_mhz:.0f} MHz "
+                                    f"({clock_src})"}
+    return out
+
+
+def timing_summary(per_launch_ms, flops=None):
+    """Mean, median and min of the per-call CUDA-event times (and the TFLOP/s
+    each gives)."""
+    t = {"ms_mean": round(statistics.mean(per_launch_ms), 5),
+         "ms_median": round(statistics.median(per_launch_ms), 5),
+         "ms_min": round(min(per_launch_ms), 5),
+         "how": "CUDA events recorded on the launching stream between consecutive calls"}
+    if flops:
+        for k in ("mean", "median", "min"):
+            t[f"tflops_{k}"] = round(flops / (t[f"ms_{k}"] * 1e-3) / 1e12, 2)
+    return t
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu model")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def run_oracle_full(args, w, world, rank):
+    """The float64 oracle timed on the whole workload on the host cores (every
+    row); for a workload too large for that, on seeded sample rows with the
+    full time extrapolated by FLOPs (and labelled so).  One JSON line."""
+    if rank != 0:
+        return 0
+    import oracle
+    import torch
+    from tiled_attention_10_gb300.inputs import make_inputs, sample_rows
+    oracle.build()
+    cores = oracle.max_threads()
+    full = w.B * w.H * w.S_q * w.S_kv <= (1 << 34)
+    line = {"oracle_full": w.name, "cores": cores, "cpu": cpu_model(), "dtype": "f64",
+            "nominal_flops": w.flops}
+    if full:
+        x = make_inputs(w)
+        t0 = time.perf_counter()
+        oracle.attention_full(x.q, x.k, x.v, dtype=w.dtype, layout=w.layout, B=w.B, H=w.H,
+                              S_q=w.S_q, S_kv=w.S_kv, D=w.D, scale=w.softmax_scale,
+                              causal=w.causal, descale=x.descale, H_kv=w.kv_heads)
+        t = time.perf_counter() - t0
+        line.update({"seconds": round(t, 3), "gflops": round(w.flops / t / 1e9, 3),
+                     "scope": "every row of every head", "extrapolated": False})
+    else:
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        x = make_inputs(w, device=dev)
+        rows = [tuple(int(v) for v in r) for r in sample_rows(w, 64, seed=0)]
+        g = w.H // w.kv_heads
+        spent, done = 0.0, 0.0
+        for (b, h, i) in rows:
+            hk = h // g
+            if w.layout == "BNSD":
+                qh, kh, vh = x.q[b, h].cpu(), x.k[b, hk].cpu(), x.v[b, hk].cpu()
+            else:
+                qh, kh, vh = x.q[b, :, h].cpu(), x.k[b, :, hk].cpu(), x.v[b, :, hk].cpu()
+            t0 = time.perf_counter()
+            oracle.attention_rows(qh, kh, vh, dtype=w.dtype, layout="BNSD", B=1, H=1, S_q=w.S_q,
+                                  S_kv=w.S_kv, D=w.D, scale=w.softmax_scale, causal=w.causal,
+                                  rows=[(0, 0, i)], descale=x.descale)
+            spent += time.perf_counter() - t0
+            done += 4.0 * w.D * (min(i + 1, w.S_kv) if w.causal else w.S_kv)
+        rate = done / spent
+        line.update({"seconds_sample": round(spent, 3), "sample": f"{len(rows)} seeded (b, h, row) "
+                     "samples, one row per oracle call (one thread's work)",
+                     "gflops_sample": round(rate / 1e9, 3),
+                     "seconds": round(w.flops / rate, 1), "extrapolated": True,
+                     "scope": "extrapolated: total FLOPs / the sample's FLOP rate (rows one at a "
+                              "time; the full run would spread rows over all cores)"})
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------------------
 # Arms.
 # ---------------------------------------------------------------------------
@@ -450,6 +557,9 @@ def run_ours(args, w, world, rank, local):
     launch_ms = statistics.mean(per_launch)
     achieved = flops / (launch_ms * 1e-3) / 1e12
     in_bytes = h2d
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clk, clk_src = ((clocks["sm_mhz"], "median SM clock sampled during the timed calls")
+                    if clocks.get("sm_mhz") else (peaks.get("sm_max_mhz", 2070.0), "maximum SM clock"))
     line = {
         "metric": "attention fwd TFLOP/s", "value": round(value, 3), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -464,7 +574,10 @@ def run_ours(args, w, world, rank, local):
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(w.name),
                      "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} bf16 GEMM"
-                                    f"{' x2 (fp8 nominal ratio)' if w.dtype == 'e4m3' else ''}"},
+                                    f"{' x2 (fp8 nominal ratio)' if w.dtype == 'e4m3' else ''}",
+                     "secondary": secondary_ceilings(visible_pairs(w), launch_ms * 1e-3, sms, clk,
+                                                     clk_src)},
+        "timing": timing_summary(per_launch, flops),
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "how": e2e_how},
         "gpu_launches": args.steps * launches_per_step,
@@ -573,6 +686,7 @@ def run_ours_bwd(args, w, world, rank, local):
                      "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} bf16 GEMM"},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "how": e2e_how},
+        "timing": timing_summary(per_step, flops),
         "gpu_launches": args.steps * 3,
         "clocks": clocks,
     }
@@ -769,6 +883,7 @@ def run_ours_packed(args, w, world, rank, local):
         "roofline": roof,
         "e2e": {"value": round(e2e_val, 3), "unit": unit, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "how": e2e_how},
+        "timing": timing_summary(per_launch, None if w.decode else w.flops),
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
     }
@@ -791,6 +906,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-full", action="store_true",
+                    help="time the float64 oracle on the whole workload (host cores) and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -798,6 +915,8 @@ def main(argv=None):
     w = {**ALL_WORKLOADS, **PACKED_WORKLOADS}[args.workload or HEADLINE]
     world, rank, local = dist_setup()
     try:
+        if args.oracle_full:
+            return run_oracle_full(args, w, world, rank)
         if hasattr(w, "seq_q"):
             if args.impl == "reference":
                 return run_reference_packed(args, w, world, rank)

@@ -67,6 +67,11 @@ typedef enum {
  * B, H, S_q, S_kv, D   sizes; all >= 1, D in {64, 128}.  Offsets are 64-bit:
  *      a single tensor may exceed 4 GB (the Hygon retrospective, defect 1).
  * scale  finite, >= 0; multiplies Q K^T before the softmax (commonly D^-0.5).
+ *      A narrowing of the definition: the reference attention of the Ascend
+ *      page (section 4.3) holds for any real scale, but the kernel takes each
+ *      row's maximum of the unscaled scores, which is the maximum of the
+ *      scaled ones only for scale >= 0; a negative scale is refused with
+ *      FA_ERR_INVALID_ARG (negate q, or k, and pass -scale instead).
  * layout FA_LAYOUT_BNSD or FA_LAYOUT_BSND (o follows q's layout).
  * causal 0: every key visible.  Non-zero: query row i sees key j only if j <= i
  *      (top-left aligned, the verifier's triu(diagonal=1) mask; with S_q == S_kv
@@ -160,7 +165,8 @@ fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
  * (a file-scope __device__ array, one copy per device).
  *
  * Arguments, checks and statuses as fa_fwd_splitkv, without workspace and
- * workspace_bytes.  n_splits = 1 uses no scratch at all.
+ * workspace_bytes: its host checks run first, then the capacity check below.
+ * n_splits = 1 uses no scratch at all.
  *   Limit: the workspace fa_fwd_splitkv would need for these B, H, S_q, D
  *   and n_splits (fp32 partial O and lse, 4 * n_splits * B * H * S_q *
  *   (D + 1) bytes plus alignment) must fit in FA_NOALLOC_SCRATCH_BYTES;
@@ -169,8 +175,10 @@ fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
  *   Zeroing: none needed; every partial the merge reads is written earlier
  *   in the same call.
  *   First call on a device: looks up the buffer's device address with that
- *   device current (cudaGetSymbolAddress) and caches it; FA_ERR_CUDA if the
- *   lookup fails.  If the calls are to be made while a stream is being
+ *   device current (cudaGetSymbolAddress) and caches it for the calling
+ *   thread's current context; a call in another context (after a device
+ *   reset, or from a caller that switched contexts) looks it up again.
+ *   FA_ERR_CUDA if the lookup fails.  If the calls are to be made while a stream is being
  *   captured, make one call on each device before capture begins, so that
  *   this setup happens outside the capture.
  *   Overlap: all callers on a device share the one buffer.  Two calls whose

@@ -21,3 +21,18 @@ def cuda_lib():
         pytest.fail("GPU test collected on a machine without CUDA")
     from tiled_attention_10_gb300 import binding
     return binding.load()
+
+
+@pytest.fixture(scope="session")
+def built_lib():
+    """The C-ABI library for host-only tests (no kernel launch): built here if
+    nvcc is available, else the one already built; skipped on a host that has
+    neither (a CPU machine without the CUDA toolkit)."""
+    import shutil
+    from tiled_attention_10_gb300 import binding, build
+    have_nvcc = shutil.which("nvcc") or os.path.exists("/usr/local/cuda/bin/nvcc")
+    if have_nvcc:
+        build.build()
+    elif not os.path.exists(build.LIB):
+        pytest.skip("no nvcc and no built library on this host")
+    return binding.load()

@@ -82,6 +82,22 @@ def compare_full(w: Workload, r: Run, x):
     return float(np.abs(og - O).max()), float(np.abs(lg - lse).max()), og, lg
 
 
+def error_stats(got: np.ndarray, ref: np.ndarray, tol: float) -> dict:
+    """The accuracy figures the Ascend page's verifier prints (section 4.3 of
+    "ops-transformer FlashAttention build and tuning"): max and mean absolute
+    difference, and how many elements lie within the tolerance."""
+    d = np.abs(got - ref)
+    return {"max_abs": float(d.max()), "mean_abs": float(d.mean()),
+            "within_tol": int((d <= tol).sum()), "elements": int(d.size), "tol": tol}
+
+
+def stats_line(name: str, so: dict, sl: dict) -> str:
+    return (f"{name}: O max abs {so['max_abs']:.3g}, mean abs {so['mean_abs']:.3g}, "
+            f"{so['within_tol']}/{so['elements']} within {so['tol']:g}; "
+            f"lse max abs {sl['max_abs']:.3g}, mean abs {sl['mean_abs']:.3g}, "
+            f"{sl['within_tol']}/{sl['elements']} within {sl['tol']:g}")
+
+
 def check(w: Workload, r: Run, err_o: float, err_l: float, og=None, lg=None):
     assert r.status == 0, binding.FA_STATUS.get(r.status)
     assert r.device_status == 0, binding.FA_STATUS.get(r.device_status)

@@ -7,15 +7,14 @@ import re
 
 import pytest
 
-from tiled_attention_10_gb300 import binding, build
+from tiled_attention_10_gb300 import binding
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.fixture(scope="module")
-def lib():
-    build.build()
-    return binding.load()
+def lib(built_lib):
+    return built_lib
 
 
 def _declared_functions():

@@ -155,12 +155,9 @@ def test_no_alloc_near_scratch_capacity(cuda_lib):
     assert bool((out.o_buf.view(torch.int16) == CANARY16).all())
 
 
-def test_no_alloc_refuses_oversize_on_host():
+def test_no_alloc_refuses_oversize_on_host(built_lib):
     # Fake pointers, never dereferenced: a problem whose partials exceed the
     # scratch fails before any CUDA call, so this runs without a GPU.
-    from tiled_attention_10_gb300 import build
-    build.build()
-    binding.load()
     base = (16, 32, 48, 64, 80, 1, 1, 1, 65028, 256, 128, 0.1, "BNSD", 0, "bf16", None, None, None)
     assert binding.fa_fwd_splitkv_noalloc(*base, 2) == 2          # 256 bytes over: unsupported
     big = (16, 32, 48, 64, 80, 1, 64, 8, 65536, 65536, 128, 0.1, "BNSD", 0, "bf16", None, None,

@@ -61,35 +61,72 @@ std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
+  CUcontext ctx = nullptr;   // the context the facts below were looked up in
   int sm_count = 0;
   uint32_t* err_word = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
 
-// The device whose primary context this thread has made current.  Tensor-map
-// encoding is a driver call that needs a current context; a thread on which
-// no CUDA runtime call has touched the device yet (a framework's worker
-// thread, say) has none, so it is made current once per thread and device
-// (cudaSetDevice on the device the thread already reports, which changes
-// nothing the caller chose).
-thread_local int t_ctx_dev = -1;
+// cuCtxGetCurrent through the runtime's driver entry point (the library does
+// not link libcuda directly).
+PFN_cuCtxGetCurrent_v4000 ctx_get_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+  });
+  return fn;
+}
 
-// Per-device facts, looked up once with that device current.
+}  // namespace
+
+namespace fa {
+// The calling thread's current context, made current first if the thread has
+// none.  Tensor-map encoding is a driver call that needs one, and a thread on
+// which no CUDA runtime call has touched the device yet (a framework's worker
+// thread, say) has none: the current device's primary context is then made
+// current (cudaSetDevice on the device the thread already reports, which
+// changes nothing the caller chose).  A context the caller made current --
+// primary or not -- is left as it is.  Null if no context can be had.
+CUcontext current_context(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  auto get = ctx_get_fn();
+  if (!get) return nullptr;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return nullptr;
+  if (!ctx) {
+    if (cudaSetDevice(dev) != cudaSuccess || get(&ctx) != CUDA_SUCCESS) return nullptr;
+  }
+  if (dev_out) *dev_out = dev;
+  return ctx;
+}
+}  // namespace fa
+
+namespace {
+
+// Per-device facts, looked up with that device current and kept until the
+// thread's current context on that device changes (a device reset, or a
+// caller that switches contexts, moves the module's symbols: the device
+// error word is then looked up again).
 fa_status_t device_info(DeviceInfo* out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
-  if (t_ctx_dev != dev) {
-    if (cudaSetDevice(dev) != cudaSuccess) return FA_ERR_CUDA;
-    t_ctx_dev = dev;
-  }
+  const CUcontext ctx = fa::current_context(&dev);
+  if (!ctx || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   DeviceInfo& d = g_dev[dev];
-  if (!d.ready) {
+  if (!d.ready || d.ctx != ctx) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FA_ERR_CUDA;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_fa_device_error) != cudaSuccess) return FA_ERR_CUDA;
+    d.ctx = ctx;
     d.sm_count = sms;
     d.err_word = static_cast<uint32_t*>(p);
     d.ready = true;
@@ -329,6 +366,29 @@ fa_status_t check_args(const void* q, const void* k, const void* v, const void* 
 }
 
 constexpr int kMaxSplits = 32;
+
+}  // namespace
+
+namespace fa {
+// Host checks of a split-KV call, apart from its workspace (all before any
+// CUDA call); fa_fwd_splitkv and the no-allocation entry point share them.
+fa_status_t check_splitkv_args(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, int64_t B, int64_t H, int64_t H_kv, int64_t S_q,
+                               int64_t S_kv, int64_t D, float scale, fa_layout_t layout,
+                               fa_dtype_t dtype, const float* descale_q, const float* descale_k,
+                               const float* descale_v, int n_splits) {
+  const fa_status_t st = check_args(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout,
+                                    dtype, descale_q, descale_k, descale_v);
+  if (st != FA_OK) return st;
+  if (n_splits < 1) return FA_ERR_INVALID_ARG;
+  if (n_splits > kMaxSplits) return FA_ERR_UNSUPPORTED;
+  if (n_splits > 1 && static_cast<double>(n_splits) * B * H * S_q * ((S_q + 127) / 128) > 2e9)
+    return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+}  // namespace fa
+
+namespace {
 
 // The busiest CTA's load under the kernels' static schedule: units in groups
 // of g heads, rank-major inside a group (heads vary fastest; rank r costs
@@ -580,17 +640,14 @@ fa_status_t fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o,
                            fa_dtype_t dtype, const float* descale_q, const float* descale_k,
                            const float* descale_v, int n_splits, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream) {
-  const fa_status_t st = check_args(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout,
-                                    dtype, descale_q, descale_k, descale_v);
+  const fa_status_t st = fa::check_splitkv_args(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale,
+                                                layout, dtype, descale_q, descale_k, descale_v,
+                                                n_splits);
   if (st != FA_OK) return st;
-  if (n_splits < 1) return FA_ERR_INVALID_ARG;
-  if (n_splits > kMaxSplits) return FA_ERR_UNSUPPORTED;
   if (n_splits > 1) {
     if (!workspace || workspace_bytes < split_workspace_bytes(B, H, S_q, D, n_splits))
       return FA_ERR_INVALID_ARG;
     if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
-    if (static_cast<double>(n_splits) * B * H * S_q * ((S_q + 127) / 128) > 2e9)
-      return FA_ERR_UNSUPPORTED;
   }
   return run_forward(q, k, v, o, lse, B, H, H_kv, S_q, S_kv, D, scale, layout, causal, dtype,
                      descale_q, descale_k, descale_v, n_splits, workspace, stream);
