@@ -276,7 +276,8 @@ def timing_summary(per_launch_ms, flops=None):
     t = {"ms_mean": round(statistics.mean(per_launch_ms), 5),
          "ms_median": round(statistics.median(per_launch_ms), 5),
          "ms_min": round(min(per_launch_ms), 5),
-         "how": "CUDA events recorded on the launching stream between consecutive calls"}
+         "how": "a second pass of as many calls right after the timed region, a CUDA event "
+                "on the launching stream between consecutive calls"}
     if flops:
         for k in ("mean", "median", "min"):
             t[f"tflops_{k}"] = round(flops / (t[f"ms_{k}"] * 1e-3) / 1e12, 2)
@@ -319,30 +320,43 @@ def run_oracle_full(args, w, world, rank):
         line.update({"seconds": round(t, 3), "gflops": round(w.flops / t / 1e9, 3),
                      "scope": "every row of every head", "extrapolated": False})
     else:
+        # Every row of one (batch, head) pair -- the same shape per head as the
+        # whole workload -- timed on all cores, then scaled by FLOPs to the
+        # B*H pairs (labelled as an extrapolation); plus the 64 seeded sample
+        # rows the parity test checks, one oracle call each.
         dev = "cuda" if torch.cuda.is_available() else "cpu"
         x = make_inputs(w, device=dev)
+        if w.layout == "BNSD":
+            qh, kh, vh = x.q[:1, :1].cpu(), x.k[:1, :1].cpu(), x.v[:1, :1].cpu()
+        else:
+            qh, kh, vh = (x.q[:1, :, :1].cpu(), x.k[:1, :, :1].cpu(), x.v[:1, :, :1].cpu())
+        t0 = time.perf_counter()
+        oracle.attention_full(qh, kh, vh, dtype=w.dtype, layout=w.layout, B=1, H=1, S_q=w.S_q,
+                              S_kv=w.S_kv, D=w.D, scale=w.softmax_scale, causal=w.causal,
+                              descale=x.descale)
+        t_head = time.perf_counter() - t0
+        head_flops = w.flops / (w.B * w.H)
         rows = [tuple(int(v) for v in r) for r in sample_rows(w, 64, seed=0)]
         g = w.H // w.kv_heads
-        spent, done = 0.0, 0.0
+        spent = 0.0
         for (b, h, i) in rows:
             hk = h // g
             if w.layout == "BNSD":
-                qh, kh, vh = x.q[b, h].cpu(), x.k[b, hk].cpu(), x.v[b, hk].cpu()
+                qr, kr, vr = x.q[b, h].cpu(), x.k[b, hk].cpu(), x.v[b, hk].cpu()
             else:
-                qh, kh, vh = x.q[b, :, h].cpu(), x.k[b, :, hk].cpu(), x.v[b, :, hk].cpu()
+                qr, kr, vr = x.q[b, :, h].cpu(), x.k[b, :, hk].cpu(), x.v[b, :, hk].cpu()
             t0 = time.perf_counter()
-            oracle.attention_rows(qh, kh, vh, dtype=w.dtype, layout="BNSD", B=1, H=1, S_q=w.S_q,
+            oracle.attention_rows(qr, kr, vr, dtype=w.dtype, layout="BNSD", B=1, H=1, S_q=w.S_q,
                                   S_kv=w.S_kv, D=w.D, scale=w.softmax_scale, causal=w.causal,
                                   rows=[(0, 0, i)], descale=x.descale)
             spent += time.perf_counter() - t0
-            done += 4.0 * w.D * (min(i + 1, w.S_kv) if w.causal else w.S_kv)
-        rate = done / spent
-        line.update({"seconds_sample": round(spent, 3), "sample": f"{len(rows)} seeded (b, h, row) "
-                     "samples, one row per oracle call (one thread's work)",
-                     "gflops_sample": round(rate / 1e9, 3),
-                     "seconds": round(w.flops / rate, 1), "extrapolated": True,
-                     "scope": "extrapolated: total FLOPs / the sample's FLOP rate (rows one at a "
-                              "time; the full run would spread rows over all cores)"})
+        line.update({"seconds_one_head": round(t_head, 3),
+                     "gflops_one_head": round(head_flops / t_head / 1e9, 3),
+                     "seconds": round(t_head * w.B * w.H, 1), "extrapolated": True,
+                     "scope": f"extrapolated: every row of (batch 0, head 0) timed, times the "
+                              f"{w.B * w.H} (batch, head) pairs",
+                     "sample_rows": len(rows), "seconds_sample_rows": round(spent, 3),
+                     "seconds_per_sample_row": round(spent / len(rows), 4)})
     print(json.dumps(line), flush=True)
     return 0
 
@@ -471,6 +485,32 @@ def e2e_ms_per_step(torch, stream, host_in, dev_in, run, dev_out, host_out, step
             E2E_STREAMED if streamed else E2E_SERIAL)
 
 
+def timed_steps(torch, stream, step, steps, world):
+    """The timed region: `steps` calls between two CUDA events on the launching
+    stream, bracketed by a barrier and a synchronize on both sides; returns its
+    milliseconds.  Then, outside it, the same number of calls each between its
+    own pair of events (events between calls add a little per call, which
+    matters for calls of a few microseconds): the per-call list for the median
+    and minimum."""
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = e0.elapsed_time(e1)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return total_ms, [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+
+
 def run_ours(args, w, world, rank, local):
     import torch
     from tiled_attention_10_gb300 import binding
@@ -519,18 +559,8 @@ def run_ours(args, w, world, rank, local):
     if binding.fa_last_device_error(sp) != 0:
         raise RuntimeError("device-side error during warm-up")
 
-    barrier(world)
-    torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step()
-        ev[i + 1].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    total_ms, per_launch = timed_steps(torch, stream, step, args.steps, world)
     clocks = ClockSampler.summarize(sampler.stop())
-    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
     ms = total_ms / args.steps
     ms_max = max_over_ranks(ms, world)
     if binding.fa_last_device_error(sp) != 0:
@@ -554,7 +584,7 @@ def run_ours(args, w, world, rank, local):
     peaks, peak_src = load_peaks()
     sustained = total_ms > 1000.0
     peak = tensor_peak(peaks, w.dtype, sustained)
-    launch_ms = statistics.mean(per_launch)
+    launch_ms = ms
     achieved = flops / (launch_ms * 1e-3) / 1e12
     in_bytes = h2d
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -631,18 +661,8 @@ def run_ours_bwd(args, w, world, rank, local):
     torch.cuda.synchronize()
     if binding.fa_last_device_error(sp) != 0:
         raise RuntimeError("device-side error during warm-up")
-    barrier(world)
-    torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step()
-        ev[i + 1].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    total_ms, per_step = timed_steps(torch, stream, step, args.steps, world)
     clocks = ClockSampler.summarize(sampler.stop())
-    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
     ms_max = max_over_ranks(total_ms / args.steps, world)
     if binding.fa_last_device_error(sp) != 0:
         raise RuntimeError("device-side error during the timed steps")
@@ -664,7 +684,7 @@ def run_ours_bwd(args, w, world, rank, local):
     peaks, peak_src = load_peaks()
     sustained = total_ms > 1000.0
     peak = tensor_peak(peaks, w.dtype, sustained)
-    step_ms = statistics.mean(per_step)
+    step_ms = total_ms / args.steps
     achieved = flops / (step_ms * 1e-3) / 1e12
     # Products the tensor cores actually run per step: the dQ kernel
     # recomputes S and dP, so 7 forward-sized products against the 5 counted.
@@ -817,18 +837,8 @@ def run_ours_packed(args, w, world, rank, local):
     torch.cuda.synchronize()
     if binding.fa_last_device_error(sp) != 0:
         raise RuntimeError("device-side error during warm-up")
-    barrier(world)
-    torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    ev[0].record(stream)
-    for i in range(args.steps):
-        step()
-        ev[i + 1].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
+    total_ms, per_launch = timed_steps(torch, stream, step, args.steps, world)
     clocks = ClockSampler.summarize(sampler.stop())
-    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
     ms_max = max_over_ranks(total_ms / args.steps, world)
     if binding.fa_last_device_error(sp) != 0:
         raise RuntimeError("device-side error during the timed steps")
@@ -846,7 +856,7 @@ def run_ours_packed(args, w, world, rank, local):
     if rank != 0:
         return 0
     peaks, peak_src = load_peaks()
-    launch_ms = statistics.mean(per_launch)
+    launch_ms = total_ms / args.steps
     q_bytes = x.q.numel() * x.q.element_size()
     algo_bytes = w.kv_bytes + q_bytes + d2h       # K / V read once, Q read, O and lse written
     if w.decode:

@@ -104,6 +104,10 @@ EXTRA_WORKLOADS = {
     # causal, bf16) at 4 x 4096 tokens: the pass the backward workload follows
     "bf16_causal_4x32x4096x128": Workload("bf16_causal_4x32x4096x128", 4, 32, 4096, 4096, 128,
                                           "bf16", "BNSD", True),
+    # one batch of the 16 x 64 x 16384 causal workload (same shape per head,
+    # values N(0, 0.5^2)): small enough for a profiler capture of one launch
+    "bf16_causal_1x64x16384x128": Workload("bf16_causal_1x64x16384x128", 1, 64, 16384, 16384,
+                                           128, "bf16", "BNSD", True, std=0.5),
     # few heads, short queries, long keys: split-KV fills the GPU
     "bf16_splitkv_1x8x512x16384x128": Workload("bf16_splitkv_1x8x512x16384x128", 1, 8, 512, 16384,
                                                128, "bf16", "BNSD", False, split=True),
