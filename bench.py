@@ -502,11 +502,20 @@ def timed_steps(torch, stream, step, steps, world):
     torch.cuda.synchronize()
     barrier(world)
     total_ms = e0.elapsed_time(e1)
+    timed_steps.host_us = None
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     ev[0].record(stream)
     for i in range(steps):
         step()
         ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    # Host time to issue one call (argument checks, tensor maps, launch), by
+    # the wall clock over a burst of calls that the device has not caught up
+    # with: when it is below the per-call device time, the device sets the pace.
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    timed_steps.host_us = (time.perf_counter() - t0) / steps * 1e6
     torch.cuda.synchronize()
     return total_ms, [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
 
@@ -607,7 +616,8 @@ def run_ours(args, w, world, rank, local):
                                     f"{' x2 (fp8 nominal ratio)' if w.dtype == 'e4m3' else ''}",
                      "secondary": secondary_ceilings(visible_pairs(w), launch_ms * 1e-3, sms, clk,
                                                      clk_src)},
-        "timing": timing_summary(per_launch, flops),
+        "timing": {**timing_summary(per_launch, flops),
+                   "host_us_per_call": round(timed_steps.host_us, 2)},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "how": e2e_how},
         "gpu_launches": args.steps * launches_per_step,
