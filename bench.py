@@ -35,10 +35,17 @@ if ROOT not in sys.path:
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
+FWD_SOURCES = ("fa_api.cu", "fa_kernel.cuh", "fa_ptx.cuh", "fa_tmem_io.cuh", "fa_inst_*.cu")
+
+
 def kernel_source_sha() -> str:
-    """Hash of the CUDA sources: ties a recorded ncu capture to the kernel it measured."""
+    """Hash of the forward kernel's sources (kernel, PTX helpers, instantiations and the host
+    code that sets up its launch): ties a recorded ncu capture to the kernel it measured."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "tiled_attention_10_gb300", "csrc", "*"))):
+    files = set()
+    for pat in FWD_SOURCES:
+        files.update(glob.glob(os.path.join(ROOT, "tiled_attention_10_gb300", "csrc", pat)))
+    for f in sorted(files):
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

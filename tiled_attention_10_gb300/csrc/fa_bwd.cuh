@@ -464,11 +464,18 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
     for (int j = 0; j < n; ++j) {
       const bool has_next = j + 1 < n;
       int slotKn = slotK;
+      // The barriers of this block, probed together without blocking (this
+      // thread sets the pace and a blocking wait costs it about a product):
+      // bit 0 K_{j+1} loaded, 1 S read, 2 dS_j written, 3 V_{j+1} loaded.
+      const uint32_t done = (mbar_test_wait(bars.kfull(kr.slot), kr.phase) ? 1u : 0u) |
+                            (mbar_test_wait(bars.s_free(), (s_issued - 1) & 1u) ? 2u : 0u) |
+                            (mbar_test_wait(bars.ds_ready(), ds_ph) ? 4u : 0u) |
+                            (mbar_test_wait(bars.vfull(vr.slot), vr.phase) ? 8u : 0u);
       if (has_next) {
         slotKn = kr.slot;
-        if (!mbar_wait(bars.kfull(slotKn), kr.phase, wc)) { ok = false; break; }
+        if (!(done & 1u) && !mbar_wait(bars.kfull(slotKn), kr.phase, wc)) { ok = false; break; }
         kr.advance();
-        if (!mbar_wait(bars.s_free(), (s_issued - 1) & 1u, wc)) { ok = false; break; }
+        if (!(done & 2u) && !mbar_wait(bars.s_free(), (s_issued - 1) & 1u, wc)) { ok = false; break; }
         tc_fence_after();
         issue_ss<D, DT>(tS, q_lo, k_kmaj0 + slotKn * kTileW);
         umma_commit(bars.s_full());
@@ -476,7 +483,7 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
       }
       // dQ (+)= dS_j K_j once dS_j is in TMEM; the first product of a unit
       // overwrites dQ, after the previous unit's epilogue has read it.
-      if (!mbar_wait(bars.ds_ready(), ds_ph, wc)) { ok = false; break; }
+      if (!(done & 4u) && !mbar_wait(bars.ds_ready(), ds_ph, wc)) { ok = false; break; }
       ds_ph ^= 1u;
       if (j == 0 && units > 0 && !mbar_wait(bars.dq_free(), (units - 1) & 1u, wc)) { ok = false; break; }
       tc_fence_after();
@@ -484,7 +491,7 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
       umma_commit(bars.kempty(slotK));
       if (has_next) {
         const int slotV = vr.slot;
-        if (!mbar_wait(bars.vfull(slotV), vr.phase, wc)) { ok = false; break; }
+        if (!(done & 8u) && !mbar_wait(bars.vfull(slotV), vr.phase, wc)) { ok = false; break; }
         vr.advance();
         tc_fence_after();
         issue_ss<D, DT>(tDP, do_lo, v_kmaj0 + slotV * kTileW);
@@ -844,22 +851,27 @@ __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const K
     umma_commit(bars.dp_full());
     for (int s = 0; s < k.n_steps; ++s) {
       const bool has_next = s + 1 < k.n_steps;
+      // Probed together without blocking: bit 0 P^T written, 1 the next
+      // query tile loaded, 2 dS^T written.
+      const uint32_t done = (mbar_test_wait(bars.p_ready(), p_ph) ? 1u : 0u) |
+                            (mbar_test_wait(bars.full(ring.slot), ring.phase) ? 2u : 0u) |
+                            (mbar_test_wait(bars.ds_ready(), ds_ph) ? 4u : 0u);
       // dV (+)= P^T dO_s.
-      if (!mbar_wait(bars.p_ready(), p_ph, wc)) { ok = false; break; }
+      if (!(done & 1u) && !mbar_wait(bars.p_ready(), p_ph, wc)) { ok = false; break; }
       p_ph ^= 1u;
       tc_fence_after();
       issue_ts<D, DT, true>(tDV, tS, q_mn0 + st * kStageW + kTileW, s > 0 ? 1u : 0u);
       int st_n = st;
       if (has_next) {
         st_n = ring.slot;
-        if (!mbar_wait(bars.full(st_n), ring.phase, wc)) { ok = false; break; }
+        if (!(done & 2u) && !mbar_wait(bars.full(st_n), ring.phase, wc)) { ok = false; break; }
         ring.advance();
         tc_fence_after();
         issue_ss<D, DT>(tS, k_lo, q_kmaj0 + st_n * kStageW);
         umma_commit(bars.s_full());
       }
       // dK (+)= dS^T Q_s.
-      if (!mbar_wait(bars.ds_ready(), ds_ph, wc)) { ok = false; break; }
+      if (!(done & 4u) && !mbar_wait(bars.ds_ready(), ds_ph, wc)) { ok = false; break; }
       ds_ph ^= 1u;
       tc_fence_after();
       issue_ts<D, DT, true>(tDK, tDP, q_mn0 + st * kStageW, s > 0 ? 1u : 0u);
