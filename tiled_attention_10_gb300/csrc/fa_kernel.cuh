@@ -331,6 +331,15 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, u
   else
     tma_load_4d(dst, map, bar, c0, h, s, b);
 }
+// A query tile: read once, so marked evict-first in L2.
+__device__ __forceinline__ void tma_q_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                           int layout, int32_t c0, int32_t s, int32_t h, int32_t b,
+                                           uint64_t pol) {
+  if (layout == 0)
+    tma_load_4d_hint(dst, map, bar, c0, s, h, b, pol);
+  else
+    tma_load_4d_hint(dst, map, bar, c0, h, s, b, pol);
+}
 
 struct Bars {
   uint32_t base;
@@ -408,6 +417,7 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
   using C = Cfg<D, DT>;
   uint32_t ring = 0, it = 0;
   bool ok = true;
+  const uint64_t pol_stream = l2_policy_evict_first();
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0; ok; ++w) {
     const int u = unit_of_round(w, grid, bid);
@@ -430,8 +440,8 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
         // block, then per step: V of each slot's block, K of each slot's next.
         mbar_arrive_expect_tx(bars.q_full(), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_tile(sQ + c * C::kChunkBytes, tmQ, bars.q_full(), p.layout, c * C::kBoxElems,
-                   item.qt * kBM, h, b);
+          tma_q_tile(sQ + c * C::kChunkBytes, tmQ, bars.q_full(), p.layout, c * C::kBoxElems,
+                     item.qt * kBM, h, b, pol_stream);
         ++it;
         auto load = [&](int kv, int blk) -> bool {
           const int slot = static_cast<int>(ring % C::kSlots);
@@ -455,9 +465,9 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
     for (int t = 0; t < 2; ++t) {
       if ((t == 0 ? n0 : n1) == 0) continue;
       for (int c = 0; c < C::kChunks; ++c)
-        tma_tile(sQ + t * C::kTileBytes + c * C::kChunkBytes, tmQ, bars.q_full(), p.layout,
-                 c * C::kBoxElems, static_cast<int32_t>(item.q_row0) + (2 * pair + t) * tok_per_tile,
-                 h, b);
+        tma_q_tile(sQ + t * C::kTileBytes + c * C::kChunkBytes, tmQ, bars.q_full(), p.layout,
+                   c * C::kBoxElems, static_cast<int32_t>(item.q_row0) + (2 * pair + t) * tok_per_tile,
+                   h, b, pol_stream);
     }
     ++it;
     // Paged: the sequence's block-table row and last page; block j + 1's
@@ -1184,13 +1194,15 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
           tma_store_4d(tmOp, stage, 32 * bx, static_cast<int32_t>(item.q_row0) + box_row0,
                        bh << shift, item.split);
         else if (kVar)
-          tma_store_4d(tmO, stage, 64 * bx, bh << shift, static_cast<int32_t>(item.q_row0) + box_row0, 0);
+          tma_store_4d_hint(tmO, stage, 64 * bx, bh << shift,
+                            static_cast<int32_t>(item.q_row0) + box_row0, 0,
+                            l2_policy_evict_first());
         else if (split)
           tma_store_4d(tmOp, stage, 32 * bx, box_row0, h, item.split * static_cast<int32_t>(p.B) + b);
-        else if (p.layout == 0)
-          tma_store_4d(tmO, stage, 64 * bx, box_row0, h, b);
+        else if (p.layout == 0)  // output tiles are written once: evict-first in L2
+          tma_store_4d_hint(tmO, stage, 64 * bx, box_row0, h, b, l2_policy_evict_first());
         else
-          tma_store_4d(tmO, stage, 64 * bx, h, box_row0, b);
+          tma_store_4d_hint(tmO, stage, 64 * bx, h, box_row0, b, l2_policy_evict_first());
         bulk_commit_group();
       }
     }
