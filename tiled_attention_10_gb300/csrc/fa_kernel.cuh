@@ -1282,6 +1282,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{p.wait_limit_ns, p.err, abort_flag};
+  // The grid is launched with programmatic stream serialization, so it may
+  // start (on SMs the kernel before it leaves idle) while that kernel still
+  // runs: nothing below touches global memory before that kernel has
+  // completed and its writes are visible.  And the kernel after it -- the
+  // next call, or the split merge -- may start its own prologue now, on SMs
+  // this grid leaves idle (its own wait guards its memory accesses).  For
+  // small problems that hides the launch and prologue of consecutive calls.
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp < kProducerWarp) {
     reg_alloc_inc<RegSplit<kMode != kModeDense>::kSoftmax>();
@@ -1295,8 +1304,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncwarp();
-  // This CTA's work is issued: a dependent grid (the split merge) may start.
-  if (threadIdx.x == 0) griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -1330,6 +1337,11 @@ cudaError_t launch_fa_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, op, p);
 }
 
