@@ -17,9 +17,8 @@
  *   warps 10-11 idle
  * The launch gives every thread 168 registers (three warps share each SM
  * sub-partition's register file); the control warpgroup then hands registers
- * to the softmax warpgroups with setmaxnreg (72 / 216; 104 / 200 for the
- * split-KV kernel), so that a softmax thread can hold its whole 128-column
- * score row in registers.
+ * to the softmax warpgroups with setmaxnreg (104 / 200), so that a softmax
+ * thread can hold its whole 128-column score row in registers.
  *
  * Tensor memory (512 columns x 128 lanes, fp32):
  *   [0,128)   S for tile 0   (P for tile 0 overwrites its first columns)
@@ -65,8 +64,8 @@ constexpr int kBN = 128;  // key/value rows per tile
 constexpr int kThreads = 384;
 // Registers per thread after setmaxnreg: softmax warpgroups / control
 // warpgroup; 256 * softmax + 128 * control = 384 * 168 (the launch budget).
-// The split-KV, varlen and paged kernels' control roles decode more per item
-// and need more.
+// 200 hold a softmax thread's 128-score row; the control roles (item
+// decoding, ring bookkeeping, the issuing thread's barrier probes) need ~100.
 // Kernel modes: the whole pass over dense [B,H,S,D] tensors, the split-KV
 // pass (partials in a workspace), packed variable-length sequences, and
 // packed queries against a paged K/V cache.
@@ -74,10 +73,9 @@ constexpr int kModeDense = 0, kModeSplit = 1, kModeVarlen = 2, kModePaged = 3;
 // Paged K/V with each unit's keys split into n_splits chunks (fp32 partials,
 // merged by the combine kernel): the partition-and-reduce of paged decoding.
 constexpr int kModePagedSplit = 4;
-template <bool kWide>
 struct RegSplit {
-  static constexpr uint32_t kSoftmax = kWide ? 200 : 216;
-  static constexpr uint32_t kControl = kWide ? 104 : 72;
+  static constexpr uint32_t kSoftmax = 200;
+  static constexpr uint32_t kControl = 104;
   static_assert(256 * kSoftmax + 128 * kControl == 384 * 168, "register budget");
 };
 constexpr int kProducerWarp = 8;
@@ -785,13 +783,20 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
         }
       }
       if (!ok) break;
-      umma_commit(bars.empty(slotV));
+      // V_j's and K_{j+1}'s slots go back to the producer once every product
+      // that reads them has completed.  When tile 1 issued S_1(j+1) above,
+      // the commit that signals it covers all of them, and tile 1's softmax
+      // warps, which wait for that signal anyway, hand the slots back (two
+      // commits fewer for this thread, which sets the pace); otherwise this
+      // thread commits them.
+      const bool released_by_softmax = j + 1 < n[1];
+      if (!released_by_softmax) umma_commit(bars.empty(slotV));
       if (has_next) {
         // Every tile that uses K_{j+1} has issued its S by now (a tile with
         // n_t = j + 1 never does), but K_{j+1} may still be unread if no tile
         // needed it: wait for it before handing its slot back.
         if (!k_ready && !(done & 8u) && !mbar_wait(bars.full(slotKn), phK, wc)) { ok = false; break; }
-        umma_commit(bars.empty(slotKn));
+        if (!released_by_softmax) umma_commit(bars.empty(slotKn));
         if (j + 2 == nmax) umma_commit(bars.q_empty());
       }
       slotK = slotKn;
@@ -1002,6 +1007,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
   sl2 = fmaxf(sl2, 1e-30f);
 
   uint32_t s_phase = 0u, o_phase = 0u, solo_phase = 0u;
+  uint32_t ring_pos = 0u;   // K/V ring positions consumed by earlier items
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0;; ++w) {
     const int u = unit_of_round(w, grid, bid);
@@ -1012,6 +1018,15 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     const int q_tile = item.solo ? item.qt : 2 * item.pair + t;
     const int n = t ? item.n[1] : item.n[0];
     const int blk0 = t ? item.b[1] : item.b[0];  // this slot's first key block
+    // Ring position of this item's first K tile; the item's tiles occupy the
+    // next 2 * max(n0, n1) positions (K_0, V_0, K_1, V_1, ...), a solo item's
+    // 2 * (n0 + n1).
+    const uint32_t ring_base = ring_pos;
+    ring_pos += item.solo ? 2u * static_cast<uint32_t>(item.n[0] + item.n[1])
+                          : 2u * static_cast<uint32_t>(max(item.n[0], item.n[1]));
+    // Tile 1 hands back the ring slots of V_{j-1} and K_j once S_1(j) is
+    // ready (see mma_role): one thread of the warpgroup.
+    const bool releaser = t == 1 && !item.solo && threadIdx.x == 128;
     // Tile rows are tokens (dense, split: 128 of one head); varlen / paged
     // with GQA packing: 2^shift heads of each of 128 >> shift tokens.
     const int shift = kVar ? p.q_pack_log2 : 0;
@@ -1045,6 +1060,10 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait(bars.s_full(t), s_phase, wc)) { ok = false; break; }
       s_phase ^= 1u;
+      if (releaser && j > 0) {
+        mbar_arrive(bars.empty((ring_base + 2u * j - 1u) % C::kSlots));
+        mbar_arrive(bars.empty((ring_base + 2u * j) % C::kSlots));
+      }
       tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
@@ -1293,10 +1312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp < kProducerWarp) {
-    reg_alloc_inc<RegSplit<kMode != kModeDense>::kSoftmax>();
+    reg_alloc_inc<RegSplit::kSoftmax>();
     softmax_role<D, DT, kMode>(p, &tmO, &tmOp, tmem, sEpi, warp, lane, bars, wc);
   } else {
-    reg_alloc_dec<RegSplit<kMode != kModeDense>::kControl>();
+    reg_alloc_dec<RegSplit::kControl>();
     if (warp == kProducerWarp) {
       if (lane == 0) producer_role<D, DT, kMode>(p, &tmQ, &tmK, &tmV, sQ, sRing, bars, wc);
     } else if (warp == kMmaWarp) {
