@@ -99,3 +99,57 @@ def test_calls_from_a_thread_that_never_touched_the_device(cuda_lib):
     torch.cuda.synchronize()
     assert res["st"] == 0
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_dependent_calls_back_to_back(split, cuda_lib):
+    """Consecutive calls on one stream may overlap their launch and prologue
+    (programmatic stream serialization): a call must read the previous
+    call's output, and must not overwrite what the previous call still
+    reads.  A chain of three calls, no synchronisation in between, on a
+    shape small enough to leave most SMs idle:
+      1. O1 = attn(Q, K, V)
+      2. O2 = attn(O1, K, V)          reads O1 written by call 1
+      3. attn(K2, K, V) written into Q's buffer, which call 1 read
+    then O1 and O2 are checked against the oracle on the original inputs."""
+    w = Workload("t", 1, 8, 512, 512, 64, "bf16", "BNSD", False, seed=31)
+    x = make_inputs(w, device="cuda")
+    q, k, v = x.q.clone(), x.k, x.v
+    q_host = q.cpu()
+    k2 = make_inputs(Workload("t2", 1, 8, 512, 512, 64, "bf16", "BNSD", False, seed=32),
+                     device="cuda").q
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    l1 = torch.empty(1, 8, 512, device="cuda")
+    l2, l3 = torch.empty_like(l1), torch.empty_like(l1)
+    stream = torch.cuda.current_stream().cuda_stream
+    ws = torch.empty(1 << 22, dtype=torch.uint8, device="cuda")
+
+    def call(qq, oo, ll):
+        if split:
+            st = binding.fa_fwd_splitkv(qq.data_ptr(), k.data_ptr(), v.data_ptr(), oo.data_ptr(),
+                                        ll.data_ptr(), 1, 8, 8, 512, 512, 64, w.softmax_scale,
+                                        "BNSD", 0, "bf16", None, None, None, 2, ws.data_ptr(),
+                                        ws.numel(), stream)
+        else:
+            st = binding.fa_fwd(qq.data_ptr(), k.data_ptr(), v.data_ptr(), oo.data_ptr(),
+                                ll.data_ptr(), 1, 8, 512, 512, 64, w.softmax_scale, "BNSD", 0,
+                                "bf16", None, None, None, stream)
+        assert st == 0, binding.FA_STATUS.get(st)
+
+    for _ in range(3):
+        call(q, o1, l1)
+        call(o1, o2, l2)
+        call(k2, q, l3)
+        torch.cuda.synchronize()
+        assert binding.fa_last_device_error(stream) == 0
+        O1, L1 = oracle.attention_full(q_host, x.k, x.v, dtype="bf16", layout="BNSD", B=1, H=8,
+                                       S_q=512, S_kv=512, D=64, scale=w.softmax_scale,
+                                       causal=False)
+        assert float(np.abs(o1.float().cpu().double().numpy() - O1).max()) <= 1.6e-2
+        assert float(np.abs(l1.cpu().double().numpy() - L1).max()) <= 1e-3
+        O2, L2 = oracle.attention_full(o1.cpu(), x.k, x.v, dtype="bf16", layout="BNSD", B=1, H=8,
+                                       S_q=512, S_kv=512, D=64, scale=w.softmax_scale,
+                                       causal=False)
+        assert float(np.abs(o2.float().cpu().double().numpy() - O2).max()) <= 1.6e-2
+        assert float(np.abs(l2.cpu().double().numpy() - L2).max()) <= 1e-3
+        q.copy_(q_host.to("cuda"))   # restore Q for the next round
