@@ -149,6 +149,33 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// The last few tensor maps this thread encoded, by their arguments: a caller
+// that runs the same shapes on the same buffers call after call (a training
+// or decode loop) skips the encoding.  A map holds only the address, sizes
+// and strides, so it stays valid for whatever the buffer holds.
+struct MapKey {
+  const void* ptr;
+  int64_t B, H, S, D;
+  int32_t dtype, layout;
+  uint32_t box_rows, box_heads;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && B == o.B && H == o.H && S == o.S && D == o.D && dtype == o.dtype &&
+           layout == o.layout && box_rows == o.box_rows && box_heads == o.box_heads;
+  }
+};
+constexpr int kMapCache = 8;
+struct MapCache {
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
+  bool used[kMapCache] = {};
+  int next = 0;
+};
+thread_local MapCache t_maps;
+
+bool make_map_encode(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, fa_layout_t layout,
+                     int64_t B, int64_t H, int64_t S, int64_t D, cuuint32_t box_rows,
+                     cuuint32_t box_heads);
+
 // 4-D tensor map over a [B,H,S,D] (BNSD) or [B,S,H,D] (BSND) tensor, boxes
 // of 128 rows x 128 bytes, 128-byte swizzle, zero fill out of bounds.  The
 // sequence dimension is its own map dimension, so rows >= S are never read
@@ -156,6 +183,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool make_map(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, fa_layout_t layout, int64_t B,
               int64_t H, int64_t S, int64_t D, cuuint32_t box_rows = 128,
               cuuint32_t box_heads = 1) {
+  const MapKey key{ptr, B, H, S, D, static_cast<int32_t>(dtype), static_cast<int32_t>(layout),
+                   box_rows, box_heads};
+  MapCache& c = t_maps;
+  for (int i = 0; i < kMapCache; ++i) {
+    if (c.used[i] && c.key[i] == key) {
+      *m = c.map[i];
+      return true;
+    }
+  }
+  if (!make_map_encode(m, ptr, dtype, layout, B, H, S, D, box_rows, box_heads)) return false;
+  c.key[c.next] = key;
+  c.map[c.next] = *m;
+  c.used[c.next] = true;
+  c.next = (c.next + 1) % kMapCache;
+  return true;
+}
+
+bool make_map_encode(CUtensorMap* m, const void* ptr, fa_dtype_t dtype, fa_layout_t layout,
+                     int64_t B, int64_t H, int64_t S, int64_t D, cuuint32_t box_rows,
+                     cuuint32_t box_heads) {
   auto enc = encode_fn();
   if (!enc) return false;
   const uint64_t eb = (dtype == FA_DTYPE_FP8E4M3) ? 1 : 2;
