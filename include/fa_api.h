@@ -89,6 +89,10 @@ typedef enum {
  * Returns FA_OK once the kernel is enqueued; FA_ERR_CUDA if a CUDA call or
  * the launch fails.  A bounded device-side wait that expires sets the
  * library's device error word; fa_last_device_error() reports it.
+ * Stream order holds as for any launch.  The forward kernels are launched
+ * with programmatic stream serialization: one may start its prologue on idle
+ * SMs while the kernel before it on the stream still runs, but reads and
+ * writes no global memory until that kernel has completed.
  */
 fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                    int64_t B, int64_t H, int64_t S_q, int64_t S_kv, int64_t D, float scale,

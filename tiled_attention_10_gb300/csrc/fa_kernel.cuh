@@ -826,7 +826,7 @@ __device__ __forceinline__ void ld_shared_f2(uint32_t addr, float& a, float& b) 
 
 // One K/V block of the softmax for one query row (the thread's TMEM lane):
 // row max, running-max update with conditional O rescale, P = 2^(s*sl2 - m)
-// in two signalled halves, row sum.  Instantiated twice -- with and without
+// in two halves (16-bit P signalled once, e4m3 P half by half), row sum.  Instantiated twice -- with and without
 // the tail/causal mask -- so the unmasked copy, which almost every block
 // runs, is one contiguous straight-line body.
 template <int D, int DT, bool kMasked>
