@@ -13,7 +13,8 @@
  *   warps 0-3  softmax for query tile 0 (one query row per thread, TMEM lanes)
  *   warps 4-7  softmax for query tile 1
  *   warp  8    TMA producer: Q tiles, then K_j, V_j through an NS-slot ring
- *   warp  9    TMEM owner and tcgen05.mma issuer (one thread)
+ *   warp  9    TMEM owner and tcgen05.mma issuer (the whole warp runs the role;
+ *              one elected lane issues the products and commits)
  *   warps 10-11 idle
  * The launch gives every thread 168 registers (three warps share each SM
  * sub-partition's register file); the control warpgroup then hands registers
@@ -510,13 +511,13 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one thread).
+// MMA issuer (one warp; one elected lane issues).
 // ---------------------------------------------------------------------------
 // S_t = Q_t K^T: K = D in kQKSteps instructions, 32 bytes of K each (inside
 // a 128-byte swizzle chunk, then the next 16 KB chunk).  qlo / klo are the low
 // descriptor words of the Q tile and the K slot.
 template <int D, int DT>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t qlo, uint32_t klo) {
+__device__ __forceinline__ void issue_qk(bool leader, uint32_t d_tmem, uint32_t qlo, uint32_t klo) {
   using C = Cfg<D, DT>;
   constexpr uint32_t hi = umma_desc_hi_sw128(1024);
 #pragma unroll
@@ -524,7 +525,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t qlo, uint32_t
     constexpr int kStepBytes = 32;
     const uint32_t off = static_cast<uint32_t>(((kk * kStepBytes / 128) * C::kChunkBytes +
                                                 (kk * kStepBytes) % 128) >> 4);
-    umma_ss_w<C::kFp8>(d_tmem, qlo + off, hi, klo + off, hi, C::kIdescQK, kk > 0 ? 1u : 0u);
+    if (leader) umma_ss_w<C::kFp8>(d_tmem, qlo + off, hi, klo + off, hi, C::kIdescQK, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -532,16 +533,17 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t qlo, uint32_t
 // TMEM (kUK elements of K = 8 columns per step), B = V rows [kk*kUK, +kUK),
 // MN-major (128-byte rows; LBO = next column chunk).
 template <int D, int DT, int H>
-__device__ __forceinline__ void issue_pv_half(uint32_t o_tmem, uint32_t p_tmem, uint32_t vlo,
-                                              uint32_t accumulate) {
+__device__ __forceinline__ void issue_pv_half(bool leader, uint32_t o_tmem, uint32_t p_tmem,
+                                              uint32_t vlo, uint32_t accumulate) {
   using C = Cfg<D, DT>;
   constexpr uint32_t hi = umma_desc_hi_sw128(1024);
   constexpr int kHalf = C::kPVSteps / 2;
 #pragma unroll
   for (int kk = H * kHalf; kk < (H + 1) * kHalf; ++kk) {
     const uint32_t off = static_cast<uint32_t>((kk * C::kUK * 128) >> 4);
-    umma_ts_w<C::kFp8>(o_tmem, p_tmem + kk * 8, vlo + off, hi, C::kIdescPV,
-                       kk > 0 ? 1u : accumulate);
+    if (leader)
+      umma_ts_w<C::kFp8>(o_tmem, p_tmem + kk * 8, vlo + off, hi, C::kIdescPV,
+                         kk > 0 ? 1u : accumulate);
   }
 }
 
@@ -563,14 +565,15 @@ __device__ __forceinline__ bool refine_tile(const KernelParams& p, const Item& i
 // e4m3: O_t += P_lo V, P_lo = the residual of P's rounding that the softmax
 // writes in the 32 columns after P for a tile refine_tile selects.
 template <int D, int DT>
-__device__ __forceinline__ void issue_pv_residual(uint32_t o_tmem, uint32_t p_tmem, uint32_t vlo) {
+__device__ __forceinline__ void issue_pv_residual(bool leader, uint32_t o_tmem, uint32_t p_tmem,
+                                                  uint32_t vlo) {
   using C = Cfg<D, DT>;
   if constexpr (C::kFp8) {
     constexpr uint32_t hi = umma_desc_hi_sw128(1024);
 #pragma unroll
     for (int kk = 0; kk < C::kPVSteps; ++kk) {
       const uint32_t off = static_cast<uint32_t>((kk * C::kUK * 128) >> 4);
-      umma_ts_w<true>(o_tmem, p_tmem + 32 + kk * 8, vlo + off, hi, C::kIdescPV, 1u);
+      if (leader) umma_ts_w<true>(o_tmem, p_tmem + 32 + kk * 8, vlo + off, hi, C::kIdescPV, 1u);
     }
   }
 }
@@ -592,8 +595,8 @@ struct RingPos {
 // Q tile (slot 0's buffer), slot t over its own key blocks, in the ring
 // order the producer loads them.  Returns false if a wait gave up.
 template <int D, int DT>
-__device__ bool mma_solo_unit(const Item& item, RingPos& rp, uint32_t (&p_phase)[2], uint32_t q_lo,
-                              uint32_t k_lo0, uint32_t v_lo0, const uint32_t (&tS)[2],
+__device__ bool mma_solo_unit(bool leader, const Item& item, RingPos& rp, uint32_t (&p_phase)[2],
+                              uint32_t q_lo, uint32_t k_lo0, uint32_t v_lo0, const uint32_t (&tS)[2],
                               const uint32_t (&tO)[2], const bool (&rf)[2], const Bars& bars,
                               const WaitCtl& wc) {
   using C = Cfg<D, DT>;
@@ -610,15 +613,15 @@ __device__ bool mma_solo_unit(const Item& item, RingPos& rp, uint32_t (&p_phase)
   if (!mbar_wait(bars.full(k[0].slot), k[0].phase, wc)) return false;
   if (n[1] > 0 && !mbar_wait(bars.full(k[1].slot), k[1].phase, wc)) return false;
   tc_fence_after();
-  issue_qk<D, DT>(tS[0], q_lo, k_lo0 + k[0].slot * kTileW);
-  umma_commit(bars.s_full(0));
+  issue_qk<D, DT>(leader, tS[0], q_lo, k_lo0 + k[0].slot * kTileW);
+  umma_commit_if(leader, bars.s_full(0));
   if (n[1] > 0) {
-    issue_qk<D, DT>(tS[1], q_lo, k_lo0 + k[1].slot * kTileW);
-    umma_commit(bars.s_full(1));
-    umma_commit(bars.empty(k[1].slot));
+    issue_qk<D, DT>(leader, tS[1], q_lo, k_lo0 + k[1].slot * kTileW);
+    umma_commit_if(leader, bars.s_full(1));
+    umma_commit_if(leader, bars.empty(k[1].slot));
   }
-  umma_commit(bars.empty(k[0].slot));
-  if (n[0] == 1) umma_commit(bars.q_empty());
+  umma_commit_if(leader, bars.empty(k[0].slot));
+  if (n[0] == 1) umma_commit_if(leader, bars.q_empty());
   for (int j = 0; j < n[0]; ++j) {
     v[0] = rp;
     rp.advance<C::kSlots>();
@@ -641,28 +644,28 @@ __device__ bool mma_solo_unit(const Item& item, RingPos& rp, uint32_t (&p_phase)
       if (!mbar_wait(bars.p_half(t, C::kFp8 ? 0 : 1), p_phase[t], wc)) return false;
       if (!mbar_wait(bars.full(vt.slot), vt.phase, wc)) return false;
       tc_fence_after();
-      issue_pv_half<D, DT, 0>(tO[t], tS[t], v_lo0 + vt.slot * kTileW, j > 0 ? 1u : 0u);
+      issue_pv_half<D, DT, 0>(leader, tO[t], tS[t], v_lo0 + vt.slot * kTileW, j > 0 ? 1u : 0u);
       if constexpr (C::kFp8) {
         if (!mbar_wait(bars.p_half(t, 1), p_phase[t], wc)) return false;
         tc_fence_after();
       }
       p_phase[t] ^= 1u;
-      issue_pv_half<D, DT, 1>(tO[t], tS[t], v_lo0 + vt.slot * kTileW, 1u);
+      issue_pv_half<D, DT, 1>(leader, tO[t], tS[t], v_lo0 + vt.slot * kTileW, 1u);
       if (j + 1 < n[t]) {
         if (!mbar_wait(bars.full(kt.slot), kt.phase, wc)) return false;
         tc_fence_after();
-        issue_qk<D, DT>(tS[t], q_lo, k_lo0 + kt.slot * kTileW);
-        umma_commit(bars.s_full(t));
+        issue_qk<D, DT>(leader, tS[t], q_lo, k_lo0 + kt.slot * kTileW);
+        umma_commit_if(leader, bars.s_full(t));
       } else {
-        if (t ? rf[1] : rf[0]) issue_pv_residual<D, DT>(tO[t], tS[t], v_lo0 + vt.slot * kTileW);
-        umma_commit(bars.o_done(t));
+        if (t ? rf[1] : rf[0]) issue_pv_residual<D, DT>(leader, tO[t], tS[t], v_lo0 + vt.slot * kTileW);
+        umma_commit_if(leader, bars.o_done(t));
       }
     }
-    umma_commit(bars.empty(v[0].slot));
-    if (j < n[1]) umma_commit(bars.empty(v[1].slot));
-    if (j + 1 < n[0]) umma_commit(bars.empty(k[0].slot));
-    if (j + 1 < n[1]) umma_commit(bars.empty(k[1].slot));
-    if (j + 2 == n[0]) umma_commit(bars.q_empty());
+    umma_commit_if(leader, bars.empty(v[0].slot));
+    if (j < n[1]) umma_commit_if(leader, bars.empty(v[1].slot));
+    if (j + 1 < n[0]) umma_commit_if(leader, bars.empty(k[0].slot));
+    if (j + 1 < n[1]) umma_commit_if(leader, bars.empty(k[1].slot));
+    if (j + 2 == n[0]) umma_commit_if(leader, bars.q_empty());
   }
   return true;
 }
@@ -671,6 +674,10 @@ template <int D, int DT, int kMode>
 __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint32_t sRing,
                          const Bars& bars, const WaitCtl& wc) {
   using C = Cfg<D, DT>;
+  // The whole warp runs this role (its control flow is warp-uniform: every
+  // lane sees the same barrier states); one elected lane issues the products
+  // and commits.
+  const bool leader = elect_one();
   constexpr uint32_t kTileW = C::kTileBytes >> 4;  // one tile, in descriptor units
   const uint32_t q_lo[2] = {umma_desc_lo(sQ, 16), umma_desc_lo(sQ, 16) + kTileW};
   const uint32_t k_lo0 = umma_desc_lo(sRing, 16);               // K-major view of slot 0
@@ -697,7 +704,8 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
     if constexpr (kMode == kModeDense) {
       if (item.solo) {
         const bool rf[2] = {rf0, rf1};
-        if (!mma_solo_unit<D, DT>(item, rp, p_phase, q_lo[0], k_lo0, v_lo0, tS, tO, rf, bars, wc)) {
+        if (!mma_solo_unit<D, DT>(leader, item, rp, p_phase, q_lo[0], k_lo0, v_lo0, tS, tO, rf, bars,
+                                  wc)) {
           ok = false;
           break;
         }
@@ -711,11 +719,11 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
     tc_fence_after();
     for (int t = 0; t < 2; ++t) {
       if (n[t] == 0) continue;
-      issue_qk<D, DT>(tS[t], q_lo[t], k_lo0 + slotK * kTileW);
-      umma_commit(bars.s_full(t));
+      issue_qk<D, DT>(leader, tS[t], q_lo[t], k_lo0 + slotK * kTileW);
+      umma_commit_if(leader, bars.s_full(t));
     }
-    umma_commit(bars.empty(slotK));
-    if (nmax == 1) umma_commit(bars.q_empty());
+    umma_commit_if(leader, bars.empty(slotK));
+    if (nmax == 1) umma_commit_if(leader, bars.q_empty());
     for (int j = 0; j < nmax; ++j) {
       const int slotV = rp.slot;
       const uint32_t phV = rp.phase;
@@ -762,24 +770,24 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
           v_ready = true;
         }
         tc_fence_after();
-        issue_pv_half<D, DT, 0>(tO[t], tS[t], v_lo0 + slotV * kTileW, j > 0 ? 1u : 0u);
+        issue_pv_half<D, DT, 0>(leader, tO[t], tS[t], v_lo0 + slotV * kTileW, j > 0 ? 1u : 0u);
         if constexpr (C::kFp8) {
           if (!mbar_wait(bars.p_half(t, 1), p_phase[t], wc)) { ok = false; break; }
           tc_fence_after();
         }
         p_phase[t] ^= 1u;
-        issue_pv_half<D, DT, 1>(tO[t], tS[t], v_lo0 + slotV * kTileW, 1u);
+        issue_pv_half<D, DT, 1>(leader, tO[t], tS[t], v_lo0 + slotV * kTileW, 1u);
         if (j + 1 < n[t]) {
           if (!k_ready) {
             if (!(done & 8u) && !mbar_wait(bars.full(slotKn), phK, wc)) { ok = false; break; }
             k_ready = true;
             tc_fence_after();
           }
-          issue_qk<D, DT>(tS[t], q_lo[t], k_lo0 + slotKn * kTileW);
-          umma_commit(bars.s_full(t));
+          issue_qk<D, DT>(leader, tS[t], q_lo[t], k_lo0 + slotKn * kTileW);
+          umma_commit_if(leader, bars.s_full(t));
         } else {
-          if (t ? rf1 : rf0) issue_pv_residual<D, DT>(tO[t], tS[t], v_lo0 + slotV * kTileW);
-          umma_commit(bars.o_done(t));
+          if (t ? rf1 : rf0) issue_pv_residual<D, DT>(leader, tO[t], tS[t], v_lo0 + slotV * kTileW);
+          umma_commit_if(leader, bars.o_done(t));
         }
       }
       if (!ok) break;
@@ -790,20 +798,20 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
       // commits fewer for this thread, which sets the pace); otherwise this
       // thread commits them.
       const bool released_by_softmax = j + 1 < n[1];
-      if (!released_by_softmax) umma_commit(bars.empty(slotV));
+      if (!released_by_softmax) umma_commit_if(leader, bars.empty(slotV));
       if (has_next) {
         // Every tile that uses K_{j+1} has issued its S by now (a tile with
         // n_t = j + 1 never does), but K_{j+1} may still be unread if no tile
         // needed it: wait for it before handing its slot back.
         if (!k_ready && !(done & 8u) && !mbar_wait(bars.full(slotKn), phK, wc)) { ok = false; break; }
-        if (!released_by_softmax) umma_commit(bars.empty(slotKn));
-        if (j + 2 == nmax) umma_commit(bars.q_empty());
+        if (!released_by_softmax) umma_commit_if(leader, bars.empty(slotKn));
+        if (j + 2 == nmax) umma_commit_if(leader, bars.q_empty());
       }
       slotK = slotKn;
     }
   }
   // Drain: every MMA issued above completes before TMEM is released.
-  umma_commit(bars.drain());
+  umma_commit_if(leader, bars.drain());
   mbar_wait_teardown(bars.drain(), 0u, ok ? 2000000000ull : 20000000ull);
 }
 
@@ -1319,7 +1327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
       if (lane == 0) producer_role<D, DT, kMode>(p, &tmQ, &tmK, &tmV, sQ, sRing, bars, wc);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) mma_role<D, DT, kMode>(p, tmem, sQ, sRing, bars, wc);
+      mma_role<D, DT, kMode>(p, tmem, sQ, sRing, bars, wc);
     }
   }
   __syncwarp();

@@ -308,6 +308,25 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
       : "memory");
 }
 
+// The same, issued by the one lane `leader` selects (see elect_one).
+__device__ __forceinline__ void umma_commit_if(bool leader, uint32_t bar) {
+  if (leader) umma_commit(bar);
+}
+
+// One lane of the (fully active) warp: true in exactly one lane.  An issuing
+// role run by the whole warp predicates its tcgen05 issue on this; measured
+// on sm_103a, an issue so predicated costs about half as many cycles, when
+// other warps keep the sub-partition busy, as the same issue from a branch
+// taken by lane 0 alone (255-294 against 595-633 cycles a product beside
+// eight FFMA-bound warps; both ~64 on a quiet SM).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------------------
 // UMMA shared-memory matrix descriptor (64 bits):
 //   [0,14)  start address >> 4        [16,30) leading-dim byte offset >> 4
