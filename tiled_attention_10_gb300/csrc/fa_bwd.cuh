@@ -30,8 +30,9 @@
  * dK/dV kernel already fills all 512 TMEM columns (S^T, dP^T, dV, dK).
  *
  * Warp roles (320 threads): warps 0-7 compute P / dS (warp w serves TMEM lane
- * quarter w % 4 and column half w / 4), warp 8 is the TMA producer, warp 9
- * issues the MMAs (one thread).  Every wait is bounded (see fa_ptx.cuh).
+ * quarter w % 4 and column half w / 4), warp 8 is the TMA producer and warp 9
+ * issues the MMAs (each role run by its whole warp, one elected lane issuing).
+ * Every wait is bounded (see fa_ptx.cuh).
  */
 #pragma once
 #include <cuda.h>
@@ -335,6 +336,8 @@ __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
                             const DqBars& bars, const WaitCtl& wc) {
   using C = DqCfg<D>;
   using T = Tile<D>;
+  // The whole warp runs this role; one elected lane issues (see elect_one).
+  const bool leader = elect_one();
   Ring<C::kKSlots> kr;
   Ring<C::kVSlots> vr;
   uint32_t k_issued = 0, v_issued = 0, it = 0;
@@ -349,8 +352,8 @@ __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
     const int32_t hk = h / p.kv_group;
     const int n = dq_kv_blocks(p, i);
     if (!mbar_wait(bars.q_empty(), (it & 1u) ^ 1u, wc)) { ok = false; break; }
-    mbar_arrive_expect_tx(bars.q_full(), 2 * T::kBytes);
-    for (int c = 0; c < T::kChunks; ++c) {
+    if (leader) mbar_arrive_expect_tx(bars.q_full(), 2 * T::kBytes);
+    for (int c = 0; c < T::kChunks && leader; ++c) {
       tma_tile(smem + C::kQOff + c * T::kChunkBytes, tmQ, bars.q_full(), p.layout, c * 64, i * 128,
                h, b);
       tma_tile(smem + C::kDOOff + c * T::kChunkBytes, tmDO, bars.q_full(), p.layout, c * 64,
@@ -359,15 +362,15 @@ __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
     ++it;
     for (int j = 0; j < n && ok; ++j) {
       if (!mbar_wait(bars.kempty(kr.slot), kr.phase ^ 1u, wc)) { ok = false; break; }
-      mbar_arrive_expect_tx(bars.kfull(kr.slot), T::kBytes);
-      for (int c = 0; c < T::kChunks; ++c)
+      if (leader) mbar_arrive_expect_tx(bars.kfull(kr.slot), T::kBytes);
+      for (int c = 0; c < T::kChunks && leader; ++c)
         tma_tile(smem + C::kKOff + kr.slot * T::kBytes + c * T::kChunkBytes, tmK,
                  bars.kfull(kr.slot), p.layout, c * 64, j * 128, hk, b);
       kr.advance();
       ++k_issued;
       if (!mbar_wait(bars.vempty(vr.slot), vr.phase ^ 1u, wc)) { ok = false; break; }
-      mbar_arrive_expect_tx(bars.vfull(vr.slot), T::kBytes);
-      for (int c = 0; c < T::kChunks; ++c)
+      if (leader) mbar_arrive_expect_tx(bars.vfull(vr.slot), T::kBytes);
+      for (int c = 0; c < T::kChunks && leader; ++c)
         tma_tile(smem + C::kVOff + vr.slot * T::kBytes + c * T::kChunkBytes, tmV,
                  bars.vfull(vr.slot), p.layout, c * 64, j * 128, hk, b);
       vr.advance();
@@ -388,7 +391,7 @@ __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
 
 // K-major x K-major product over the head dim: D[128 x 128] = A[128 x D] B[128 x D]^T.
 template <int D, int DT>
-__device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo) {
+__device__ __forceinline__ void issue_ss(bool leader, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo) {
   using T = Tile<D>;
   constexpr uint32_t hi = umma_desc_hi_sw128(1024);
   constexpr uint32_t idesc = umma_idesc(DT == kBF16 ? 1u : 0u, false, 128, 128);
@@ -396,7 +399,7 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a_lo, uint32_
   for (int kk = 0; kk < T::kDSteps; ++kk) {
     const uint32_t off =
         static_cast<uint32_t>(((kk * 32 / 128) * T::kChunkBytes + (kk * 32) % 128) >> 4);
-    umma_ss_w<false>(d_tmem, a_lo + off, hi, b_lo + off, hi, idesc, kk > 0 ? 1u : 0u);
+    if (leader) umma_ss_w<false>(d_tmem, a_lo + off, hi, b_lo + off, hi, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -404,8 +407,8 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint32_t a_lo, uint32_
 // along K, MN-major).  A's K step kk (16 elements = 8 columns) sits at
 // column a_col(kk).
 template <int D, int DT, bool kSplitHalves>
-__device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
-                                         uint32_t accumulate) {
+__device__ __forceinline__ void issue_ts(bool leader, uint32_t d_tmem, uint32_t a_tmem,
+                                         uint32_t b_lo, uint32_t accumulate) {
   constexpr uint32_t hi = umma_desc_hi_sw128(1024);
   constexpr uint32_t idesc = umma_idesc(DT == kBF16 ? 1u : 0u, true, 128, D);
 #pragma unroll
@@ -413,13 +416,16 @@ __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint3
     const uint32_t acol = kSplitHalves ? static_cast<uint32_t>(64 * (kk / 4) + 8 * (kk % 4))
                                        : static_cast<uint32_t>(8 * kk);
     const uint32_t off = static_cast<uint32_t>((kk * 16 * 128) >> 4);
-    umma_ts_w<false>(d_tmem, a_tmem + acol, b_lo + off, hi, idesc, kk > 0 ? 1u : accumulate);
+    if (leader)
+      umma_ts_w<false>(d_tmem, a_tmem + acol, b_lo + off, hi, idesc, kk > 0 ? 1u : accumulate);
   }
 }
 
 template <int D, int DT>
 __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const DqBars& bars,
                        const WaitCtl& wc) {
+  // The whole warp runs this role; one elected lane issues (see elect_one).
+  const bool leader = elect_one();
   using C = DqCfg<D>;
   using T = Tile<D>;
   constexpr uint32_t kTileW = T::kBytes >> 4;
@@ -448,8 +454,8 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
     kr.advance();
     if (s_issued > 0 && !mbar_wait(bars.s_free(), (s_issued - 1) & 1u, wc)) { ok = false; break; }
     tc_fence_after();
-    issue_ss<D, DT>(tS, q_lo, k_kmaj0 + slotK * kTileW);
-    umma_commit(bars.s_full());
+    issue_ss<D, DT>(leader, tS, q_lo, k_kmaj0 + slotK * kTileW);
+    umma_commit_if(leader, bars.s_full());
     ++s_issued;
     // dP_0 = dO V_0^T.
     {
@@ -457,9 +463,9 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
       if (!mbar_wait(bars.vfull(slotV), vr.phase, wc)) { ok = false; break; }
       vr.advance();
       tc_fence_after();
-      issue_ss<D, DT>(tDP, do_lo, v_kmaj0 + slotV * kTileW);
-      umma_commit(bars.dp_full());
-      umma_commit(bars.vempty(slotV));
+      issue_ss<D, DT>(leader, tDP, do_lo, v_kmaj0 + slotV * kTileW);
+      umma_commit_if(leader, bars.dp_full());
+      umma_commit_if(leader, bars.vempty(slotV));
     }
     for (int j = 0; j < n; ++j) {
       const bool has_next = j + 1 < n;
@@ -477,8 +483,8 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
         kr.advance();
         if (!(done & 2u) && !mbar_wait(bars.s_free(), (s_issued - 1) & 1u, wc)) { ok = false; break; }
         tc_fence_after();
-        issue_ss<D, DT>(tS, q_lo, k_kmaj0 + slotKn * kTileW);
-        umma_commit(bars.s_full());
+        issue_ss<D, DT>(leader, tS, q_lo, k_kmaj0 + slotKn * kTileW);
+        umma_commit_if(leader, bars.s_full());
         ++s_issued;
       }
       // dQ (+)= dS_j K_j once dS_j is in TMEM; the first product of a unit
@@ -487,25 +493,25 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
       ds_ph ^= 1u;
       if (j == 0 && units > 0 && !mbar_wait(bars.dq_free(), (units - 1) & 1u, wc)) { ok = false; break; }
       tc_fence_after();
-      issue_ts<D, DT, false>(tDQ, tDS, k_mn0 + slotK * kTileW, j > 0 ? 1u : 0u);
-      umma_commit(bars.kempty(slotK));
+      issue_ts<D, DT, false>(leader, tDQ, tDS, k_mn0 + slotK * kTileW, j > 0 ? 1u : 0u);
+      umma_commit_if(leader, bars.kempty(slotK));
       if (has_next) {
         const int slotV = vr.slot;
         if (!(done & 8u) && !mbar_wait(bars.vfull(slotV), vr.phase, wc)) { ok = false; break; }
         vr.advance();
         tc_fence_after();
-        issue_ss<D, DT>(tDP, do_lo, v_kmaj0 + slotV * kTileW);
-        umma_commit(bars.dp_full());
-        umma_commit(bars.vempty(slotV));
+        issue_ss<D, DT>(leader, tDP, do_lo, v_kmaj0 + slotV * kTileW);
+        umma_commit_if(leader, bars.dp_full());
+        umma_commit_if(leader, bars.vempty(slotV));
       }
       slotK = slotKn;
     }
     if (!ok) break;
-    umma_commit(bars.dq_done());
-    umma_commit(bars.q_empty());
+    umma_commit_if(leader, bars.dq_done());
+    umma_commit_if(leader, bars.q_empty());
     ++units;
   }
-  umma_commit(bars.drain());
+  umma_commit_if(leader, bars.drain());
   mbar_wait_teardown(bars.drain(), 0u, ok ? 2000000000ull : 20000000ull);
 }
 
@@ -680,9 +686,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kProducerWarp) {
     dq_softmax<D, DT>(p, dq_out, tmem, warp, lane, bars, wc);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) dq_producer<D>(p, &tmQ, &tmK, &tmV, &tmDO, base, bars, wc);
+    dq_producer<D>(p, &tmQ, &tmK, &tmV, &tmDO, base, bars, wc);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) dq_mma<D, DT>(p, tmem, base, bars, wc);
+    dq_mma<D, DT>(p, tmem, base, bars, wc);
   }
   __syncwarp();
   tc_fence_before();
@@ -767,6 +773,8 @@ __device__ void kv_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
                             const KvBars& bars, const WaitCtl& wc) {
   using C = KvCfg<D>;
   using T = Tile<D>;
+  // The whole warp runs this role; one elected lane issues (see elect_one).
+  const bool leader = elect_one();
   Ring<C::kStages> ring;
   uint32_t issued = 0, units = 0, kv_loads = 0;
   bool ok = true;
@@ -779,8 +787,8 @@ __device__ void kv_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
     if (units > 0 && !mbar_wait(bars.epi_done(), (units - 1) & 1u, wc)) { ok = false; break; }
     ++units;
     if (k.n_steps == 0) continue;
-    mbar_arrive_expect_tx(bars.kv_full(), 2 * T::kBytes);
-    for (int c = 0; c < T::kChunks; ++c) {
+    if (leader) mbar_arrive_expect_tx(bars.kv_full(), 2 * T::kBytes);
+    for (int c = 0; c < T::kChunks && leader; ++c) {
       tma_tile(smem + C::kKOff + c * T::kChunkBytes, tmK, bars.kv_full(), p.layout, c * 64,
                k.j * 128, k.hk, k.b);
       tma_tile(smem + C::kVOff + c * T::kChunkBytes, tmV, bars.kv_full(), p.layout, c * 64,
@@ -794,15 +802,17 @@ __device__ void kv_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
       if (!mbar_wait(bars.empty(ring.slot), ring.phase ^ 1u, wc)) { ok = false; break; }
       const uint32_t st = smem + C::kRingOff + ring.slot * C::kStageBytes;
       const uint32_t bar = bars.full(ring.slot);
-      mbar_arrive_expect_tx(bar, 2 * T::kBytes + 1024);
-      for (int c = 0; c < T::kChunks; ++c) {
+      if (leader) mbar_arrive_expect_tx(bar, 2 * T::kBytes + 1024);
+      for (int c = 0; c < T::kChunks && leader; ++c) {
         tma_tile(st + c * T::kChunkBytes, tmQ, bar, p.layout, c * 64, i * 128, h, k.b);
         tma_tile(st + T::kBytes + c * T::kChunkBytes, tmDO, bar, p.layout, c * 64, i * 128, h,
                  k.b);
       }
       const int64_t row = (static_cast<int64_t>(k.b) * p.H + h) * p.S_q_pad + static_cast<int64_t>(i) * 128;
-      bulk_load_1d(st + 2 * T::kBytes, p.lse2 + row, 512, bar);
-      bulk_load_1d(st + 2 * T::kBytes + 512, p.dsum + row, 512, bar);
+      if (leader) {
+        bulk_load_1d(st + 2 * T::kBytes, p.lse2 + row, 512, bar);
+        bulk_load_1d(st + 2 * T::kBytes + 512, p.dsum + row, 512, bar);
+      }
       ring.advance();
       ++issued;
     }
@@ -818,6 +828,8 @@ __device__ void kv_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
 template <int D, int DT>
 __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const KvBars& bars,
                        const WaitCtl& wc) {
+  // The whole warp runs this role; one elected lane issues (see elect_one).
+  const bool leader = elect_one();
   using C = KvCfg<D>;
   using T = Tile<D>;
   constexpr uint32_t kStageW = C::kStageBytes >> 4;
@@ -836,7 +848,7 @@ __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const K
     if (u >= p.num_units) break;
     const KvUnit k = kv_decode(p, u);
     if (k.n_steps == 0) {
-      umma_commit(bars.dkv_done());  // nothing to accumulate: dK = dV = 0
+      umma_commit_if(leader, bars.dkv_done());  // nothing to accumulate: dK = dV = 0
       continue;
     }
     if (!mbar_wait(bars.kv_full(), kv_loads & 1u, wc)) { ok = false; break; }
@@ -845,10 +857,10 @@ __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const K
     if (!mbar_wait(bars.full(st), ring.phase, wc)) { ok = false; break; }
     ring.advance();
     tc_fence_after();
-    issue_ss<D, DT>(tS, k_lo, q_kmaj0 + st * kStageW);
-    umma_commit(bars.s_full());
-    issue_ss<D, DT>(tDP, v_lo, q_kmaj0 + st * kStageW + kTileW);
-    umma_commit(bars.dp_full());
+    issue_ss<D, DT>(leader, tS, k_lo, q_kmaj0 + st * kStageW);
+    umma_commit_if(leader, bars.s_full());
+    issue_ss<D, DT>(leader, tDP, v_lo, q_kmaj0 + st * kStageW + kTileW);
+    umma_commit_if(leader, bars.dp_full());
     for (int s = 0; s < k.n_steps; ++s) {
       const bool has_next = s + 1 < k.n_steps;
       // Probed together without blocking: bit 0 P^T written, 1 the next
@@ -860,32 +872,32 @@ __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const K
       if (!(done & 1u) && !mbar_wait(bars.p_ready(), p_ph, wc)) { ok = false; break; }
       p_ph ^= 1u;
       tc_fence_after();
-      issue_ts<D, DT, true>(tDV, tS, q_mn0 + st * kStageW + kTileW, s > 0 ? 1u : 0u);
+      issue_ts<D, DT, true>(leader, tDV, tS, q_mn0 + st * kStageW + kTileW, s > 0 ? 1u : 0u);
       int st_n = st;
       if (has_next) {
         st_n = ring.slot;
         if (!(done & 2u) && !mbar_wait(bars.full(st_n), ring.phase, wc)) { ok = false; break; }
         ring.advance();
         tc_fence_after();
-        issue_ss<D, DT>(tS, k_lo, q_kmaj0 + st_n * kStageW);
-        umma_commit(bars.s_full());
+        issue_ss<D, DT>(leader, tS, k_lo, q_kmaj0 + st_n * kStageW);
+        umma_commit_if(leader, bars.s_full());
       }
       // dK (+)= dS^T Q_s.
       if (!(done & 4u) && !mbar_wait(bars.ds_ready(), ds_ph, wc)) { ok = false; break; }
       ds_ph ^= 1u;
       tc_fence_after();
-      issue_ts<D, DT, true>(tDK, tDP, q_mn0 + st * kStageW, s > 0 ? 1u : 0u);
-      umma_commit(bars.empty(st));
+      issue_ts<D, DT, true>(leader, tDK, tDP, q_mn0 + st * kStageW, s > 0 ? 1u : 0u);
+      umma_commit_if(leader, bars.empty(st));
       if (has_next) {
-        issue_ss<D, DT>(tDP, v_lo, q_kmaj0 + st_n * kStageW + kTileW);
-        umma_commit(bars.dp_full());
+        issue_ss<D, DT>(leader, tDP, v_lo, q_kmaj0 + st_n * kStageW + kTileW);
+        umma_commit_if(leader, bars.dp_full());
       }
       st = st_n;
     }
     if (!ok) break;
-    umma_commit(bars.dkv_done());
+    umma_commit_if(leader, bars.dkv_done());
   }
-  umma_commit(bars.drain());
+  umma_commit_if(leader, bars.drain());
   mbar_wait_teardown(bars.drain(), 0u, ok ? 2000000000ull : 20000000ull);
 }
 
@@ -1075,9 +1087,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kProducerWarp) {
     kv_softmax<D, DT>(p, &tmDK, &tmDV, tmem, base, warp, lane, bars, wc);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) kv_producer<D>(p, &tmQ, &tmK, &tmV, &tmDO, base, bars, wc);
+    kv_producer<D>(p, &tmQ, &tmK, &tmV, &tmDO, base, bars, wc);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) kv_mma<D, DT>(p, tmem, base, bars, wc);
+    kv_mma<D, DT>(p, tmem, base, bars, wc);
   }
   __syncwarp();
   tc_fence_before();

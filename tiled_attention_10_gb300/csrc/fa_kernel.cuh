@@ -367,7 +367,8 @@ __device__ __forceinline__ void mbar_wait_teardown(uint32_t bar, uint32_t parity
 }
 
 // ---------------------------------------------------------------------------
-// Producer (one thread): Q pair, then K_0, V_0, K_1, V_1, ... into the ring.
+// Producer (one warp; one elected lane issues): Q pair, then K_0, V_0, K_1,
+// V_1, ... into the ring.
 // ---------------------------------------------------------------------------
 // Paged K/V: the 128 keys of block j of sequence `seq` come from one page
 // (page_size >= 128) or from 128 / page_size pages, one TMA box each.  Page
@@ -414,6 +415,9 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
                               const CUtensorMap* tmK, const CUtensorMap* tmV, uint32_t sQ,
                               uint32_t sRing, const Bars& bars, const WaitCtl& wc) {
   using C = Cfg<D, DT>;
+  // The whole warp runs this role; one elected lane arms the barriers and
+  // issues the copies (see elect_one).
+  const bool leader = elect_one();
   uint32_t ring = 0, it = 0;
   bool ok = true;
   const uint64_t pol_stream = l2_policy_evict_first();
@@ -437,18 +441,20 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
       if (item.solo) {
         // One Q tile (into slot 0's buffer), then K of each slot's first
         // block, then per step: V of each slot's block, K of each slot's next.
-        mbar_arrive_expect_tx(bars.q_full(), C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_q_tile(sQ + c * C::kChunkBytes, tmQ, bars.q_full(), p.layout, c * C::kBoxElems,
-                     item.qt * kBM, h, b, pol_stream);
+        if (leader) mbar_arrive_expect_tx(bars.q_full(), C::kTileBytes);
+        if (leader)
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_q_tile(sQ + c * C::kChunkBytes, tmQ, bars.q_full(), p.layout, c * C::kBoxElems,
+                       item.qt * kBM, h, b, pol_stream);
         ++it;
         auto load = [&](int kv, int blk) -> bool {
           const int slot = static_cast<int>(ring % C::kSlots);
           if (!mbar_wait(bars.empty(slot), ((ring / C::kSlots) & 1u) ^ 1u, wc)) return false;
-          mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_tile(sRing + slot * C::kTileBytes + c * C::kChunkBytes, kv == 0 ? tmK : tmV,
-                     bars.full(slot), p.layout, c * C::kBoxElems, blk * kBN, hk, b);
+          if (leader) mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
+          if (leader)
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_tile(sRing + slot * C::kTileBytes + c * C::kChunkBytes, kv == 0 ? tmK : tmV,
+                       bars.full(slot), p.layout, c * C::kBoxElems, blk * kBN, hk, b);
           ++ring;
           return true;
         };
@@ -460,8 +466,9 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
         continue;
       }
     }
-    mbar_arrive_expect_tx(bars.q_full(), (n0 > 0 ? C::kTileBytes : 0) + (n1 > 0 ? C::kTileBytes : 0));
-    for (int t = 0; t < 2; ++t) {
+    if (leader)
+      mbar_arrive_expect_tx(bars.q_full(), (n0 > 0 ? C::kTileBytes : 0) + (n1 > 0 ? C::kTileBytes : 0));
+    for (int t = 0; t < 2 && leader; ++t) {
       if ((t == 0 ? n0 : n1) == 0) continue;
       for (int c = 0; c < C::kChunks; ++c)
         tma_q_tile(sQ + t * C::kTileBytes + c * C::kChunkBytes, tmQ, bars.q_full(), p.layout,
@@ -486,12 +493,12 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
       for (int kv = 0; kv < 2; ++kv) {
         const int slot = static_cast<int>(ring % C::kSlots);
         if (!mbar_wait(bars.empty(slot), ((ring / C::kSlots) & 1u) ^ 1u, wc)) { ok = false; break; }
-        mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
+        if (leader) mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
         const CUtensorMap* map = kv == 0 ? tmK : tmV;
         if constexpr (kPagedMode) {
-          paged_tile<D, DT>(sRing + slot * C::kTileBytes, map, bars.full(slot), p, pb, hk);
+          if (leader) paged_tile<D, DT>(sRing + slot * C::kTileBytes, map, bars.full(slot), p, pb, hk);
           if (kv == 1 && j + 1 < nmax) paged_lookup(p, table, last_page, item.lo + j + 1, pb);
-        } else {
+        } else if (leader) {
           for (int c = 0; c < C::kChunks; ++c)
             tma_tile(sRing + slot * C::kTileBytes + c * C::kChunkBytes, map, bars.full(slot),
                      p.layout, c * C::kBoxElems,
@@ -1325,7 +1332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     reg_alloc_dec<RegSplit::kControl>();
     if (warp == kProducerWarp) {
-      if (lane == 0) producer_role<D, DT, kMode>(p, &tmQ, &tmK, &tmV, sQ, sRing, bars, wc);
+      producer_role<D, DT, kMode>(p, &tmQ, &tmK, &tmV, sQ, sRing, bars, wc);
     } else if (warp == kMmaWarp) {
       mma_role<D, DT, kMode>(p, tmem, sQ, sRing, bars, wc);
     }
