@@ -185,7 +185,7 @@ __device__ __forceinline__ int dkdv_first_q_tile(const BwdParams& p, int j) {
 // With `zero` nothing is read from TMEM and zeros are written.
 template <int DT>
 __device__ __forceinline__ void store_box64(uint32_t tsrc, float mul, bool zero, uint32_t stage,
-                                            int lane, const CUtensorMap* map, int layout,
+                                            int lane, bool leader, const CUtensorMap* map, int layout,
                                             int32_t col0, int32_t row0, int32_t h, int32_t b,
                                             bool do_store) {
   uint32_t pk[32];
@@ -207,7 +207,7 @@ __device__ __forceinline__ void store_box64(uint32_t tsrc, float mul, bool zero,
     }
   }
   // The previous TMA store from this staging box must have read it.
-  if (lane == 0) bulk_wait_group_read0();
+  if (leader) bulk_wait_group_read0();
   __syncwarp();
 #pragma unroll
   for (int u = 0; u < 8; ++u)
@@ -215,7 +215,7 @@ __device__ __forceinline__ void store_box64(uint32_t tsrc, float mul, bool zero,
                  pk[4 * u + 2], pk[4 * u + 3]);
   fence_proxy_async_smem();
   __syncwarp();
-  if (lane == 0 && do_store) {
+  if (leader && do_store) {
     tma_store_tile(map, stage, layout, col0, row0, h, b);
     bulk_commit_group();
   }
@@ -905,6 +905,8 @@ template <int D, int DT>
 __device__ void kv_softmax(const BwdParams& p, const CUtensorMap* tmDK, const CUtensorMap* tmDV,
                            uint32_t tmem, uint32_t smem, int warp, int lane, const KvBars& bars,
                            const WaitCtl& wc) {
+  // Issues and waits for this warp's bulk stores (see elect_one).
+  const bool leader = elect_one();
   using C = KvCfg<D>;
   const int quad = warp & 3, half = warp >> 2;
   const int r = quad * 32 + lane;
@@ -1015,24 +1017,25 @@ __device__ void kv_softmax(const BwdParams& p, const CUtensorMap* tmDK, const CU
     const bool in_range = row0 < p.S_kv;
     if (D == 128) {
       const uint32_t stV = smem + static_cast<uint32_t>(warp) * 2 * C::kEpiBox;
-      store_box64<DT>(tDV + 64 * half, 1.0f, zero, stV, lane, tmDV, p.layout, 64 * half, row0,
-                      k.hk, k.b, in_range);
-      store_box64<DT>(tDK + 64 * half, p.scale, zero, stV + C::kEpiBox, lane, tmDK, p.layout,
-                      64 * half, row0, k.hk, k.b, in_range);
+      store_box64<DT>(tDV + 64 * half, 1.0f, zero, stV, lane, leader, tmDV, p.layout, 64 * half,
+                      row0, k.hk, k.b, in_range);
+      store_box64<DT>(tDK + 64 * half, p.scale, zero, stV + C::kEpiBox, lane, leader, tmDK,
+                      p.layout, 64 * half, row0, k.hk, k.b, in_range);
     } else if (half == 0) {
       const uint32_t stV = smem + static_cast<uint32_t>(warp) * 2 * C::kEpiBox;
-      store_box64<DT>(tDV, 1.0f, zero, stV, lane, tmDV, p.layout, 0, row0, k.hk, k.b, in_range);
-      store_box64<DT>(tDK, p.scale, zero, stV + C::kEpiBox, lane, tmDK, p.layout, 0, row0, k.hk,
-                      k.b, in_range);
+      store_box64<DT>(tDV, 1.0f, zero, stV, lane, leader, tmDV, p.layout, 0, row0, k.hk, k.b,
+                      in_range);
+      store_box64<DT>(tDK, p.scale, zero, stV + C::kEpiBox, lane, leader, tmDK, p.layout, 0, row0,
+                      k.hk, k.b, in_range);
     }
     // The staging boxes are the next unit's K / V tiles: their stores must
     // have read them before the producer reloads.
-    if (lane == 0) bulk_wait_group_read0();
+    if (leader) bulk_wait_group_read0();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.epi_done());
   }
-  if (lane == 0) bulk_wait_group0();
+  if (leader) bulk_wait_group0();
   __syncwarp();
 }
 

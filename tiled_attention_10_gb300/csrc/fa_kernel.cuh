@@ -1006,6 +1006,10 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
   constexpr bool kSplit = kMode == kModeSplit;    // dense split: [n*B, H, S_q, D] partials
   constexpr bool split = kSplit || kVarSplit;     // fp32 partial O and lse
   constexpr bool kVar = kMode >= kModeVarlen;
+  // The lane that issues this warp's output stores and waits for them (a
+  // bulk async-group belongs to the thread that committed it, so the same
+  // elected lane does both; see elect_one).
+  const bool leader = elect_one();
 
   float sl2 = p.scale_log2;
   float o_mul = 1.0f;
@@ -1119,7 +1123,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
       const uint32_t ph = solo_phase;
       solo_phase ^= 1u;
       if (t == 1) {
-        if (lane == 0) bulk_wait_group_read0();  // this box's last store has read it
+        if (leader) bulk_wait_group_read0();  // this box's last store has read it
         __syncwarp();
         st_shared_f2(ml, m_run, l);
         tc_fence_before();
@@ -1208,7 +1212,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
         }
       }
       // The previous TMA store from this staging box must have read it.
-      if (lane == 0) bulk_wait_group_read0();
+      if (leader) bulk_wait_group_read0();
       __syncwarp();
       // Staging row of this thread's row: the box's element order.  The
       // head-major partial box of a packed tile (heads x tokens) takes row
@@ -1222,7 +1226,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
       __syncwarp();
       // Rows past S_q are clipped by the map; a store never starts at a
       // negative row.
-      if (lane == 0 && (kVar ? (item.q_row0 + box_row0 >= 0 && item.q_row0 + box_row0 < p.S_q)
+      if (leader && (kVar ? (item.q_row0 + box_row0 >= 0 && item.q_row0 + box_row0 < p.S_q)
                              : box_row0 < p.S_q)) {
         if (kVarSplit)
           tma_store_4d(tmOp, stage, 32 * bx, static_cast<int32_t>(item.q_row0) + box_row0,
@@ -1257,7 +1261,7 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     tc_fence_before();
   }
   // Every TMA store of this warp has completed before the CTA exits.
-  if (lane == 0) bulk_wait_group0();
+  if (leader) bulk_wait_group0();
   __syncwarp();
 }
 
