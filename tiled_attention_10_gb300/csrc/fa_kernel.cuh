@@ -648,14 +648,12 @@ __device__ bool mma_solo_unit(bool leader, const Item& item, RingPos& rp, uint32
       if (j >= n[t]) continue;
       const RingPos& vt = t ? v[1] : v[0];
       const RingPos& kt = t ? k[1] : k[0];
-      if (!mbar_wait(bars.p_half(t, C::kFp8 ? 0 : 1), p_phase[t], wc)) return false;
+      if (!mbar_wait(bars.p_half(t, 0), p_phase[t], wc)) return false;
       if (!mbar_wait(bars.full(vt.slot), vt.phase, wc)) return false;
       tc_fence_after();
       issue_pv_half<D, DT, 0>(leader, tO[t], tS[t], v_lo0 + vt.slot * kTileW, j > 0 ? 1u : 0u);
-      if constexpr (C::kFp8) {
-        if (!mbar_wait(bars.p_half(t, 1), p_phase[t], wc)) return false;
-        tc_fence_after();
-      }
+      if (!mbar_wait(bars.p_half(t, 1), p_phase[t], wc)) return false;
+      tc_fence_after();
       p_phase[t] ^= 1u;
       issue_pv_half<D, DT, 1>(leader, tO[t], tS[t], v_lo0 + vt.slot * kTileW, 1u);
       if (j + 1 < n[t]) {
@@ -744,31 +742,27 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
         rp.advance<C::kSlots>();
       }
       bool v_ready = false, k_ready = !has_next;
-      // This thread sets the pace, and a blocking wait costs it about as much
-      // as a product even when the barrier has long completed (the loads run
-      // blocks ahead, and the softmax is usually done).  So every barrier the
-      // block needs is first probed with non-blocking tests issued together,
-      // whose latencies overlap; a blocking wait runs only for one that has
-      // not completed yet.  (Skipping the K and V waits altogether -- unsafe,
-      // measured once as a bound -- took the 4 x 32 x 4096 x 128 bf16 pass
-      // from 697 to 647 us.)
-      // 16-bit P: one barrier for the whole of P, then both halves' products
-      // back to back (686 against 715 us with a wait per half).  e4m3 P: the
-      // first half's product starts while the softmax, which sets the pace
-      // there, computes the second half.
-      constexpr int kPH = C::kFp8 ? 0 : 1;
-      // bit 0 / 1: P of tile 0 / 1, bit 2: V_j, bit 3: K_{j+1}.  (e4m3: the
-      // softmax sets the pace and the blocking waits are kept.)
+      // This warp's issue sets the pace, and a blocking wait costs it about as
+      // much as a product even when the barrier has long completed (the
+      // loads run blocks ahead, and the softmax is usually done).  So every
+      // barrier the block needs is first probed with non-blocking tests
+      // issued together, whose latencies overlap; a blocking wait runs only
+      // for one that has not completed yet.  (Skipping the K and V waits
+      // altogether -- unsafe, measured once as a bound -- took the 4 x 32 x
+      // 4096 x 128 bf16 pass from 697 to 647 us.)  P comes in two halves: the
+      // first half's product runs while the softmax computes the second.
+      // bit 0 / 1: first half of P of tile 0 / 1, bit 2: V_j, bit 3: K_{j+1}.
+      // (e4m3: the softmax sets the pace and the blocking waits are kept.)
       uint32_t done = 0u;
       if constexpr (!C::kFp8) {
-        done = (mbar_test_wait(bars.p_half(0, kPH), p_phase[0]) ? 1u : 0u) |
-               (mbar_test_wait(bars.p_half(1, kPH), p_phase[1]) ? 2u : 0u) |
+        done = (mbar_test_wait(bars.p_half(0, 0), p_phase[0]) ? 1u : 0u) |
+               (mbar_test_wait(bars.p_half(1, 0), p_phase[1]) ? 2u : 0u) |
                (mbar_test_wait(bars.full(slotV), phV) ? 4u : 0u) |
                (mbar_test_wait(bars.full(slotKn), phK) ? 8u : 0u);
       }
       for (int t = 0; t < 2; ++t) {
         if (j >= n[t]) continue;
-        if (!((done >> t) & 1u) && !mbar_wait(bars.p_half(t, kPH), p_phase[t], wc)) {
+        if (!((done >> t) & 1u) && !mbar_wait(bars.p_half(t, 0), p_phase[t], wc)) {
           ok = false;
           break;
         }
@@ -778,10 +772,8 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
         }
         tc_fence_after();
         issue_pv_half<D, DT, 0>(leader, tO[t], tS[t], v_lo0 + slotV * kTileW, j > 0 ? 1u : 0u);
-        if constexpr (C::kFp8) {
-          if (!mbar_wait(bars.p_half(t, 1), p_phase[t], wc)) { ok = false; break; }
-          tc_fence_after();
-        }
+        if (!mbar_wait(bars.p_half(t, 1), p_phase[t], wc)) { ok = false; break; }
+        tc_fence_after();
         p_phase[t] ^= 1u;
         issue_pv_half<D, DT, 1>(leader, tO[t], tS[t], v_lo0 + slotV * kTileW, 1u);
         if (j + 1 < n[t]) {
@@ -799,12 +791,13 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
       }
       if (!ok) break;
       // V_j's and K_{j+1}'s slots go back to the producer once every product
-      // that reads them has completed.  When tile 1 issued S_1(j+1) above,
-      // the commit that signals it covers all of them, and tile 1's softmax
-      // warps, which wait for that signal anyway, hand the slots back (two
-      // commits fewer for this thread, which sets the pace); otherwise this
-      // thread commits them.
-      const bool released_by_softmax = j + 1 < n[1];
+      // that reads them has completed.  16-bit: when tile 1 issued S_1(j+1)
+      // above, the commit that signals it covers all of them, and tile 1's
+      // softmax warps, which wait for that signal anyway, hand the slots back
+      // (two commits fewer for this warp); otherwise, and always for e4m3
+      // (whose softmax sets the pace: 346 against 332 us on 1 x 32 x 8192
+      // causal when it releases), this warp commits them.
+      const bool released_by_softmax = !C::kFp8 && j + 1 < n[1];
       if (!released_by_softmax) umma_commit_if(leader, bars.empty(slotV));
       if (has_next) {
         // Every tile that uses K_{j+1} has issued its S by now (a tile with
@@ -841,9 +834,9 @@ __device__ __forceinline__ void ld_shared_f2(uint32_t addr, float& a, float& b) 
 
 // One K/V block of the softmax for one query row (the thread's TMEM lane):
 // row max, running-max update with conditional O rescale, P = 2^(s*sl2 - m)
-// in two halves (16-bit P signalled once, e4m3 P half by half), row sum.  Instantiated twice -- with and without
-// the tail/causal mask -- so the unmasked copy, which almost every block
-// runs, is one contiguous straight-line body.
+// in two halves, each signalled once written, row sum.  Instantiated twice --
+// with and without the tail/causal mask -- so the unmasked copy, which almost
+// every block runs, is one contiguous straight-line body.
 template <int D, int DT, bool kMasked>
 __device__ __forceinline__ void softmax_block(float (&s)[128], int lim, int j, float sl2,
                                               float& m_run, float& l, uint32_t tS, uint32_t tO,
@@ -962,13 +955,11 @@ __device__ __forceinline__ void softmax_block(float (&s)[128], int lim, int j, f
       }
       tmem_st_x32(tS + 32 * h, pk);
     }
-    // 16-bit P is signalled once, after both halves (the issuing thread waits
-    // for all of it); e4m3 P half by half.
-    if (C::kFp8 || h == 1) {
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bars.p_half(t, h));
-    }
+    // Each half is signalled once written: its product runs while the next
+    // half is computed.
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bars.p_half(t, h));
   }
   {
     float x0, x1;
@@ -1043,9 +1034,9 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
     const uint32_t ring_base = ring_pos;
     ring_pos += item.solo ? 2u * static_cast<uint32_t>(item.n[0] + item.n[1])
                           : 2u * static_cast<uint32_t>(max(item.n[0], item.n[1]));
-    // Tile 1 hands back the ring slots of V_{j-1} and K_j once S_1(j) is
-    // ready (see mma_role): one thread of the warpgroup.
-    const bool releaser = t == 1 && !item.solo && threadIdx.x == 128;
+    // 16-bit: tile 1 hands back the ring slots of V_{j-1} and K_j once S_1(j)
+    // is ready (see mma_role): one thread of the warpgroup.
+    const bool releaser = !C::kFp8 && t == 1 && !item.solo && threadIdx.x == 128;
     // Tile rows are tokens (dense, split: 128 of one head); varlen / paged
     // with GQA packing: 2^shift heads of each of 128 >> shift tokens.
     const int shift = kVar ? p.q_pack_log2 : 0;
