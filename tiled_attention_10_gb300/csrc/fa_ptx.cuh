@@ -218,47 +218,11 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // ---------------------------------------------------------------------------
-// tcgen05.mma (single CTA).  D in TMEM (fp32), A from a shared-memory
-// descriptor or from TMEM, B from a shared-memory descriptor.
+// tcgen05.mma (single CTA), D in TMEM (fp32): A from a shared-memory
+// descriptor (umma_ss_w) or from TMEM (umma_ts_w), B from a shared-memory
+// descriptor.  Each 64-bit descriptor is passed as its two 32-bit words so
+// that a caller can step the start-address field (low word) with one add.
 // ---------------------------------------------------------------------------
-template <bool kFp8>
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  if constexpr (kFp8) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
-}
-
-template <bool kFp8>
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  if constexpr (kFp8) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
-}
-
-// Same, with each 64-bit descriptor passed as its two 32-bit words so that a
-// caller can step the start-address field (low word) with one 32-bit add.
 template <bool kFp8>
 __device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                           uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
@@ -340,15 +304,6 @@ __device__ __forceinline__ bool elect_one() {
 //   dimension for one k; 8 k-rows form a 1024-byte atom; SBO = distance to the
 //   next 8 k-rows, LBO = distance to the next 128-byte chunk of MN.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
 
 // The two 32-bit words of a 128-byte-swizzle descriptor.  The start address
 // (>> 4) sits in the low 14 bits of the low word; shared-memory addresses stay
