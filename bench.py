@@ -22,6 +22,7 @@ import glob
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -38,16 +39,25 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 FWD_SOURCES = ("fa_api.cu", "fa_kernel.cuh", "fa_ptx.cuh", "fa_tmem_io.cuh", "fa_inst_*.cu")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without its comments and with runs of white space collapsed (the kernel
+    sources hold no string literal with a comment marker in it)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_sha() -> str:
-    """Hash of the forward kernel's sources (kernel, PTX helpers, instantiations and the host
-    code that sets up its launch): ties a recorded ncu capture to the kernel it measured."""
+    """Hash of the forward kernel's code (kernel, PTX helpers, instantiations and the host
+    code that sets up its launch; comments and layout excluded): ties a recorded ncu capture
+    to the kernel it measured, and a comment edit does not detach it."""
     h = hashlib.sha256()
     files = set()
     for pat in FWD_SOURCES:
         files.update(glob.glob(os.path.join(ROOT, "tiled_attention_10_gb300", "csrc", pat)))
     for f in sorted(files):
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -66,7 +66,7 @@ constexpr int kThreads = 384;
 // Registers per thread after setmaxnreg: softmax warpgroups / control
 // warpgroup; 256 * softmax + 128 * control = 384 * 168 (the launch budget).
 // 200 hold a softmax thread's 128-score row; the control roles (item
-// decoding, ring bookkeeping, the issuing thread's barrier probes) need ~100.
+// decoding, ring bookkeeping, the issuing warp's barrier probes) need ~100.
 // Kernel modes: the whole pass over dense [B,H,S,D] tensors, the split-KV
 // pass (partials in a workspace), packed variable-length sequences, and
 // packed queries against a paged K/V cache.
