@@ -471,7 +471,7 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
       const bool has_next = j + 1 < n;
       int slotKn = slotK;
       // The barriers of this block, probed together without blocking (this
-      // thread sets the pace and a blocking wait costs it about a product):
+      // warp's issue sets the pace; a blocking wait costs it about a product):
       // bit 0 K_{j+1} loaded, 1 S read, 2 dS_j written, 3 V_{j+1} loaded.
       const uint32_t done = (mbar_test_wait(bars.kfull(kr.slot), kr.phase) ? 1u : 0u) |
                             (mbar_test_wait(bars.s_free(), (s_issued - 1) & 1u) ? 2u : 0u) |
