@@ -18,8 +18,9 @@
  *   warps 10-11 idle
  * The launch gives every thread 168 registers (three warps share each SM
  * sub-partition's register file); the control warpgroup then hands registers
- * to the softmax warpgroups with setmaxnreg (104 / 200), so that a softmax
- * thread can hold its whole 128-column score row in registers.
+ * to the softmax warpgroups with setmaxnreg (104 / 200; 120 / 192 at D = 64),
+ * so that a softmax thread can hold its whole 128-column score row in
+ * registers.
  *
  * Tensor memory (512 columns x 128 lanes, fp32):
  *   [0,128)   S for tile 0   (P for tile 0 overwrites its first columns)
@@ -63,10 +64,6 @@ namespace fa {
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // key/value rows per tile
 constexpr int kThreads = 384;
-// Registers per thread after setmaxnreg: softmax warpgroups / control
-// warpgroup; 256 * softmax + 128 * control = 384 * 168 (the launch budget).
-// 200 hold a softmax thread's 128-score row; the control roles (item
-// decoding, ring bookkeeping, the issuing warp's barrier probes) need ~100.
 // Kernel modes: the whole pass over dense [B,H,S,D] tensors, the split-KV
 // pass (partials in a workspace), packed variable-length sequences, and
 // packed queries against a paged K/V cache.
@@ -74,11 +71,6 @@ constexpr int kModeDense = 0, kModeSplit = 1, kModeVarlen = 2, kModePaged = 3;
 // Paged K/V with each unit's keys split into n_splits chunks (fp32 partials,
 // merged by the combine kernel): the partition-and-reduce of paged decoding.
 constexpr int kModePagedSplit = 4;
-struct RegSplit {
-  static constexpr uint32_t kSoftmax = 200;
-  static constexpr uint32_t kControl = 104;
-  static_assert(256 * kSoftmax + 128 * kControl == 384 * 168, "register budget");
-};
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
@@ -149,6 +141,15 @@ struct Cfg {
   static constexpr uint32_t kIdescQK = umma_idesc(kFmt, false, kBM, kBN);
   static constexpr uint32_t kIdescPV = umma_idesc(kFmt, true, kBM, D);
   static constexpr float kRescaleThreshold = kFp8 ? 0.0f : 8.0f;
+  // Registers per thread after setmaxnreg: softmax warpgroups / control
+  // warpgroup; 256 * softmax + 128 * control = 384 * 168 (the launch budget).
+  // ~200 hold a softmax thread's 128-score row; the control roles (item
+  // decoding, ring bookkeeping, the issuing warp's barrier probes) need ~100.
+  // D = 64 runs ~2 % faster with 192 / 120 (2x16x4097x64 causal 86.4 -> 84.8
+  // us); D = 128 keeps 200 / 104 (192 / 120 made e4m3 1.8 % slower).
+  static constexpr uint32_t kRegSoftmax = D == 64 ? 192 : 200;
+  static constexpr uint32_t kRegControl = D == 64 ? 120 : 104;
+  static_assert(256 * kRegSoftmax + 128 * kRegControl == 384 * 168, "register budget");
   // log2 of P's scale: e4m3 P holds 256 * p (= 2^(x + 8)), so that weights
   // down to 2^-17 of the row max stay representable; the row sum l then
   // carries the same factor, which O / l cancels and the LSE subtracts.
@@ -1322,10 +1323,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp < kProducerWarp) {
-    reg_alloc_inc<RegSplit::kSoftmax>();
+    reg_alloc_inc<C::kRegSoftmax>();
     softmax_role<D, DT, kMode>(p, &tmO, &tmOp, tmem, sEpi, warp, lane, bars, wc);
   } else {
-    reg_alloc_dec<RegSplit::kControl>();
+    reg_alloc_dec<C::kRegControl>();
     if (warp == kProducerWarp) {
       producer_role<D, DT, kMode>(p, &tmQ, &tmK, &tmV, sQ, sRing, bars, wc);
     } else if (warp == kMmaWarp) {
