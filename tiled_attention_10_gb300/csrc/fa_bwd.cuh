@@ -565,12 +565,19 @@ __device__ void dq_softmax(const BwdParams& p, void* dq_out, uint32_t tmem, int 
       const bool masked = (static_cast<int64_t>(j) * 128 + 128 > p.S_kv) ||
                           (p.causal && static_cast<int64_t>(j) * 128 + 127 > static_cast<int64_t>(i) * 128);
       const int lim = static_cast<int>(max(min(col_end - col0, int64_t(64)), int64_t(0)));
+      // Two straight-line loops, the mask test outside them (a block-uniform
+      // branch inside the unrolled loop splits it into basic blocks).
       float pr[64];
+      if (masked) {
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float x = __uint_as_float(sr[c >> 5][c & 31]);
-        if (masked) x = (c < lim) ? x : -CUDART_INF_F;
-        pr[c] = ex2(fmaf(x, sl2, neg_lse2));
+        for (int c = 0; c < 64; ++c) {
+          const float x = (c < lim) ? __uint_as_float(sr[c >> 5][c & 31]) : -CUDART_INF_F;
+          pr[c] = ex2(fmaf(x, sl2, neg_lse2));
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          pr[c] = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, neg_lse2));
       }
       if (!mbar_wait(bars.dp_full(), dp_ph, wc)) { ok = false; break; }
       dp_ph ^= 1u;
@@ -953,17 +960,30 @@ __device__ void kv_softmax(const BwdParams& p, const CUtensorMap* tmDK, const CU
       tmem_wait_ld();
       reg_dep_x32(sr[0]);
       reg_dep_x32(sr[1]);
+      // Two straight-line loops, the mask test outside them (as in dq_softmax).
       float pr[64];
+      if (masked) {
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l4 = ld_shared_f4(sLse + 16 * c4);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = ld_shared_f4(sLse + 16 * c4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 4 * c4 + e;
-          float x = __uint_as_float(sr[c >> 5][c & 31]);
-          if (masked) x = (c >= lo) ? x : -CUDART_INF_F;
-          pr[c] = ex2(fmaf(x, sl2, -lv[e]));
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            const float x = (c >= lo) ? __uint_as_float(sr[c >> 5][c & 31]) : -CUDART_INF_F;
+            pr[c] = ex2(fmaf(x, sl2, -lv[e]));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = ld_shared_f4(sLse + 16 * c4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            pr[c] = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lv[e]));
+          }
         }
       }
       {
