@@ -522,6 +522,14 @@ __device__ __forceinline__ void st_global_v4(void* ptr, uint32_t a, uint32_t b, 
                : "memory");
 }
 
+// Packed fp32 pair product (sm_100+), beside the pair FMA / add of fa_ptx.cuh:
+// the P and dS arithmetic of the backward's softmax warps runs on pairs.
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 template <int D, int DT>
 __device__ void dq_softmax(const BwdParams& p, void* dq_out, uint32_t tmem, int warp, int lane,
                            const DqBars& bars, const WaitCtl& wc) {
@@ -568,16 +576,26 @@ __device__ void dq_softmax(const BwdParams& p, void* dq_out, uint32_t tmem, int 
       // Two straight-line loops, the mask test outside them (a block-uniform
       // branch inside the unrolled loop splits it into basic blocks).
       float pr[64];
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nlse2 = f2_pack(neg_lse2, neg_lse2);
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float x = (c < lim) ? __uint_as_float(sr[c >> 5][c & 31]) : -CUDART_INF_F;
-          pr[c] = ex2(fmaf(x, sl2, neg_lse2));
+        for (int c = 0; c < 64; c += 2) {
+          const float x0 = (c < lim) ? __uint_as_float(sr[c >> 5][c & 31]) : -CUDART_INF_F;
+          const float x1 = (c + 1 < lim) ? __uint_as_float(sr[c >> 5][(c + 1) & 31]) : -CUDART_INF_F;
+          f2_unpack(f2_fma(f2_pack(x0, x1), sl2x2, nlse2), pr[c], pr[c + 1]);
+          pr[c] = ex2(pr[c]);
+          pr[c + 1] = ex2(pr[c + 1]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          pr[c] = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, neg_lse2));
+        for (int c = 0; c < 64; c += 2) {
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c >> 5][c & 31]),
+                                   __uint_as_float(sr[c >> 5][(c + 1) & 31])),
+                           sl2x2, nlse2),
+                    pr[c], pr[c + 1]);
+          pr[c] = ex2(pr[c]);
+          pr[c + 1] = ex2(pr[c + 1]);
+        }
       }
       if (!mbar_wait(bars.dp_full(), dp_ph, wc)) { ok = false; break; }
       dp_ph ^= 1u;
@@ -589,11 +607,15 @@ __device__ void dq_softmax(const BwdParams& p, void* dq_out, uint32_t tmem, int 
       reg_dep_x32(dr[0]);
       reg_dep_x32(dr[1]);
       uint32_t pk[32];
+      const uint64_t ndsum2 = f2_pack(-dsum, -dsum);
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float d0 = pr[2 * c] * (__uint_as_float(dr[(2 * c) >> 5][(2 * c) & 31]) - dsum);
-        const float d1 =
-            pr[2 * c + 1] * (__uint_as_float(dr[(2 * c + 1) >> 5][(2 * c + 1) & 31]) - dsum);
+        float d0, d1;
+        f2_unpack(f2_mul(f2_pack(pr[2 * c], pr[2 * c + 1]),
+                         f2_add(f2_pack(__uint_as_float(dr[(2 * c) >> 5][(2 * c) & 31]),
+                                        __uint_as_float(dr[(2 * c + 1) >> 5][(2 * c + 1) & 31])),
+                                ndsum2)),
+                  d0, d1);
         pk[c] = pack2<DT>(d0, d1);
       }
       tmem_st_x32(tDS, pk);
@@ -962,16 +984,20 @@ __device__ void kv_softmax(const BwdParams& p, const CUtensorMap* tmDK, const CU
       reg_dep_x32(sr[1]);
       // Two straight-line loops, the mask test outside them (as in dq_softmax).
       float pr[64];
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
       if (masked) {
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {
           const float4 l4 = ld_shared_f4(sLse + 16 * c4);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
+          for (int e = 0; e < 4; e += 2) {
             const int c = 4 * c4 + e;
-            const float x = (c >= lo) ? __uint_as_float(sr[c >> 5][c & 31]) : -CUDART_INF_F;
-            pr[c] = ex2(fmaf(x, sl2, -lv[e]));
+            const float x0 = (c >= lo) ? __uint_as_float(sr[c >> 5][c & 31]) : -CUDART_INF_F;
+            const float x1 = (c + 1 >= lo) ? __uint_as_float(sr[c >> 5][(c + 1) & 31]) : -CUDART_INF_F;
+            f2_unpack(f2_fma(f2_pack(x0, x1), sl2x2, f2_pack(-lv[e], -lv[e + 1])), pr[c], pr[c + 1]);
+            pr[c] = ex2(pr[c]);
+            pr[c + 1] = ex2(pr[c + 1]);
           }
         }
       } else {
@@ -980,9 +1006,14 @@ __device__ void kv_softmax(const BwdParams& p, const CUtensorMap* tmDK, const CU
           const float4 l4 = ld_shared_f4(sLse + 16 * c4);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
+          for (int e = 0; e < 4; e += 2) {
             const int c = 4 * c4 + e;
-            pr[c] = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lv[e]));
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c >> 5][c & 31]),
+                                     __uint_as_float(sr[c >> 5][(c + 1) & 31])),
+                             sl2x2, f2_pack(-lv[e], -lv[e + 1])),
+                      pr[c], pr[c + 1]);
+            pr[c] = ex2(pr[c]);
+            pr[c + 1] = ex2(pr[c + 1]);
           }
         }
       }
@@ -1011,10 +1042,17 @@ __device__ void kv_softmax(const BwdParams& p, const CUtensorMap* tmDK, const CU
         for (int c4 = 0; c4 < 16; ++c4) {
           const float4 d4 = ld_shared_f4(sDsum + 16 * c4);
           const int c = 4 * c4;
-          const float a0 = pr[c] * (__uint_as_float(dr[c >> 5][c & 31]) - d4.x);
-          const float a1 = pr[c + 1] * (__uint_as_float(dr[(c + 1) >> 5][(c + 1) & 31]) - d4.y);
-          const float a2 = pr[c + 2] * (__uint_as_float(dr[(c + 2) >> 5][(c + 2) & 31]) - d4.z);
-          const float a3 = pr[c + 3] * (__uint_as_float(dr[(c + 3) >> 5][(c + 3) & 31]) - d4.w);
+          float a0, a1, a2, a3;
+          f2_unpack(f2_mul(f2_pack(pr[c], pr[c + 1]),
+                           f2_add(f2_pack(__uint_as_float(dr[c >> 5][c & 31]),
+                                          __uint_as_float(dr[c >> 5][(c + 1) & 31])),
+                                  f2_pack(-d4.x, -d4.y))),
+                    a0, a1);
+          f2_unpack(f2_mul(f2_pack(pr[c + 2], pr[c + 3]),
+                           f2_add(f2_pack(__uint_as_float(dr[c >> 5][(c + 2) & 31]),
+                                          __uint_as_float(dr[c >> 5][(c + 3) & 31])),
+                                  f2_pack(-d4.z, -d4.w))),
+                    a2, a3);
           pk[2 * c4] = pack2<DT>(a0, a1);
           pk[2 * c4 + 1] = pack2<DT>(a2, a3);
         }
