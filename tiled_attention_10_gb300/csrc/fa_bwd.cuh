@@ -712,6 +712,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{p.wait_limit_ns, p.err, abort_flag};
+  // Launched as a programmatic dependent of the row-statistics pass: wait for
+  // it before any global access, then let the dK/dV kernel (which needs only
+  // that pass) take the SMs this grid leaves as its CTAs finish.
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp < kProducerWarp) {
     dq_softmax<D, DT>(p, dq_out, tmem, warp, lane, bars, wc);
   } else if (warp == kProducerWarp) {
@@ -1145,6 +1150,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{p.wait_limit_ns, p.err, abort_flag};
+  // Launched as a programmatic dependent of the dQ kernel, which it does not
+  // read (both read only the inputs and the row statistics, complete before
+  // the dQ kernel let this grid start): no wait before the work.  But this
+  // grid finishes only after the dQ kernel has, so that work queued after the
+  // backward on the stream sees dQ too.
   if (warp < kProducerWarp) {
     kv_softmax<D, DT>(p, &tmDK, &tmDV, tmem, base, warp, lane, bars, wc);
   } else if (warp == kProducerWarp) {
@@ -1152,6 +1162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     kv_mma<D, DT>(p, tmem, base, bars, wc);
   }
+  griddep_wait();
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -1170,8 +1181,13 @@ cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
                           const BwdParams& p_kv, int grid_dq, int grid_kv, int grid_prep,
                           cudaStream_t stream) {
   // Every launch reports its own status (cudaLaunchKernelEx), so an error
-  // left pending by other code on this thread is never taken for ours.
+  // left pending by other code on this thread is never taken for ours.  The
+  // dQ and dK/dV kernels are programmatic dependents of the launch before
+  // them (see their kernels for the waits).
   cudaError_t e;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_prep);
@@ -1190,6 +1206,8 @@ cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = DqCfg<D>::kLaunchSmem;
     cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, q, k, v, dout, dq_ptr, p_dq);
     if (e != cudaSuccess) return e;
   }
@@ -1202,6 +1220,8 @@ cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = KvCfg<D>::kLaunchSmem;
     cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, q, k, v, dout, dk, dv, p_kv);
   }
   return e;
