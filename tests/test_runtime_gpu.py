@@ -153,3 +153,56 @@ def test_dependent_calls_back_to_back(split, cuda_lib):
         assert float(np.abs(o2.float().cpu().double().numpy() - O2).max()) <= 1.6e-2
         assert float(np.abs(l2.cpu().double().numpy() - L2).max()) <= 1e-3
         q.copy_(q_host.to("cuda"))   # restore Q for the next round
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_calls_back_to_back(causal, cuda_lib):
+    """The backward's dQ and dK/dV kernels are programmatic dependents of the
+    launch before them (the dK/dV kernel may start while the dQ kernel still
+    runs and waits for it only before it exits): work queued after a backward
+    call must still see all of its outputs.  Two calls, no synchronisation in
+    between: the second reads the first's dQ as its dO and writes its own dQ
+    into the buffer the first read as dO.  Compared with the same two calls
+    synchronised one by one; the backward is deterministic, so bit for bit."""
+    B, H, S, D = 1, 8, 1024, 128
+    w = Workload("t", B, H, S, S, D, "bf16", "BNSD", causal, seed=41)
+    x = make_inputs(w, device="cuda")
+    q, k, v = x.q, x.k, x.v
+    stream = torch.cuda.current_stream().cuda_stream
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, S, device="cuda")
+    assert binding.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          B, H, S, S, D, w.softmax_scale, "BNSD", causal, "bf16", None, None,
+                          None, stream) == 0
+    st, nb = binding.fa_bwd_workspace_size(B, H, S)
+    assert st == 0
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(42)
+    do0 = (torch.randn(q.shape, generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+
+    def bwd(dout, dq, dk, dv):
+        st = binding.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                            dv.data_ptr(), B, H, H, S, S, D, w.softmax_scale, "BNSD", causal,
+                            "bf16", ws.data_ptr(), nb, stream)
+        assert st == 0, binding.FA_STATUS.get(st)
+
+    def run(sync):
+        do = do0.clone()
+        dq1, dk1, dv1, dk2, dv2 = (torch.empty_like(q) for _ in range(5))
+        torch.cuda.synchronize()
+        bwd(do, dq1, dk1, dv1)
+        if sync:
+            torch.cuda.synchronize()
+        bwd(dq1, do, dk2, dv2)          # dO = the first call's dQ; dQ into the first's dO
+        torch.cuda.synchronize()
+        assert binding.fa_last_device_error(stream) == 0
+        return [t.clone() for t in (dq1, dk1, dv1, do, dk2, dv2)]
+
+    ref = run(sync=True)
+    for _ in range(3):
+        got = run(sync=False)
+        for name, a, b in zip(("dq1", "dk1", "dv1", "dq2", "dk2", "dv2"), got, ref):
+            assert torch.equal(a, b), f"{name} differs from the synchronised calls"
+        assert all(torch.isfinite(t.float()).all() for t in got)
