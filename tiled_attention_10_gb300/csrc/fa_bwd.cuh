@@ -237,15 +237,18 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __rest
   const int sub = threadIdx.x % G;
   // The block iterates uniformly (base is the same for all its threads), so
   // every lane takes part in the shuffles below.
+  // Row indices in 32 bits (a tensor of 2^32 rows of 16-bit elements would
+  // not fit in device memory): the divisions are the loop's costliest work.
+  const uint32_t s_q_pad = static_cast<uint32_t>(p.S_q_pad), n_h = static_cast<uint32_t>(p.H);
   for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x; base < total; base += stride) {
     const int64_t t = base + threadIdx.x;
     const bool active = t < total;
-    const int64_t row = active ? t / G : 0;  // (b*H + h) * S_q_pad + s
-    const int64_t bh = row / p.S_q_pad;
-    const int64_t s = row - bh * p.S_q_pad;
+    const uint32_t row = active ? static_cast<uint32_t>(t / G) : 0u;  // (b*H + h) * S_q_pad + s
+    const uint32_t bh = row / s_q_pad;
+    const uint32_t s = row - bh * s_q_pad;
     float acc = 0.0f;
     if (active && s < p.S_q) {
-      const int64_t b = bh / p.H, h = bh - b * p.H;
+      const int64_t b = bh / n_h, h = bh - static_cast<uint32_t>(b) * n_h;
       const int64_t off_o = b * p.o_st[0] + h * p.o_st[1] + s * p.o_st[2] + sub * 8;
       const int64_t off_do = b * p.do_st[0] + h * p.do_st[1] + s * p.do_st[2] + sub * 8;
       const uint4 ov = *reinterpret_cast<const uint4*>(o + off_o);
@@ -274,7 +277,8 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const uint16_t* __rest
     for (int m = G / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m, G);
     if (active && sub == 0) {
       dsum[row] = acc;
-      lse2[row] = (s < p.S_q) ? lse[bh * p.S_q + s] * 1.4426950408889634f : CUDART_INF_F;
+      lse2[row] = (s < p.S_q) ? lse[static_cast<int64_t>(bh) * p.S_q + s] * 1.4426950408889634f
+                              : CUDART_INF_F;
     }
   }
 }
