@@ -185,7 +185,8 @@ __device__ __forceinline__ int dkdv_first_q_tile(const BwdParams& p, int j) {
 // With `zero` nothing is read from TMEM and zeros are written.
 template <int DT>
 __device__ __forceinline__ void store_box64(uint32_t tsrc, float mul, bool zero, uint32_t stage,
-                                            int lane, bool leader, const CUtensorMap* map, int layout,
+                                            int lane, bool leader, const CUtensorMap* map,
+                                            int layout,
                                             int32_t col0, int32_t row0, int32_t h, int32_t b,
                                             bool do_store) {
   uint32_t pk[32];
@@ -395,7 +396,8 @@ __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
 
 // K-major x K-major product over the head dim: D[128 x 128] = A[128 x D] B[128 x D]^T.
 template <int D, int DT>
-__device__ __forceinline__ void issue_ss(bool leader, uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo) {
+__device__ __forceinline__ void issue_ss(bool leader, uint32_t d_tmem, uint32_t a_lo,
+                                         uint32_t b_lo) {
   using T = Tile<D>;
   constexpr uint32_t hi = umma_desc_hi_sw128(1024);
   constexpr uint32_t idesc = umma_idesc(DT == kBF16 ? 1u : 0u, false, 128, 128);
@@ -585,7 +587,8 @@ __device__ void dq_softmax(const BwdParams& p, void* dq_out, uint32_t tmem, int 
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           const float x0 = (c < lim) ? __uint_as_float(sr[c >> 5][c & 31]) : -CUDART_INF_F;
-          const float x1 = (c + 1 < lim) ? __uint_as_float(sr[c >> 5][(c + 1) & 31]) : -CUDART_INF_F;
+          const float x1 =
+              (c + 1 < lim) ? __uint_as_float(sr[c >> 5][(c + 1) & 31]) : -CUDART_INF_F;
           f2_unpack(f2_fma(f2_pack(x0, x1), sl2x2, nlse2), pr[c], pr[c + 1]);
           pr[c] = ex2(pr[c]);
           pr[c + 1] = ex2(pr[c + 1]);
@@ -1003,8 +1006,10 @@ __device__ void kv_softmax(const BwdParams& p, const CUtensorMap* tmDK, const CU
           for (int e = 0; e < 4; e += 2) {
             const int c = 4 * c4 + e;
             const float x0 = (c >= lo) ? __uint_as_float(sr[c >> 5][c & 31]) : -CUDART_INF_F;
-            const float x1 = (c + 1 >= lo) ? __uint_as_float(sr[c >> 5][(c + 1) & 31]) : -CUDART_INF_F;
-            f2_unpack(f2_fma(f2_pack(x0, x1), sl2x2, f2_pack(-lv[e], -lv[e + 1])), pr[c], pr[c + 1]);
+            const float x1 =
+                (c + 1 >= lo) ? __uint_as_float(sr[c >> 5][(c + 1) & 31]) : -CUDART_INF_F;
+            f2_unpack(f2_fma(f2_pack(x0, x1), sl2x2, f2_pack(-lv[e], -lv[e + 1])), pr[c],
+                      pr[c + 1]);
             pr[c] = ex2(pr[c]);
             pr[c + 1] = ex2(pr[c + 1]);
           }

@@ -468,7 +468,8 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
       }
     }
     if (leader)
-      mbar_arrive_expect_tx(bars.q_full(), (n0 > 0 ? C::kTileBytes : 0) + (n1 > 0 ? C::kTileBytes : 0));
+      mbar_arrive_expect_tx(bars.q_full(),
+                            (n0 > 0 ? C::kTileBytes : 0) + (n1 > 0 ? C::kTileBytes : 0));
     for (int t = 0; t < 2 && leader; ++t) {
       if ((t == 0 ? n0 : n1) == 0) continue;
       for (int c = 0; c < C::kChunks; ++c)
@@ -497,7 +498,8 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
         if (leader) mbar_arrive_expect_tx(bars.full(slot), C::kTileBytes);
         const CUtensorMap* map = kv == 0 ? tmK : tmV;
         if constexpr (kPagedMode) {
-          if (leader) paged_tile<D, DT>(sRing + slot * C::kTileBytes, map, bars.full(slot), p, pb, hk);
+          if (leader)
+            paged_tile<D, DT>(sRing + slot * C::kTileBytes, map, bars.full(slot), p, pb, hk);
           if (kv == 1 && j + 1 < nmax) paged_lookup(p, table, last_page, item.lo + j + 1, pb);
         } else if (leader) {
           for (int c = 0; c < C::kChunks; ++c)
@@ -533,7 +535,8 @@ __device__ __forceinline__ void issue_qk(bool leader, uint32_t d_tmem, uint32_t 
     constexpr int kStepBytes = 32;
     const uint32_t off = static_cast<uint32_t>(((kk * kStepBytes / 128) * C::kChunkBytes +
                                                 (kk * kStepBytes) % 128) >> 4);
-    if (leader) umma_ss_w<C::kFp8>(d_tmem, qlo + off, hi, klo + off, hi, C::kIdescQK, kk > 0 ? 1u : 0u);
+    if (leader)
+      umma_ss_w<C::kFp8>(d_tmem, qlo + off, hi, klo + off, hi, C::kIdescQK, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -663,7 +666,8 @@ __device__ bool mma_solo_unit(bool leader, const Item& item, RingPos& rp, uint32
         issue_qk<D, DT>(leader, tS[t], q_lo, k_lo0 + kt.slot * kTileW);
         umma_commit_if(leader, bars.s_full(t));
       } else {
-        if (t ? rf[1] : rf[0]) issue_pv_residual<D, DT>(leader, tO[t], tS[t], v_lo0 + vt.slot * kTileW);
+        if (t ? rf[1] : rf[0])
+          issue_pv_residual<D, DT>(leader, tO[t], tS[t], v_lo0 + vt.slot * kTileW);
         umma_commit_if(leader, bars.o_done(t));
       }
     }
