@@ -23,6 +23,16 @@ def test_clock_summary_flags_throttle_reasons():
     assert bench.ClockSampler.summarize([])["samples"] == 0
 
 
+def test_peak_choice_follows_run_length_and_power_cap():
+    # a short burst at full clock compares against the burst GEMM figure; a
+    # region over a second, or one that ran under the power cap, against the
+    # sustained one
+    assert not bench.use_sustained_peak(200.0, {"reasons": []})
+    assert not bench.use_sustained_peak(200.0, {})
+    assert bench.use_sustained_peak(1500.0, {"reasons": []})
+    assert bench.use_sustained_peak(200.0, {"reasons": ["sw_power_cap"]})
+
+
 def test_sample_flops_matches_nominal_formula_on_full_problem():
     w = Workload("t", 1, 1, 64, 64, 128, "bf16", "BNSD", False)
     assert bench.sample_flops(w, 1, 64) == w.flops
