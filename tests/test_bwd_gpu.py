@@ -4,7 +4,9 @@ Every element of dQ, dK and dV is held to the bound derived from the
 kernels' arithmetic (tests/bwd_helpers.py), on shapes that span several tiles
 with ragged tails in S_q and S_kv, causal and not, both layouts, fp16 and
 bf16, D = 64 and 128, grouped-query heads, S_q != S_kv (including key tiles
-no query sees), NaN-poisoned memory past the valid rows, and a NaN-filled
+no query sees), more work units than SMs (each CTA hands one unit's tiles
+and accumulators over to the next), NaN-poisoned memory past the valid
+rows, and a NaN-filled
 workspace.  O and lse come from the oracle (rounded to the types a training
 step passes) or, end to end, from the GPU forward pass.  Plus: canaries after
 every output intact, no NaN / Inf, bit-identical repeat runs, argument
@@ -95,6 +97,12 @@ CASES = [
     (1, 1, 1, 1, 300, 128, "f16", "BNSD", True, False),
     (1, 8, 2, 640, 640, 128, "bf16", "BNSD", True, False),
     (1, 2, 2, 777, 129, 64, "bf16", "BSND", False, True),
+    # more work units than SMs, so each CTA runs several in turn: 384 dQ
+    # units and 96 dK/dV units of 4 query heads each ...
+    (1, 32, 8, 1536, 1536, 64, "f16", "BSND", True, False),
+    # ... and 400 dK/dV units of which 398 no query sees (zeros), taken
+    # right after a unit with products by two of the CTAs
+    (1, 2, 2, 128, 25600, 64, "bf16", "BNSD", True, False),
 ]
 
 

@@ -29,10 +29,14 @@
  * needs no atomics and keeps every result deterministic; with D = 128 the
  * dK/dV kernel already fills all 512 TMEM columns (S^T, dP^T, dV, dK).
  *
- * Warp roles (320 threads): warps 0-7 compute P / dS (warp w serves TMEM lane
- * quarter w % 4 and column half w / 4), warp 8 is the TMA producer and warp 9
- * issues the MMAs (each role run by its whole warp, one elected lane issuing).
- * Every wait is bounded (see fa_ptx.cuh).
+ * Warp roles (512 threads): warps 0-7 compute P / dS (warp w serves TMEM lane
+ * quarter w % 4 and column half w / 4), warp 8 is the TMA producer, warp 9
+ * issues the MMAs (each role run by its whole warp, one elected lane issuing)
+ * and warps 12-15 run the epilogue: they read a unit's accumulators out of
+ * TMEM, hand them back, and write them out while the next unit's products
+ * run.  Consecutive units overlap further: Q / dO (dQ kernel) and K / V (dK/dV
+ * kernel) are reloaded as soon as the previous unit's last products that read
+ * them are done.  Every wait is bounded (see fa_ptx.cuh).
  */
 #pragma once
 #include <cuda.h>
@@ -49,9 +53,17 @@ namespace fa {
 namespace bwd {
 
 constexpr int kF16 = 0, kBF16 = 1;  // element type codes (as the forward's)
-constexpr int kThreads = 320;
+// Warp roles (512 threads, four warpgroups): warps 0-7 compute P and dS,
+// warp 8 is the TMA producer, warp 9 issues the MMAs (10 and 11 idle), warps
+// 12-15 run the epilogue -- read the accumulators out of TMEM, hand them back
+// and write them out while the next unit's products run.
+constexpr int kThreads = 512;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kEpiWarp0 = 12;
+// Registers per thread by warpgroup (setmaxnreg): launched with 128 each.
+constexpr uint32_t kRegSoftmax = 168, kRegControl = 72, kRegEpilogue = 104;
+static_assert(2 * kRegSoftmax + kRegControl + kRegEpilogue == 4 * 128, "register budget");
 constexpr uint32_t kTmemCols = 512;
 
 struct BwdParams {
@@ -68,10 +80,13 @@ struct BwdParams {
   const float* dsum;      // [B*H, S_q_pad]: rowsum(dO * O); 0 for rows >= S_q
   uint32_t* err;
   uint64_t wait_limit_ns;
+  // dK and dV (written by the dK/dV epilogue).
+  void* dk;
+  void* dv;
   // Element strides (batch, head, seq) of the tensors read or written
-  // without a tensor map: O and dO by the row-statistics pass, dQ by the dQ
-  // epilogue.  D is contiguous.
-  int64_t o_st[3], do_st[3], dq_st[3];
+  // without a tensor map: O and dO by the row-statistics pass, dQ, dK and dV
+  // by the epilogues.  D is contiguous.
+  int64_t o_st[3], do_st[3], dq_st[3], dk_st[3], dv_st[3];
 };
 
 template <int D>
@@ -94,26 +109,11 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, u
     tma_load_4d(dst, map, bar, c0, h, s, b);
 }
 
-__device__ __forceinline__ void tma_store_tile(const CUtensorMap* map, uint32_t src, int layout,
-                                               int32_t c0, int32_t s, int32_t h, int32_t b) {
-  if (layout == 0)
-    tma_store_4d(map, src, c0, s, h, b);
-  else
-    tma_store_4d(map, src, c0, h, s, b);
-}
-
 __device__ __forceinline__ void mbar_wait_teardown(uint32_t bar, uint32_t parity, uint64_t limit) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > limit) return;
   }
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
 }
 
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
@@ -128,6 +128,43 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
 template <int DT>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return DT == kF16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
+__device__ __forceinline__ void st_global_v4(void* ptr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// Epilogue helpers.  load_row: this thread's TMEM lane, D fp32 accumulator
+// columns from `src` (one 32-column load at a time), times `mul`, rounded to
+// 16-bit pairs; zeros with `zero`.  store_row: those D / 2 pairs to `dst`
+// (2 * D contiguous bytes) with 16-byte stores.
+template <int D, int DT>
+__device__ __forceinline__ void load_row(uint32_t src, float mul, bool zero,
+                                         uint32_t (&pk)[D / 2]) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t a[32];
+    if (zero) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a[i] = 0u;
+    } else {
+      tmem_ld_x32(src + 32 * c, a);
+      tmem_wait_ld();
+      reg_dep_x32(a);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[16 * c + i] = pack2<DT>(__uint_as_float(a[2 * i]) * mul, __uint_as_float(a[2 * i + 1]) * mul);
+  }
+}
+template <int D>
+__device__ __forceinline__ void store_row(uint8_t* dst, const uint32_t (&pk)[D / 2]) {
+#pragma unroll
+  for (int q = 0; q < D / 8; ++q)
+    st_global_v4(dst + 16 * q, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 }
 
 // Ring position: slot index and the parity of its current use.
@@ -178,48 +215,6 @@ __device__ __forceinline__ int dq_kv_blocks(const BwdParams& p, int i) {
 // queries q >= k): tile i sees it iff i*128 + 127 >= j*128, i.e. i >= j.
 __device__ __forceinline__ int dkdv_first_q_tile(const BwdParams& p, int j) {
   return p.causal ? j : 0;
-}
-
-// Epilogue helper: 32 rows x 64 fp32 columns of TMEM (this warp's lane
-// quarter) -> 16-bit, staged in a 32 x 128-byte swizzled box and stored by TMA.
-// With `zero` nothing is read from TMEM and zeros are written.
-template <int DT>
-__device__ __forceinline__ void store_box64(uint32_t tsrc, float mul, bool zero, uint32_t stage,
-                                            int lane, bool leader, const CUtensorMap* map,
-                                            int layout,
-                                            int32_t col0, int32_t row0, int32_t h, int32_t b,
-                                            bool do_store) {
-  uint32_t pk[32];
-  if (zero) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) pk[i] = 0u;
-  } else {
-    uint32_t a0[32], a1[32];
-    tmem_ld_x32(tsrc, a0);
-    tmem_ld_x32(tsrc + 32, a1);
-    tmem_wait_ld();
-    reg_dep_x32(a0);
-    reg_dep_x32(a1);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      pk[i] = pack2<DT>(__uint_as_float(a0[2 * i]) * mul, __uint_as_float(a0[2 * i + 1]) * mul);
-      pk[16 + i] =
-          pack2<DT>(__uint_as_float(a1[2 * i]) * mul, __uint_as_float(a1[2 * i + 1]) * mul);
-    }
-  }
-  // The previous TMA store from this staging box must have read it.
-  if (leader) bulk_wait_group_read0();
-  __syncwarp();
-#pragma unroll
-  for (int u = 0; u < 8; ++u)
-    st_shared_v4(stage + lane * 128 + ((u ^ (lane & 7)) << 4), pk[4 * u], pk[4 * u + 1],
-                 pk[4 * u + 2], pk[4 * u + 3]);
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (leader && do_store) {
-    tma_store_tile(map, stage, layout, col0, row0, h, b);
-    bulk_commit_group();
-  }
 }
 
 // ===========================================================================
@@ -300,7 +295,7 @@ struct DqCfg {
   static constexpr int kKOff = 2 * T::kBytes;
   static constexpr int kVOff = kKOff + kKSlots * T::kBytes;
   static constexpr int kBarOff = kVOff + kVSlots * T::kBytes;
-  static constexpr int kNumBars = 2 * (kKSlots + kVSlots) + 9;
+  static constexpr int kNumBars = 2 * (kKSlots + kVSlots) + 11;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
   // Requested at launch: more than half of an SM's shared memory, so that
@@ -327,6 +322,8 @@ struct DqBars {
   __device__ uint32_t dq_done() const { return x(6); }
   __device__ uint32_t dq_free() const { return x(7); }
   __device__ uint32_t drain() const { return x(8); }
+  __device__ uint32_t do_full() const { return x(9); }
+  __device__ uint32_t do_empty() const { return x(10); }
 };
 
 __device__ __forceinline__ void dq_decode(const BwdParams& p, int u, int& bh, int& i) {
@@ -334,7 +331,9 @@ __device__ __forceinline__ void dq_decode(const BwdParams& p, int u, int& bh, in
 }
 
 // Producer: Q_i and dO_i once per unit, then K_0, V_0, K_1, V_1, ... into
-// their rings.
+// their rings.  Q and dO are reloaded as soon as the previous unit's last
+// S and dP products have read them, so the next unit's loads overlap that
+// unit's last block.
 template <int D>
 __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CUtensorMap* tmK,
                             const CUtensorMap* tmV, const CUtensorMap* tmDO, uint32_t smem,
@@ -345,7 +344,7 @@ __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
   const bool leader = elect_one();
   Ring<C::kKSlots> kr;
   Ring<C::kVSlots> vr;
-  uint32_t k_issued = 0, v_issued = 0, it = 0;
+  uint32_t k_issued = 0, v_issued = 0, it = 0, do_it = 0;
   bool ok = true;
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0; ok; ++w) {
@@ -357,14 +356,17 @@ __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
     const int32_t hk = h / p.kv_group;
     const int n = dq_kv_blocks(p, i);
     if (!mbar_wait(bars.q_empty(), (it & 1u) ^ 1u, wc)) { ok = false; break; }
-    if (leader) mbar_arrive_expect_tx(bars.q_full(), 2 * T::kBytes);
-    for (int c = 0; c < T::kChunks && leader; ++c) {
+    if (leader) mbar_arrive_expect_tx(bars.q_full(), T::kBytes);
+    for (int c = 0; c < T::kChunks && leader; ++c)
       tma_tile(smem + C::kQOff + c * T::kChunkBytes, tmQ, bars.q_full(), p.layout, c * 64, i * 128,
                h, b);
-      tma_tile(smem + C::kDOOff + c * T::kChunkBytes, tmDO, bars.q_full(), p.layout, c * 64,
-               i * 128, h, b);
-    }
     ++it;
+    if (!mbar_wait(bars.do_empty(), (do_it & 1u) ^ 1u, wc)) { ok = false; break; }
+    if (leader) mbar_arrive_expect_tx(bars.do_full(), T::kBytes);
+    for (int c = 0; c < T::kChunks && leader; ++c)
+      tma_tile(smem + C::kDOOff + c * T::kChunkBytes, tmDO, bars.do_full(), p.layout, c * 64,
+               i * 128, h, b);
+    ++do_it;
     for (int j = 0; j < n && ok; ++j) {
       if (!mbar_wait(bars.kempty(kr.slot), kr.phase ^ 1u, wc)) { ok = false; break; }
       if (leader) mbar_arrive_expect_tx(bars.kfull(kr.slot), T::kBytes);
@@ -391,6 +393,7 @@ __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
     for (uint32_t r = fv; r < v_issued; ++r)
       mbar_wait_teardown(bars.vfull(r % C::kVSlots), (r / C::kVSlots) & 1u, 20000000ull);
     if (it > 0) mbar_wait_teardown(bars.q_full(), (it - 1) & 1u, 20000000ull);
+    if (do_it > 0) mbar_wait_teardown(bars.do_full(), (do_it - 1) & 1u, 20000000ull);
   }
 }
 
@@ -453,7 +456,6 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
     dq_decode(p, u, bh, i);
     const int n = dq_kv_blocks(p, i);
     if (!mbar_wait(bars.q_full(), it & 1u, wc)) { ok = false; break; }
-    ++it;
     // S_0 = Q K_0^T once the softmax warps have read the previous S.
     int slotK = kr.slot;
     if (!mbar_wait(bars.kfull(slotK), kr.phase, wc)) { ok = false; break; }
@@ -463,8 +465,12 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
     issue_ss<D, DT>(leader, tS, q_lo, k_kmaj0 + slotK * kTileW);
     umma_commit_if(leader, bars.s_full());
     ++s_issued;
+    // Q and dO go back to the producer once the unit's last S and dP
+    // products (the commit covers every earlier product) have read them.
+    if (n == 1) umma_commit_if(leader, bars.q_empty());
     // dP_0 = dO V_0^T.
     {
+      if (!mbar_wait(bars.do_full(), it & 1u, wc)) { ok = false; break; }
       const int slotV = vr.slot;
       if (!mbar_wait(bars.vfull(slotV), vr.phase, wc)) { ok = false; break; }
       vr.advance();
@@ -472,7 +478,9 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
       issue_ss<D, DT>(leader, tDP, do_lo, v_kmaj0 + slotV * kTileW);
       umma_commit_if(leader, bars.dp_full());
       umma_commit_if(leader, bars.vempty(slotV));
+      if (n == 1) umma_commit_if(leader, bars.do_empty());
     }
+    ++it;
     for (int j = 0; j < n; ++j) {
       const bool has_next = j + 1 < n;
       int slotKn = slotK;
@@ -492,6 +500,7 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
         issue_ss<D, DT>(leader, tS, q_lo, k_kmaj0 + slotKn * kTileW);
         umma_commit_if(leader, bars.s_full());
         ++s_issued;
+        if (j + 2 == n) umma_commit_if(leader, bars.q_empty());
       }
       // dQ (+)= dS_j K_j once dS_j is in TMEM; the first product of a unit
       // overwrites dQ, after the previous unit's epilogue has read it.
@@ -509,23 +518,16 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
         issue_ss<D, DT>(leader, tDP, do_lo, v_kmaj0 + slotV * kTileW);
         umma_commit_if(leader, bars.dp_full());
         umma_commit_if(leader, bars.vempty(slotV));
+        if (j + 2 == n) umma_commit_if(leader, bars.do_empty());
       }
       slotK = slotKn;
     }
     if (!ok) break;
     umma_commit_if(leader, bars.dq_done());
-    umma_commit_if(leader, bars.q_empty());
     ++units;
   }
   umma_commit_if(leader, bars.drain());
   mbar_wait_teardown(bars.drain(), 0u, ok ? 2000000000ull : 20000000ull);
-}
-
-__device__ __forceinline__ void st_global_v4(void* ptr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
 }
 
 // Packed fp32 pair product (sm_100+), beside the pair FMA / add of fa_ptx.cuh:
@@ -537,7 +539,7 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
 }
 
 template <int D, int DT>
-__device__ void dq_softmax(const BwdParams& p, void* dq_out, uint32_t tmem, int warp, int lane,
+__device__ void dq_softmax(const BwdParams& p, uint32_t tmem, int warp, int lane,
                            const DqBars& bars, const WaitCtl& wc) {
   using C = DqCfg<D>;
   const int quad = warp & 3, half = warp >> 2;
@@ -546,10 +548,9 @@ __device__ void dq_softmax(const BwdParams& p, void* dq_out, uint32_t tmem, int 
   const uint32_t tS = tmem + lane_off + C::kS + 64 * half;
   const uint32_t tDP = tmem + lane_off + C::kDP + 64 * half;
   const uint32_t tDS = tmem + lane_off + C::kDS + 32 * half;
-  const uint32_t tDQ = tmem + lane_off + C::kDQ;
   // A masked score is -inf and must give p = 0: keep the scale positive.
   const float sl2 = fmaxf(p.scale_log2, 1e-30f);
-  uint32_t s_ph = 0, dp_ph = 0, dq_ph = 0;
+  uint32_t s_ph = 0, dp_ph = 0;
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0;; ++w) {
     const int u = unit_of_round(w, grid, bid);
@@ -632,40 +633,42 @@ __device__ void dq_softmax(const BwdParams& p, void* dq_out, uint32_t tmem, int 
       if (lane == 0) mbar_arrive(bars.ds_ready());
     }
     if (!ok) break;
-    // Epilogue: dQ = scale * (dS K), 16-bit, this thread's row written with
-    // 16-byte stores (rows past S_q are not written).
+  }
+}
+
+// dQ epilogue (warps 12-15, one TMEM lane quarter each): once a unit's last
+// product is done, dQ = scale * (dS K) is read out of TMEM and handed back
+// to the issuing warp, then written as 16-bit, one row per thread with
+// 16-byte stores (rows past S_q are not written).
+template <int D, int DT>
+__device__ void dq_epilogue(const BwdParams& p, void* dq_out, uint32_t tmem, int warp, int lane,
+                            const DqBars& bars, const WaitCtl& wc) {
+  using C = DqCfg<D>;
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;
+  const uint32_t tDQ = tmem + (static_cast<uint32_t>(quad * 32) << 16) + C::kDQ;
+  uint32_t dq_ph = 0;
+  const int grid = gridDim.x, bid = blockIdx.x;
+  for (int w = 0;; ++w) {
+    const int u = unit_of_round(w, grid, bid);
+    if (u >= p.num_units) break;
+    int bh, i;
+    dq_decode(p, u, bh, i);
+    const int64_t qi = static_cast<int64_t>(i) * 128 + r;
     if (!mbar_wait(bars.dq_done(), dq_ph, wc)) break;
     dq_ph ^= 1u;
     tc_fence_after();
-    if (D == 128 || half == 0) {
-      uint32_t a0[32], a1[32];
-      tmem_ld_x32(tDQ + 64 * half, a0);
-      tmem_ld_x32(tDQ + 64 * half + 32, a1);
-      tmem_wait_ld();
-      reg_dep_x32(a0);
-      reg_dep_x32(a1);
-      if (qi < p.S_q) {
-        const int64_t b = bh / p.H, h = bh - b * p.H;
-        const int64_t off = b * p.dq_st[0] + h * p.dq_st[1] + qi * p.dq_st[2] + 64 * half;
-        uint8_t* dst = static_cast<uint8_t*>(dq_out) + off * 2;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int c = 4 * q;
-          st_global_v4(dst + 16 * q,
-                       pack2<DT>(__uint_as_float((c < 16 ? a0 : a1)[(2 * c) & 31]) * p.scale,
-                                 __uint_as_float((c < 16 ? a0 : a1)[(2 * c + 1) & 31]) * p.scale),
-                       pack2<DT>(__uint_as_float((c < 16 ? a0 : a1)[(2 * c + 2) & 31]) * p.scale,
-                                 __uint_as_float((c < 16 ? a0 : a1)[(2 * c + 3) & 31]) * p.scale),
-                       pack2<DT>(__uint_as_float((c < 16 ? a0 : a1)[(2 * c + 4) & 31]) * p.scale,
-                                 __uint_as_float((c < 16 ? a0 : a1)[(2 * c + 5) & 31]) * p.scale),
-                       pack2<DT>(__uint_as_float((c < 16 ? a0 : a1)[(2 * c + 6) & 31]) * p.scale,
-                                 __uint_as_float((c < 16 ? a0 : a1)[(2 * c + 7) & 31]) * p.scale));
-        }
-      }
-    }
+    uint32_t pk[D / 2];
+    load_row<D, DT>(tDQ, p.scale, false, pk);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.dq_free());
+    if (qi < p.S_q) {
+      const int64_t b = bh / p.H, h = bh - b * p.H;
+      store_row<D>(static_cast<uint8_t*>(dq_out) +
+                       (b * p.dq_st[0] + h * p.dq_st[1] + qi * p.dq_st[2]) * 2,
+                   pk);
+    }
   }
 }
 
@@ -694,12 +697,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bars.q_full(), 1);
     mbar_init(bars.q_empty(), 1);
+    mbar_init(bars.do_full(), 1);
+    mbar_init(bars.do_empty(), 1);
     mbar_init(bars.s_full(), 1);
     mbar_init(bars.s_free(), 8);
     mbar_init(bars.dp_full(), 1);
     mbar_init(bars.ds_ready(), 8);
     mbar_init(bars.dq_done(), 1);
-    mbar_init(bars.dq_free(), 8);
+    mbar_init(bars.dq_free(), 4);
     mbar_init(bars.drain(), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -725,11 +730,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
   if (warp < kProducerWarp) {
-    dq_softmax<D, DT>(p, dq_out, tmem, warp, lane, bars, wc);
-  } else if (warp == kProducerWarp) {
-    dq_producer<D>(p, &tmQ, &tmK, &tmV, &tmDO, base, bars, wc);
-  } else if (warp == kMmaWarp) {
-    dq_mma<D, DT>(p, tmem, base, bars, wc);
+    reg_alloc_inc<kRegSoftmax>();
+    dq_softmax<D, DT>(p, tmem, warp, lane, bars, wc);
+  } else if (warp < kEpiWarp0) {
+    reg_alloc_dec<kRegControl>();
+    if (warp == kProducerWarp)
+      dq_producer<D>(p, &tmQ, &tmK, &tmV, &tmDO, base, bars, wc);
+    else if (warp == kMmaWarp)
+      dq_mma<D, DT>(p, tmem, base, bars, wc);
+  } else {
+    reg_alloc_dec<kRegEpilogue>();
+    dq_epilogue<D, DT>(p, dq_out, tmem, warp, lane, bars, wc);
   }
   __syncwarp();
   tc_fence_before();
@@ -752,7 +763,7 @@ struct KvCfg {
   static constexpr int kVOff = T::kBytes;
   static constexpr int kRingOff = 2 * T::kBytes;
   static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-  static constexpr int kNumBars = 2 * kStages + 8;
+  static constexpr int kNumBars = 2 * kStages + 10;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
@@ -761,9 +772,6 @@ struct KvCfg {
   // dS^T (16-bit pairs) overwrite the first 32 columns of each 64-column half
   // of S^T and dP^T.
   static constexpr uint32_t kS = 0, kDP = 128, kDV = 256, kDK = 256 + D;
-  // Epilogue staging reuses the K / V tiles: one 4 KB box per 64 output
-  // columns per warp.
-  static constexpr int kEpiBox = 32 * 128;
 };
 
 struct KvBars {
@@ -771,13 +779,15 @@ struct KvBars {
   __device__ uint32_t full(int s) const { return base + 8u * s; }
   __device__ uint32_t empty(int s) const { return base + 8u * (2 + s); }
   __device__ uint32_t kv_full() const { return base + 8u * 4; }
-  __device__ uint32_t epi_done() const { return base + 8u * 5; }
+  __device__ uint32_t dv_free() const { return base + 8u * 5; }  // dV read by the epilogue
   __device__ uint32_t s_full() const { return base + 8u * 6; }
   __device__ uint32_t p_ready() const { return base + 8u * 7; }
   __device__ uint32_t dp_full() const { return base + 8u * 8; }
   __device__ uint32_t ds_ready() const { return base + 8u * 9; }
   __device__ uint32_t dkv_done() const { return base + 8u * 10; }
   __device__ uint32_t drain() const { return base + 8u * 11; }
+  __device__ uint32_t kv_empty() const { return base + 8u * 12; }  // K, V read by their last products
+  __device__ uint32_t dk_free() const { return base + 8u * 13; }   // dK read by the epilogue
 };
 
 struct KvUnit {
@@ -817,17 +827,17 @@ __device__ void kv_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
   // The whole warp runs this role; one elected lane issues (see elect_one).
   const bool leader = elect_one();
   Ring<C::kStages> ring;
-  uint32_t issued = 0, units = 0, kv_loads = 0;
+  uint32_t issued = 0, kv_loads = 0;
   bool ok = true;
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0; ok; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
     const KvUnit k = kv_decode(p, u);
-    // K / V smem doubles as the previous unit's epilogue staging.
-    if (units > 0 && !mbar_wait(bars.epi_done(), (units - 1) & 1u, wc)) { ok = false; break; }
-    ++units;
     if (k.n_steps == 0) continue;
+    // The previous K / V tiles are reloaded once that unit's last S^T and
+    // dP^T products have read them: the load overlaps its last step.
+    if (kv_loads > 0 && !mbar_wait(bars.kv_empty(), (kv_loads - 1) & 1u, wc)) { ok = false; break; }
     if (leader) mbar_arrive_expect_tx(bars.kv_full(), 2 * T::kBytes);
     for (int c = 0; c < T::kChunks && leader; ++c) {
       tma_tile(smem + C::kKOff + c * T::kChunkBytes, tmK, bars.kv_full(), p.layout, c * 64,
@@ -881,14 +891,22 @@ __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const K
   const uint32_t q_mn0 = umma_desc_lo(smem + C::kRingOff, T::kChunkBytes);
   const uint32_t tS = tmem + C::kS, tDP = tmem + C::kDP, tDV = tmem + C::kDV, tDK = tmem + C::kDK;
   Ring<C::kStages> ring;
-  uint32_t kv_loads = 0, p_ph = 0, ds_ph = 0;
+  uint32_t kv_loads = 0, p_ph = 0, ds_ph = 0, units = 0;
   bool ok = true;
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0; ok; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
     const KvUnit k = kv_decode(p, u);
+    // The previous unit's epilogue must have read dV (dK) from TMEM before
+    // this unit's first dV (dK) product overwrites it -- and both before this
+    // unit's dkv_done, so that its phases never run two ahead of the epilogue.
+    const bool acc_wait = units > 0;
+    const uint32_t acc_ph = (units - 1u) & 1u;
+    ++units;
     if (k.n_steps == 0) {
+      if (acc_wait && (!mbar_wait(bars.dv_free(), acc_ph, wc) ||
+                       !mbar_wait(bars.dk_free(), acc_ph, wc))) { ok = false; break; }
       umma_commit_if(leader, bars.dkv_done());  // nothing to accumulate: dK = dV = 0
       continue;
     }
@@ -902,6 +920,9 @@ __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const K
     umma_commit_if(leader, bars.s_full());
     issue_ss<D, DT>(leader, tDP, v_lo, q_kmaj0 + st * kStageW + kTileW);
     umma_commit_if(leader, bars.dp_full());
+    // K and V go back to the producer after the unit's last S^T and dP^T
+    // (the commit covers every earlier product).
+    if (k.n_steps == 1) umma_commit_if(leader, bars.kv_empty());
     for (int s = 0; s < k.n_steps; ++s) {
       const bool has_next = s + 1 < k.n_steps;
       // Probed together without blocking: bit 0 P^T written, 1 the next
@@ -912,6 +933,7 @@ __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const K
       // dV (+)= P^T dO_s.
       if (!(done & 1u) && !mbar_wait(bars.p_ready(), p_ph, wc)) { ok = false; break; }
       p_ph ^= 1u;
+      if (s == 0 && acc_wait && !mbar_wait(bars.dv_free(), acc_ph, wc)) { ok = false; break; }
       tc_fence_after();
       issue_ts<D, DT, true>(leader, tDV, tS, q_mn0 + st * kStageW + kTileW, s > 0 ? 1u : 0u);
       int st_n = st;
@@ -926,12 +948,14 @@ __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const K
       // dK (+)= dS^T Q_s.
       if (!(done & 4u) && !mbar_wait(bars.ds_ready(), ds_ph, wc)) { ok = false; break; }
       ds_ph ^= 1u;
+      if (s == 0 && acc_wait && !mbar_wait(bars.dk_free(), acc_ph, wc)) { ok = false; break; }
       tc_fence_after();
       issue_ts<D, DT, true>(leader, tDK, tDP, q_mn0 + st * kStageW, s > 0 ? 1u : 0u);
       umma_commit_if(leader, bars.empty(st));
       if (has_next) {
         issue_ss<D, DT>(leader, tDP, v_lo, q_kmaj0 + st_n * kStageW + kTileW);
         umma_commit_if(leader, bars.dp_full());
+        if (s + 2 == k.n_steps) umma_commit_if(leader, bars.kv_empty());
       }
       st = st_n;
     }
@@ -943,11 +967,8 @@ __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const K
 }
 
 template <int D, int DT>
-__device__ void kv_softmax(const BwdParams& p, const CUtensorMap* tmDK, const CUtensorMap* tmDV,
-                           uint32_t tmem, uint32_t smem, int warp, int lane, const KvBars& bars,
-                           const WaitCtl& wc) {
-  // Issues and waits for this warp's bulk stores (see elect_one).
-  const bool leader = elect_one();
+__device__ void kv_softmax(const BwdParams& p, uint32_t tmem, uint32_t smem, int warp, int lane,
+                           const KvBars& bars, const WaitCtl& wc) {
   using C = KvCfg<D>;
   const int quad = warp & 3, half = warp >> 2;
   const int r = quad * 32 + lane;
@@ -957,7 +978,7 @@ __device__ void kv_softmax(const BwdParams& p, const CUtensorMap* tmDK, const CU
   const uint32_t tDV = tmem + lane_off + C::kDV;
   const uint32_t tDK = tmem + lane_off + C::kDK;
   const float sl2 = fmaxf(p.scale_log2, 1e-30f);
-  uint32_t s_ph = 0, dp_ph = 0, done_ph = 0;
+  uint32_t s_ph = 0, dp_ph = 0;
   Ring<C::kStages> ring;
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0;; ++w) {
@@ -1078,44 +1099,55 @@ __device__ void kv_softmax(const BwdParams& p, const CUtensorMap* tmDK, const CU
       if (lane == 0) mbar_arrive(bars.ds_ready());
     }
     if (!ok) break;
-    // Epilogue: dV and dK = scale * (dS^T Q), 16-bit, staged in the K / V
-    // tiles (free once every product of the unit completed), TMA stores
-    // clipped at S_kv.
+  }
+}
+
+// dK / dV epilogue (warps 12-15, one TMEM lane quarter each): once a unit's
+// last product is done, dV, then dK = scale * (dS^T Q), is read out of TMEM,
+// handed back to the issuing warp (the next unit's first dV / dK product
+// overwrites it) and written as 16-bit, one key row per thread with 16-byte
+// stores (rows past S_kv are not written).  A key tile that no query sees
+// writes zeros.
+template <int D, int DT>
+__device__ void kv_epilogue(const BwdParams& p, uint32_t tmem, int warp, int lane,
+                            const KvBars& bars, const WaitCtl& wc) {
+  using C = KvCfg<D>;
+  const int quad = warp & 3;
+  const int r = quad * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  uint32_t done_ph = 0;
+  const int grid = gridDim.x, bid = blockIdx.x;
+  for (int w = 0;; ++w) {
+    const int u = unit_of_round(w, grid, bid);
+    if (u >= p.num_units) break;
+    const KvUnit k = kv_decode(p, u);
+    const int64_t kj = static_cast<int64_t>(k.j) * 128 + r;
     if (!mbar_wait(bars.dkv_done(), done_ph, wc)) break;
     done_ph ^= 1u;
     tc_fence_after();
     const bool zero = k.n_steps == 0;
-    const int32_t row0 = k.j * 128 + quad * 32;
-    const bool in_range = row0 < p.S_kv;
-    if (D == 128) {
-      const uint32_t stV = smem + static_cast<uint32_t>(warp) * 2 * C::kEpiBox;
-      store_box64<DT>(tDV + 64 * half, 1.0f, zero, stV, lane, leader, tmDV, p.layout, 64 * half,
-                      row0, k.hk, k.b, in_range);
-      store_box64<DT>(tDK + 64 * half, p.scale, zero, stV + C::kEpiBox, lane, leader, tmDK,
-                      p.layout, 64 * half, row0, k.hk, k.b, in_range);
-    } else if (half == 0) {
-      const uint32_t stV = smem + static_cast<uint32_t>(warp) * 2 * C::kEpiBox;
-      store_box64<DT>(tDV, 1.0f, zero, stV, lane, leader, tmDV, p.layout, 0, row0, k.hk, k.b,
-                      in_range);
-      store_box64<DT>(tDK, p.scale, zero, stV + C::kEpiBox, lane, leader, tmDK, p.layout, 0, row0,
-                      k.hk, k.b, in_range);
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {  // dV, then dK
+      uint32_t pk[D / 2];
+      load_row<D, DT>(tmem + lane_off + (which ? C::kDK : C::kDV), which ? p.scale : 1.0f, zero,
+                      pk);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(which ? bars.dk_free() : bars.dv_free());
+      if (kj < p.S_kv) {
+        const int64_t* st = which ? p.dk_st : p.dv_st;
+        store_row<D>(static_cast<uint8_t*>(which ? p.dk : p.dv) +
+                         (k.b * st[0] + k.hk * st[1] + kj * st[2]) * 2,
+                     pk);
+      }
     }
-    // The staging boxes are the next unit's K / V tiles: their stores must
-    // have read them before the producer reloads.
-    if (leader) bulk_wait_group_read0();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars.epi_done());
   }
-  if (leader) bulk_wait_group0();
-  __syncwarp();
 }
 
 template <int D, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                       const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const __grid_constant__ BwdParams p) {
   using C = KvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -1132,7 +1164,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bars.empty(s), 1);
     }
     mbar_init(bars.kv_full(), 1);
-    mbar_init(bars.epi_done(), 8);
+    mbar_init(bars.dv_free(), 4);
+    mbar_init(bars.dk_free(), 4);
+    mbar_init(bars.kv_empty(), 1);
     mbar_init(bars.s_full(), 1);
     mbar_init(bars.p_ready(), 8);
     mbar_init(bars.dp_full(), 1);
@@ -1147,8 +1181,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
-    tma_prefetch_desc(&tmDK);
-    tma_prefetch_desc(&tmDV);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -1165,11 +1197,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // grid finishes only after the dQ kernel has, so that work queued after the
   // backward on the stream sees dQ too.
   if (warp < kProducerWarp) {
-    kv_softmax<D, DT>(p, &tmDK, &tmDV, tmem, base, warp, lane, bars, wc);
-  } else if (warp == kProducerWarp) {
-    kv_producer<D>(p, &tmQ, &tmK, &tmV, &tmDO, base, bars, wc);
-  } else if (warp == kMmaWarp) {
-    kv_mma<D, DT>(p, tmem, base, bars, wc);
+    reg_alloc_inc<kRegSoftmax>();
+    kv_softmax<D, DT>(p, tmem, base, warp, lane, bars, wc);
+  } else if (warp < kEpiWarp0) {
+    reg_alloc_dec<kRegControl>();
+    if (warp == kProducerWarp)
+      kv_producer<D>(p, &tmQ, &tmK, &tmV, &tmDO, base, bars, wc);
+    else if (warp == kMmaWarp)
+      kv_mma<D, DT>(p, tmem, base, bars, wc);
+  } else {
+    reg_alloc_dec<kRegEpilogue>();
+    kv_epilogue<D, DT>(p, tmem, warp, lane, bars, wc);
   }
   griddep_wait();
   __syncwarp();
@@ -1184,8 +1222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Host-side launchers (explicit instantiations in fa_bwd_inst_*.cu).
 template <int D, int DT>
 cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& dout, void* dq_ptr, const CUtensorMap& dk,
-                          const CUtensorMap& dv, const void* o, const void* dout_ptr,
+                          const CUtensorMap& dout, void* dq_ptr, const void* o, const void* dout_ptr,
                           const float* lse, float* lse2, float* dsum, const BwdParams& p_dq,
                           const BwdParams& p_kv, int grid_dq, int grid_kv, int grid_prep,
                           cudaStream_t stream) {
@@ -1231,7 +1268,7 @@ cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
     cfg.stream = stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, q, k, v, dout, dk, dv, p_kv);
+    e = cudaLaunchKernelEx(&cfg, kern, q, k, v, dout, p_kv);
   }
   return e;
 }
@@ -1243,6 +1280,6 @@ cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
 #define FA_BWD_INSTANTIATE(PREFIX, D, DT)                                                      \
   PREFIX template cudaError_t fa::bwd::launch_fa_bwd<D, DT>(                                   \
       const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, void*,   \
-      const CUtensorMap&, const CUtensorMap&, const void*, const void*,                        \
+      const void*, const void*,                                                                \
       const float*, float*, float*, const fa::bwd::BwdParams&, const fa::bwd::BwdParams&, int, \
       int, int, cudaStream_t);
