@@ -785,14 +785,16 @@ fa_status_t run_backward(const void* q, const void* k, const void* v, const void
 
   DeviceInfo dev;
   if (device_info(&dev) != FA_OK) return FA_ERR_CUDA;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdk, mdv;
   fa_strides_t ts[8];  // q, k, v, o, dout, dq, dk, dv
   if (strides) {
     for (int i = 0; i < 8; ++i) ts[i] = strides[i];
     if (!make_map_strided(&mq, q, dtype, B, H, S_q, D, ts[0]) ||
         !make_map_strided(&mk, k, dtype, B, H_kv, S_kv, D, ts[1]) ||
         !make_map_strided(&mv, v, dtype, B, H_kv, S_kv, D, ts[2]) ||
-        !make_map_strided(&mdo, dout, dtype, B, H, S_q, D, ts[4]))
+        !make_map_strided(&mdo, dout, dtype, B, H, S_q, D, ts[4]) ||
+        !make_map_strided(&mdk, dk, dtype, B, H_kv, S_kv, D, ts[6], 16) ||
+        !make_map_strided(&mdv, dv, dtype, B, H_kv, S_kv, D, ts[7], 16))
       return FA_ERR_CUDA;
     layout = FA_LAYOUT_BNSD;  // the maps take BNSD coordinates
   } else {
@@ -802,7 +804,9 @@ fa_status_t run_backward(const void* q, const void* k, const void* v, const void
     if (!make_map(&mq, q, dtype, layout, B, H, S_q, D) ||
         !make_map(&mk, k, dtype, layout, B, H_kv, S_kv, D) ||
         !make_map(&mv, v, dtype, layout, B, H_kv, S_kv, D) ||
-        !make_map(&mdo, dout, dtype, layout, B, H, S_q, D))
+        !make_map(&mdo, dout, dtype, layout, B, H, S_q, D) ||
+        !make_map(&mdk, dk, dtype, layout, B, H_kv, S_kv, D, 16) ||
+        !make_map(&mdv, dv, dtype, layout, B, H_kv, S_kv, D, 16))
       return FA_ERR_CUDA;
   }
 
@@ -825,14 +829,12 @@ fa_status_t run_backward(const void* q, const void* k, const void* v, const void
   p.dsum = dsum;
   p.err = dev.err_word;
   p.wait_limit_ns = g_wait_limit_ns.load();
-  p.dk = dk;
-  p.dv = dv;
-  const fa_strides_t* sp5[5] = {&ts[3], &ts[4], &ts[5], &ts[6], &ts[7]};
-  int64_t* dst5[5] = {p.o_st, p.do_st, p.dq_st, p.dk_st, p.dv_st};
-  for (int i = 0; i < 5; ++i) {
-    dst5[i][0] = sp5[i]->batch;
-    dst5[i][1] = sp5[i]->head;
-    dst5[i][2] = sp5[i]->seq;
+  const fa_strides_t* sp3[3] = {&ts[3], &ts[4], &ts[5]};
+  int64_t* dst3[3] = {p.o_st, p.do_st, p.dq_st};
+  for (int i = 0; i < 3; ++i) {
+    dst3[i][0] = sp3[i]->batch;
+    dst3[i][1] = sp3[i]->head;
+    dst3[i][2] = sp3[i]->seq;
   }
 
   // dQ: one unit per (query head, query tile); causal runs group heads so
@@ -871,17 +873,17 @@ fa_status_t run_backward(const void* q, const void* k, const void* v, const void
   const int grid_p = static_cast<int>(prep_blocks < 8ll * dev.sm_count ? prep_blocks : 8ll * dev.sm_count);
   cudaError_t e;
   if (dtype == FA_DTYPE_F16)
-    e = (D == 64) ? fa::bwd::launch_fa_bwd<64, fa::bwd::kF16>(mq, mk, mv, mdo, dq, o, dout,
+    e = (D == 64) ? fa::bwd::launch_fa_bwd<64, fa::bwd::kF16>(mq, mk, mv, mdo, dq, mdk, mdv, o, dout,
                                                               lse, lse2, dsum, pq, pk, grid_q,
                                                               grid_k, grid_p, stream)
-                  : fa::bwd::launch_fa_bwd<128, fa::bwd::kF16>(mq, mk, mv, mdo, dq, o,
+                  : fa::bwd::launch_fa_bwd<128, fa::bwd::kF16>(mq, mk, mv, mdo, dq, mdk, mdv, o,
                                                                dout, lse, lse2, dsum, pq, pk,
                                                                grid_q, grid_k, grid_p, stream);
   else
-    e = (D == 64) ? fa::bwd::launch_fa_bwd<64, fa::bwd::kBF16>(mq, mk, mv, mdo, dq, o,
+    e = (D == 64) ? fa::bwd::launch_fa_bwd<64, fa::bwd::kBF16>(mq, mk, mv, mdo, dq, mdk, mdv, o,
                                                                dout, lse, lse2, dsum, pq, pk,
                                                                grid_q, grid_k, grid_p, stream)
-                  : fa::bwd::launch_fa_bwd<128, fa::bwd::kBF16>(mq, mk, mv, mdo, dq, o,
+                  : fa::bwd::launch_fa_bwd<128, fa::bwd::kBF16>(mq, mk, mv, mdo, dq, mdk, mdv, o,
                                                                 dout, lse, lse2, dsum, pq, pk,
                                                                 grid_q, grid_k, grid_p, stream);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;

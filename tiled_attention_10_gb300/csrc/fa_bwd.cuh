@@ -80,13 +80,10 @@ struct BwdParams {
   const float* dsum;      // [B*H, S_q_pad]: rowsum(dO * O); 0 for rows >= S_q
   uint32_t* err;
   uint64_t wait_limit_ns;
-  // dK and dV (written by the dK/dV epilogue).
-  void* dk;
-  void* dv;
   // Element strides (batch, head, seq) of the tensors read or written
-  // without a tensor map: O and dO by the row-statistics pass, dQ, dK and dV
-  // by the epilogues.  D is contiguous.
-  int64_t o_st[3], do_st[3], dq_st[3], dk_st[3], dv_st[3];
+  // without a tensor map: O and dO by the row-statistics pass, dQ by the dQ
+  // epilogue.  D is contiguous.
+  int64_t o_st[3], do_st[3], dq_st[3];
 };
 
 template <int D>
@@ -107,6 +104,21 @@ __device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, u
     tma_load_4d(dst, map, bar, c0, s, h, b);
   else
     tma_load_4d(dst, map, bar, c0, h, s, b);
+}
+
+__device__ __forceinline__ void tma_store_tile(const CUtensorMap* map, uint32_t src, int layout,
+                                               int32_t c0, int32_t s, int32_t h, int32_t b) {
+  if (layout == 0)
+    tma_store_4d(map, src, c0, s, h, b);
+  else
+    tma_store_4d(map, src, c0, h, s, b);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 
 __device__ __forceinline__ void mbar_wait_teardown(uint32_t bar, uint32_t parity, uint64_t limit) {
@@ -762,7 +774,11 @@ struct KvCfg {
   static constexpr int kKOff = 0;
   static constexpr int kVOff = T::kBytes;
   static constexpr int kRingOff = 2 * T::kBytes;
-  static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
+  // Epilogue staging: per epilogue warp 16 rows x 2 * D bytes, as 128-byte
+  // swizzled boxes of 16 rows x 128 bytes (one per 64 columns).
+  static constexpr int kEpiOff = kRingOff + kStages * kStageBytes;
+  static constexpr int kEpiWarpBytes = 16 * 2 * D;
+  static constexpr int kBarOff = kEpiOff + 4 * kEpiWarpBytes;
   static constexpr int kNumBars = 2 * kStages + 10;
   static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
@@ -1105,23 +1121,28 @@ __device__ void kv_softmax(const BwdParams& p, uint32_t tmem, uint32_t smem, int
 // dK / dV epilogue (warps 12-15, one TMEM lane quarter each): once a unit's
 // last product is done, dV, then dK = scale * (dS^T Q), is read out of TMEM,
 // handed back to the issuing warp (the next unit's first dV / dK product
-// overwrites it) and written as 16-bit, one key row per thread with 16-byte
-// stores (rows past S_kv are not written).  A key tile that no query sees
-// writes zeros.
+// overwrites it) and rounded to 16-bit; each warp then stages its 32 key rows
+// in two rounds of 16 in shared memory and writes them by TMA stores, which
+// clip rows past S_kv (the tensor cores, reading their operands from the same
+// shared memory, lose far less to these than to per-thread row stores).  A
+// key tile that no query sees writes zeros.
 template <int D, int DT>
-__device__ void kv_epilogue(const BwdParams& p, uint32_t tmem, int warp, int lane,
-                            const KvBars& bars, const WaitCtl& wc) {
+__device__ void kv_epilogue(const BwdParams& p, const CUtensorMap* tmDK, const CUtensorMap* tmDV,
+                            uint32_t tmem, uint32_t smem, int warp, int lane, const KvBars& bars,
+                            const WaitCtl& wc) {
   using C = KvCfg<D>;
+  // Issues this warp's bulk stores and waits for them (a bulk async-group
+  // belongs to the thread that committed it; see elect_one).
+  const bool leader = elect_one();
   const int quad = warp & 3;
-  const int r = quad * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+  const uint32_t stage = smem + C::kEpiOff + static_cast<uint32_t>(quad * C::kEpiWarpBytes);
   uint32_t done_ph = 0;
   const int grid = gridDim.x, bid = blockIdx.x;
   for (int w = 0;; ++w) {
     const int u = unit_of_round(w, grid, bid);
     if (u >= p.num_units) break;
     const KvUnit k = kv_decode(p, u);
-    const int64_t kj = static_cast<int64_t>(k.j) * 128 + r;
     if (!mbar_wait(bars.dkv_done(), done_ph, wc)) break;
     done_ph ^= 1u;
     tc_fence_after();
@@ -1134,20 +1155,41 @@ __device__ void kv_epilogue(const BwdParams& p, uint32_t tmem, int warp, int lan
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(which ? bars.dk_free() : bars.dv_free());
-      if (kj < p.S_kv) {
-        const int64_t* st = which ? p.dk_st : p.dv_st;
-        store_row<D>(static_cast<uint8_t*>(which ? p.dk : p.dv) +
-                         (k.b * st[0] + k.hk * st[1] + kj * st[2]) * 2,
-                     pk);
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        // The previous stores from the staging boxes must have read them.
+        if (leader) bulk_wait_group_read0();
+        __syncwarp();
+        if ((lane >> 4) == rr) {
+          const int rl = lane & 15;
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              st_shared_v4(stage + h * 2048 + rl * 128 + ((c ^ (rl & 7)) << 4), pk[32 * h + 4 * c],
+                           pk[32 * h + 4 * c + 1], pk[32 * h + 4 * c + 2], pk[32 * h + 4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int32_t row = k.j * 128 + quad * 32 + 16 * rr;
+        if (leader && row < p.S_kv) {
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h)
+            tma_store_tile(which ? tmDK : tmDV, stage + h * 2048, p.layout, 64 * h, row, k.hk, k.b);
+          bulk_commit_group();
+        }
       }
     }
   }
+  if (leader) bulk_wait_group0();
+  __syncwarp();
 }
 
 template <int D, int DT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const __grid_constant__ BwdParams p) {
   using C = KvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -1181,6 +1223,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmDK);
+    tma_prefetch_desc(&tmDV);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -1207,7 +1251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       kv_mma<D, DT>(p, tmem, base, bars, wc);
   } else {
     reg_alloc_dec<kRegEpilogue>();
-    kv_epilogue<D, DT>(p, tmem, warp, lane, bars, wc);
+    kv_epilogue<D, DT>(p, &tmDK, &tmDV, tmem, base, warp, lane, bars, wc);
   }
   griddep_wait();
   __syncwarp();
@@ -1222,7 +1266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Host-side launchers (explicit instantiations in fa_bwd_inst_*.cu).
 template <int D, int DT>
 cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                          const CUtensorMap& dout, void* dq_ptr, const void* o, const void* dout_ptr,
+                          const CUtensorMap& dout, void* dq_ptr, const CUtensorMap& dk,
+                          const CUtensorMap& dv, const void* o, const void* dout_ptr,
                           const float* lse, float* lse2, float* dsum, const BwdParams& p_dq,
                           const BwdParams& p_kv, int grid_dq, int grid_kv, int grid_prep,
                           cudaStream_t stream) {
@@ -1268,7 +1313,7 @@ cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
     cfg.stream = stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, q, k, v, dout, p_kv);
+    e = cudaLaunchKernelEx(&cfg, kern, q, k, v, dout, dk, dv, p_kv);
   }
   return e;
 }
@@ -1280,6 +1325,6 @@ cudaError_t launch_fa_bwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
 #define FA_BWD_INSTANTIATE(PREFIX, D, DT)                                                      \
   PREFIX template cudaError_t fa::bwd::launch_fa_bwd<D, DT>(                                   \
       const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, void*,   \
-      const void*, const void*,                                                                \
+      const CUtensorMap&, const CUtensorMap&, const void*, const void*,                        \
       const float*, float*, float*, const fa::bwd::BwdParams&, const fa::bwd::BwdParams&, int, \
       int, int, cudaStream_t);
