@@ -45,7 +45,7 @@ typedef enum { FA_DTYPE_F16 = 0, FA_DTYPE_BF16 = 1, FA_DTYPE_FP8E4M3 = 2 } fa_dt
 /* Status codes.  Errors are returned, never thrown or trapped. */
 typedef enum {
   FA_OK = 0,
-  FA_ERR_INVALID_ARG = 1,    /* null pointer, size < 1, non-finite or negative scale,
+  FA_ERR_INVALID_ARG = 1,    /* null pointer, size < 1, non-finite scale,
                                 descale given for a 16-bit dtype, bad enum              */
   FA_ERR_UNSUPPORTED = 2,    /* D not in {64, 128}, or a size past the library's limits  */
   FA_ERR_MISALIGNED = 3,     /* a tensor pointer not 16-byte aligned (TMA requirement)   */
@@ -66,12 +66,12 @@ typedef enum {
  *      row's softmax denominator including `scale` (and the descales).
  * B, H, S_q, S_kv, D   sizes; all >= 1, D in {64, 128}.  Offsets are 64-bit:
  *      a single tensor may exceed 4 GB (the Hygon retrospective, defect 1).
- * scale  finite, >= 0; multiplies Q K^T before the softmax (commonly D^-0.5).
- *      A narrowing of the definition: the reference attention of the Ascend
- *      page (section 4.3) holds for any real scale, but the kernel takes each
- *      row's maximum of the unscaled scores, which is the maximum of the
- *      scaled ones only for scale >= 0; a negative scale is refused with
- *      FA_ERR_INVALID_ARG (negate q, or k, and pass -scale instead).
+ * scale  finite, of either sign (the reference attention of the Ascend page,
+ *      section 4.3, holds for any real scale); multiplies Q K^T before the
+ *      softmax (commonly D^-0.5).  For a negative scale the tensor cores
+ *      compute -Q K^T (the products' negate-B bit) and the softmax works with
+ *      |scale|, so that a row's maximum of the scores it sees is that of the
+ *      scaled scores either way.
  * layout FA_LAYOUT_BNSD or FA_LAYOUT_BSND (o follows q's layout).
  * causal 0: every key visible.  Non-zero: query row i sees key j only if j <= i
  *      (top-left aligned, the verifier's triu(diagonal=1) mask; with S_q == S_kv

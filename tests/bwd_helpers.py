@@ -54,7 +54,7 @@ def head_bounds(t, q, k, v, do, o_in, lse_in, scale, dtype):
     vis = P > 0
     # exponent error of P (log2 units) -> relative error eta
     A = aq @ ak.T
-    sl2 = scale * LOG2E
+    sl2 = abs(scale) * LOG2E                          # error terms scale with |scale|
     s2 = np.where(vis, t["S"] * LOG2E, 0.0)           # S * log2(e), S already scaled
     lse2 = lse_in * LOG2E
     x = np.where(vis, s2 - lse2[:, None], 0.0)
@@ -71,8 +71,8 @@ def head_bounds(t, q, k, v, do, o_in, lse_in, scale, dtype):
     e_ds32 = P * eta * g + P * (ddp + dD[:, None]) * (1 + eta) + 2 * 2.0 ** -24 * P * g
     eps_ds16 = e_ds32 * (1 + u) + u * np.abs(dS) + a16 * vis
     ads = np.abs(dS)
-    b_dk = scale * (eps_ds16.T @ aq + S_q * GAM * (ads.T @ aq))
-    b_dq = scale * (eps_ds16 @ ak + S_kv * GAM * (ads @ ak))
+    b_dk = abs(scale) * (eps_ds16.T @ aq + S_q * GAM * (ads.T @ aq))
+    b_dq = abs(scale) * (eps_ds16 @ ak + S_kv * GAM * (ads @ ak))
     return b_dq, b_dk, b_dv
 
 

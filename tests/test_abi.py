@@ -56,7 +56,7 @@ def _call(**over):
     (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1), (dict(lse=None), 1),
     (dict(B=0), 1), (dict(H=0), 1), (dict(S_q=0), 1), (dict(S_kv=0), 1), (dict(D=0), 1),
     (dict(S_kv=-5), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
-    (dict(scale=-1.0), 1), (dict(layout=7), 1), (dict(dtype=9), 1),
+    (dict(scale=float("-inf")), 1), (dict(layout=7), 1), (dict(dtype=9), 1),
     (dict(dq=16), 1),                                   # descale with a 16-bit dtype
     (dict(D=96), 2), (dict(D=256), 2), (dict(D=64, dtype="e4m3"), 2),
     (dict(S_q=1 << 31), 2),

@@ -12,6 +12,8 @@ step passes) or, end to end, from the GPU forward pass.  Plus: canaries after
 every output intact, no NaN / Inf, bit-identical repeat runs, argument
 checks that launch nothing.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -118,6 +120,15 @@ def test_bwd_parity(case, cuda_lib):
 def test_bwd_end_to_end_from_gpu_forward(dtype, causal, cuda_lib):
     w = Workload("bwd", 2, 4, 384, 384, 128, dtype, "BNSD", causal, seed=40)
     _run_case(w, end_to_end=True)
+
+
+@pytest.mark.parametrize("dtype,causal,D", [("bf16", True, 128), ("f16", False, 64)])
+def test_bwd_negative_scale(dtype, causal, D, cuda_lib):
+    """A negative scale: S is computed as -Q K^T (and -K Q^T) with |scale| in
+    the exponent, dQ and dK are multiplied by the signed scale."""
+    w = Workload("bwd", 1, 4, 300, 300, D, dtype, "BNSD", causal, seed=21, H_kv=2,
+                 scale=-1.0 / math.sqrt(D))
+    _run_case(w)
 
 
 def test_bwd_deterministic(cuda_lib):

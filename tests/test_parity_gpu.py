@@ -4,6 +4,8 @@ Small shapes span several 128-row tiles and ragged tails; every output row is
 compared.  Tolerances are the max-abs bounds of the method's specification:
 O within 4e-3 (fp16), 1.6e-2 (bf16), 6e-2 (fp8 e4m3); lse within 1e-3.
 """
+import math
+
 import pytest
 import torch
 
@@ -57,6 +59,16 @@ def test_parity_fp8(S_q, S_kv, causal, cuda_lib):
 @pytest.mark.parametrize("scale", [0.0, 0.02, 1.0])
 def test_parity_scales(scale, cuda_lib):
     w = Workload("t", 1, 2, 200, 260, 128, "bf16", "BNSD", True, scale=scale, seed=4)
+    run_small(w)
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f16", 64), ("e4m3", 128), ("bf16", 64)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_parity_negative_scale(dtype, D, causal, cuda_lib):
+    """A negative scale: the definition holds for any real scale; the
+    products then compute -Q K^T and the softmax works with |scale|."""
+    w = Workload("t", 1, 3, 200, 333, D, dtype, "BSND", causal, scale=-1.0 / math.sqrt(D),
+                 seed=11 + D)
     run_small(w)
 
 

@@ -81,6 +81,13 @@ def test_splitkv_parity_dtypes_layouts(dtype, layout, cuda_lib):
     _run(w, 4)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_splitkv_negative_scale(causal, cuda_lib):
+    """A negative scale through the split path and the merge."""
+    w = Workload("t", 1, 4, 130, 1500, 128, "bf16", "BNSD", causal, scale=-0.3, seed=12)
+    _run(w, 4)
+
+
 def test_splitkv_more_splits_than_blocks(cuda_lib):
     """Splits beyond the key blocks are empty: zero weight, never read."""
     w = Workload("t", 1, 2, 200, 300, 128, "bf16", "BNSD", False, seed=4)

@@ -79,12 +79,15 @@ VARLEN_CASES = [
     ([40, 1, 257, 130], [100, 700, 257, 65], 4, 1, 128, "bf16", 2),
     ([64, 260], [64, 513], 2, 2, 128, "e4m3", 2),
     ([300, 17], [300, 17], 8, 8, 64, "bf16", 1),
+    # a negative scale (optional eighth field: the scale's sign)
+    ([300, 17, 900], [300, 700, 900], 4, 2, 128, "bf16", 1, -1.0),
+    ([64, 260], [64, 513], 2, 2, 128, "e4m3", 2, -1.0),
 ]
 
 
 @pytest.mark.parametrize("case", range(len(VARLEN_CASES)))
 def test_varlen_parity(case, cuda_lib):
-    seq_q, seq_k, H, H_kv, D, dtype, causal = VARLEN_CASES[case]
+    seq_q, seq_k, H, H_kv, D, dtype, causal, *sign = VARLEN_CASES[case]
     g = np.random.default_rng(100 + case)
     cu_q = np.concatenate([[0], np.cumsum(seq_q)]).astype(np.int32)
     cu_k = np.concatenate([[0], np.cumsum(seq_k)]).astype(np.int32)
@@ -92,7 +95,7 @@ def test_varlen_parity(case, cuda_lib):
     q, dq = _rand((tq, H, D), dtype, g)
     k, dk = _rand((tk, H_kv, D), dtype, g)
     v, dv = _rand((tk, H_kv, D), dtype, g)
-    scale = 1.0 / np.sqrt(D)
+    scale = (sign[0] if sign else 1.0) / np.sqrt(D)
     O, L = ov.attention_varlen(q, k, v, cu_q=cu_q, cu_k=cu_k, H=H, H_kv=H_kv, D=D, scale=scale,
                                causal_mode=causal, dtype=dtype, descale=(dq, dk, dv))
     out = Out(tq, H, D, dtype, unused_rows=7)   # 7 trailing rows belong to no sequence

@@ -389,7 +389,7 @@ fa_status_t check_args(const void* q, const void* k, const void* v, const void* 
   if (layout != FA_LAYOUT_BNSD && layout != FA_LAYOUT_BSND) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP8E4M3)
     return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || scale < 0.0f) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_FP8E4M3 && (descale_q || descale_k || descale_v)) return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   if (dtype == FA_DTYPE_FP8E4M3 && D != 128) return FA_ERR_UNSUPPORTED;
@@ -589,7 +589,9 @@ fa_status_t run_forward(const void* q, const void* k, const void* v, void* o, fl
   p.group_heads = static_cast<int32_t>(group);
   p.layout = static_cast<int32_t>(layout);
   p.causal = causal ? 1 : 0;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  // A negative scale: the products give -Q K^T and the softmax takes |scale|.
+  p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.neg_scale = scale < 0.0f ? 1 : 0;
   p.descale_q = descale_q;
   p.descale_k = descale_k;
   p.descale_v = descale_v;
@@ -823,7 +825,9 @@ fa_status_t run_backward(const void* q, const void* k, const void* v, const void
   p.n_kv_tiles = static_cast<int32_t>(n_kv);
   p.layout = static_cast<int32_t>(layout);
   p.causal = causal ? 1 : 0;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  // A negative scale: the products give -Q K^T and the softmax takes |scale|.
+  p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.neg_scale = scale < 0.0f ? 1 : 0;
   p.scale = scale;
   p.lse2 = lse2;
   p.dsum = dsum;
@@ -956,7 +960,7 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
   if (causal < 0 || causal > 2) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP8E4M3)
     return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || scale < 0.0f) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_FP8E4M3 && (descale_q || descale_k || descale_v)) return FA_ERR_INVALID_ARG;
   if (paged) {
     if (max_pages < 1 || num_pages < 1 || page_size < 16) return FA_ERR_INVALID_ARG;
@@ -1034,7 +1038,9 @@ fa_status_t run_var(const void* q, const void* k, const void* v, void* o, float*
   p.layout = 1;
   p.causal = causal != 0 ? 1 : 0;
   p.causal_br = causal == 2 ? 1 : 0;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  // A negative scale: the products give -Q K^T and the softmax takes |scale|.
+  p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.neg_scale = scale < 0.0f ? 1 : 0;
   p.descale_q = descale_q;
   p.descale_k = descale_k;
   p.descale_v = descale_v;

@@ -74,8 +74,9 @@ struct BwdParams {
   int32_t num_units;
   int32_t group_heads;    // heads (dq) / key-value heads (dkdv) per scheduling group
   int32_t layout, causal;
-  float scale_log2;       // scale * log2(e)
+  float scale_log2;       // |scale| * log2(e)
   float scale;
+  int32_t neg_scale;      // scale < 0: S (S^T) is computed as -Q K^T (-K Q^T)
   const float* lse2;      // [B*H, S_q_pad]: lse * log2(e); +inf for rows >= S_q
   const float* dsum;      // [B*H, S_q_pad]: rowsum(dO * O); 0 for rows >= S_q
   uint32_t* err;
@@ -412,10 +413,12 @@ __device__ void dq_producer(const BwdParams& p, const CUtensorMap* tmQ, const CU
 // K-major x K-major product over the head dim: D[128 x 128] = A[128 x D] B[128 x D]^T.
 template <int D, int DT>
 __device__ __forceinline__ void issue_ss(bool leader, uint32_t d_tmem, uint32_t a_lo,
-                                         uint32_t b_lo) {
+                                         uint32_t b_lo, bool neg_b = false) {
   using T = Tile<D>;
   constexpr uint32_t hi = umma_desc_hi_sw128(1024);
-  constexpr uint32_t idesc = umma_idesc(DT == kBF16 ? 1u : 0u, false, 128, 128);
+  // neg_b: B negated (instruction descriptor bit 14), for S with a negative scale.
+  const uint32_t idesc =
+      umma_idesc(DT == kBF16 ? 1u : 0u, false, 128, 128) | (neg_b ? 1u << 14 : 0u);
 #pragma unroll
   for (int kk = 0; kk < T::kDSteps; ++kk) {
     const uint32_t off =
@@ -474,7 +477,7 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
     kr.advance();
     if (s_issued > 0 && !mbar_wait(bars.s_free(), (s_issued - 1) & 1u, wc)) { ok = false; break; }
     tc_fence_after();
-    issue_ss<D, DT>(leader, tS, q_lo, k_kmaj0 + slotK * kTileW);
+    issue_ss<D, DT>(leader, tS, q_lo, k_kmaj0 + slotK * kTileW, p.neg_scale != 0);
     umma_commit_if(leader, bars.s_full());
     ++s_issued;
     // Q and dO go back to the producer once the unit's last S and dP
@@ -509,7 +512,7 @@ __device__ void dq_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const D
         kr.advance();
         if (!(done & 2u) && !mbar_wait(bars.s_free(), (s_issued - 1) & 1u, wc)) { ok = false; break; }
         tc_fence_after();
-        issue_ss<D, DT>(leader, tS, q_lo, k_kmaj0 + slotKn * kTileW);
+        issue_ss<D, DT>(leader, tS, q_lo, k_kmaj0 + slotKn * kTileW, p.neg_scale != 0);
         umma_commit_if(leader, bars.s_full());
         ++s_issued;
         if (j + 2 == n) umma_commit_if(leader, bars.q_empty());
@@ -932,7 +935,7 @@ __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const K
     if (!mbar_wait(bars.full(st), ring.phase, wc)) { ok = false; break; }
     ring.advance();
     tc_fence_after();
-    issue_ss<D, DT>(leader, tS, k_lo, q_kmaj0 + st * kStageW);
+    issue_ss<D, DT>(leader, tS, k_lo, q_kmaj0 + st * kStageW, p.neg_scale != 0);
     umma_commit_if(leader, bars.s_full());
     issue_ss<D, DT>(leader, tDP, v_lo, q_kmaj0 + st * kStageW + kTileW);
     umma_commit_if(leader, bars.dp_full());
@@ -958,7 +961,7 @@ __device__ void kv_mma(const BwdParams& p, uint32_t tmem, uint32_t smem, const K
         if (!(done & 2u) && !mbar_wait(bars.full(st_n), ring.phase, wc)) { ok = false; break; }
         ring.advance();
         tc_fence_after();
-        issue_ss<D, DT>(leader, tS, k_lo, q_kmaj0 + st_n * kStageW);
+        issue_ss<D, DT>(leader, tS, k_lo, q_kmaj0 + st_n * kStageW, p.neg_scale != 0);
         umma_commit_if(leader, bars.s_full());
       }
       // dK (+)= dS^T Q_s.
