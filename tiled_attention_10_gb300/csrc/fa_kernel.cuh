@@ -195,6 +195,61 @@ __device__ __forceinline__ int tile_kv_blocks(const KernelParams& p, int q_tile)
   return static_cast<int>(max_col / kBN) + 1;
 }
 
+// A CTA's work units in order: unit u of [0, num_units) goes to one CTA by
+// the static snake (unit_of_round).  In the varlen / paged modes the snake
+// runs over the units that hold query rows only: a query-tile pair past a
+// sequence's length is empty, and as a slot of its own it would leave its
+// CTA a unit short of the others (32 heads of 32 sequences of 512-8192
+// tokens, causal: the busiest CTA 13 % above an even share, 2 % with the
+// empty units left out of the count).  Each role walks the list itself; all
+// get the same sequence.
+template <int kMode>
+struct UnitWalk {
+  int w = 0;       // this CTA's next round
+  int rank = 0;    // varlen / paged: the group (rank, si) the walk is at,
+  int si = 0;      // and the units with rows before it
+  int64_t k = 0;
+  __device__ __forceinline__ bool next(const KernelParams& p, int grid, int bid, int& u) {
+    // (A single pair index -- decoding, short prompts -- leaves only
+    // sequences without queries empty: the plain snake, without the walk's
+    // loads on every unit's path (they cost 2 % on decoding).)
+    if (kMode < kModeVarlen || p.n_pairs <= 1) {
+      u = unit_of_round(w, grid, bid);
+      ++w;
+      return u < p.num_units;
+    } else {
+      // Units with rows, counted in list order, that this CTA takes next.
+      const int64_t t = static_cast<int64_t>(w) * grid + ((w & 1) ? (grid - 1 - bid) : bid);
+      const int groups = static_cast<int>(p.H) >> p.q_pack_log2;
+      const int ns = kMode == kModePagedSplit ? p.n_splits : 1;
+      const int64_t gsz = static_cast<int64_t>(groups) * ns;  // units per (rank, sequence)
+      const int tile_log2 = 7 - p.q_pack_log2;                  // tokens per query tile
+      while (rank < p.n_pairs) {
+        const int pair = p.n_pairs - 1 - rank;
+        const int seq = p.seq_order ? min(max(p.seq_order[si], 0), p.n_seqs - 1) : si;
+        const int64_t q_len =
+            min(max(static_cast<int64_t>(p.cu_q[seq + 1]) - p.cu_q[seq], int64_t(0)), p.S_q);
+        const int64_t tiles = (q_len + (int64_t(1) << tile_log2) - 1) >> tile_log2;
+        if (pair < (tiles + 1) / 2) {
+          if (t < k + gsz) {
+            // The same unit index decode_item takes: ((rank * n_seqs + si)
+            // * groups + head group) * n_splits + split.
+            u = static_cast<int>((static_cast<int64_t>(rank) * p.n_seqs + si) * gsz + (t - k));
+            ++w;
+            return true;
+          }
+          k += gsz;
+        }
+        if (++si == p.n_seqs) {
+          si = 0;
+          ++rank;
+        }
+      }
+      return false;
+    }
+  }
+};
+
 // Work item u = (unit, split): the unit's K/V blocks are cut into n_splits
 // chunks of equal length; the item covers blocks [lo, lo + chunk) and tile t
 // processes n[t] of them (0: nothing for that tile).  With n_splits = 1 an
@@ -429,9 +484,8 @@ __device__ void producer_role(const KernelParams& p, const CUtensorMap* tmQ,
   bool ok = true;
   const uint64_t pol_stream = l2_policy_evict_first();
   const int grid = gridDim.x, bid = blockIdx.x;
-  for (int w = 0; ok; ++w) {
-    const int u = unit_of_round(w, grid, bid);
-    if (u >= p.num_units) break;
+  UnitWalk<kMode> walk;
+  for (int u; ok && walk.next(p, grid, bid, u);) {
     const Item item = decode_item<kMode>(p, u);
     const int bh = item.bh, pair = item.pair;
     // First query head of the tile (varlen / paged: of the head group) and
@@ -710,9 +764,8 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
   uint32_t p_phase[2] = {0u, 0u};
   bool ok = true;
   const int grid = gridDim.x, bid = blockIdx.x;
-  for (int w = 0; ok; ++w) {
-    const int u = unit_of_round(w, grid, bid);
-    if (u >= p.num_units) break;
+  UnitWalk<kMode> walk;
+  for (int u; ok && walk.next(p, grid, bid, u);) {
     const Item item = decode_item<kMode>(p, u);
     const int n[2] = {item.n[0], item.n[1]};
     const int nmax = max(n[0], n[1]);
@@ -1035,9 +1088,8 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
   uint32_t s_phase = 0u, o_phase = 0u, solo_phase = 0u;
   uint32_t ring_pos = 0u;   // K/V ring positions consumed by earlier items
   const int grid = gridDim.x, bid = blockIdx.x;
-  for (int w = 0;; ++w) {
-    const int u = unit_of_round(w, grid, bid);
-    if (u >= p.num_units) break;
+  UnitWalk<kMode> walk;
+  for (int u; walk.next(p, grid, bid, u);) {
     const Item item = decode_item<kMode>(p, u);
     const int bh = item.bh;
     // A solo item's two slots work on the same tile, qt.
