@@ -63,7 +63,6 @@ namespace fa {
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // key/value rows per tile
-constexpr int kThreads = 384;
 // Kernel modes: the whole pass over dense [B,H,S,D] tensors, the split-KV
 // pass (partials in a workspace), packed variable-length sequences, and
 // packed queries against a paged K/V cache.
@@ -73,6 +72,7 @@ constexpr int kModeDense = 0, kModeSplit = 1, kModeVarlen = 2, kModePaged = 3;
 constexpr int kModePagedSplit = 4;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kCorrWarp0 = 12;  // e4m3: the correction warpgroup (warps 12-15)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kDtF16 = 0, kDtBF16 = 1, kDtE4M3 = 2;
 
@@ -135,8 +135,11 @@ struct Cfg {
   // written by the warp and drained by a TMA store: 8 warps x 4 KB.
   static constexpr int kEpiBoxBytes = 32 * 128;
   static constexpr int kEpiOffset = kQBytes + kSlots * kTileBytes;
-  static constexpr int kBarOffset = kEpiOffset + 8 * kEpiBoxBytes;
-  static constexpr int kNumBars = 2 * kSlots + 13;
+  // e4m3: each block's O-rescale factors (per tile, one fp32 per row), handed
+  // from the softmax warps to the correction warpgroup.
+  static constexpr int kAlphaOffset = kEpiOffset + 8 * kEpiBoxBytes;
+  static constexpr int kBarOffset = kAlphaOffset + (kFp8 ? 2 * 128 * 4 : 0);
+  static constexpr int kNumBars = 2 * kSlots + 17;
   static constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;  // + align slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static constexpr uint32_t kFmt = kFp8 ? 0u : (DT == kDtBF16 ? 1u : 0u);
@@ -153,9 +156,20 @@ struct Cfg {
   // decoding, ring bookkeeping, the issuing warp's barrier probes) need ~100.
   // D = 64 runs ~2 % faster with 192 / 120 (2x16x4097x64 causal 86.4 -> 84.8
   // us); D = 128 keeps 200 / 104 (192 / 120 made e4m3 1.8 % slower).
-  static constexpr uint32_t kRegSoftmax = D == 64 ? 192 : 200;
-  static constexpr uint32_t kRegControl = D == 64 ? 120 : 104;
-  static_assert(256 * kRegSoftmax + 128 * kRegControl == 384 * 168, "register budget");
+  // e4m3 runs a fourth warpgroup (512 threads, launched at 128 registers):
+  // the correction warps, which rescale O when a block moves a row's max --
+  // on most e4m3 blocks, since the max moves on every increase (see
+  // kRescaleThreshold) -- so that the softmax warps do not wait for O's TMEM
+  // round trip (a probe that skipped it: 338 -> 274 us on 1x32x8192 causal).
+  // 16-bit P moves the max rarely and keeps three warpgroups.
+  static constexpr bool kCorr = kFp8;
+  static constexpr int kThreads = kCorr ? 512 : 384;
+  static constexpr uint32_t kRegSoftmax = kCorr ? 184 : (D == 64 ? 192 : 200);
+  static constexpr uint32_t kRegControl = kCorr ? 72 : (D == 64 ? 120 : 104);
+  static constexpr uint32_t kRegCorr = 72;
+  static_assert(kCorr ? 2 * kRegSoftmax + kRegControl + kRegCorr == 4 * 128
+                      : 256 * kRegSoftmax + 128 * kRegControl == 384 * 168,
+                "register budget");
   // log2 of P's scale: e4m3 P holds 256 * p (= 2^(x + 8)), so that weights
   // down to 2^-17 of the row max stay representable; the row sum l then
   // carries the same factor, which O / l cancels and the LSE subtracts.
@@ -417,6 +431,10 @@ struct Bars {
   // slot 1's O (one arrival per thread of the warpgroup).
   __device__ uint32_t solo_ml() const { return base + 8u * (2 * ns + 11); }
   __device__ uint32_t solo_read() const { return base + 8u * (2 * ns + 12); }
+  // e4m3 correction: tile t's rescale factors of the block are in shared
+  // memory / its O is rescaled (one per block and tile).
+  __device__ uint32_t alpha_ready(int t) const { return base + 8u * (2 * ns + 13 + t); }
+  __device__ uint32_t o_ready(int t) const { return base + 8u * (2 * ns + 15 + t); }
 };
 
 // Short bounded wait used only while tearing down after an abort: it ignores
@@ -668,6 +686,7 @@ struct RingPos {
 // order the producer loads them.  Returns false if a wait gave up.
 template <int D, int DT>
 __device__ bool mma_solo_unit(bool leader, const Item& item, RingPos& rp, uint32_t (&p_phase)[2],
+                              uint32_t (&o_rphase)[2],
                               uint32_t q_lo, uint32_t k_lo0, uint32_t v_lo0, const uint32_t (&tS)[2],
                               const uint32_t (&tO)[2], const bool (&rf)[2], uint32_t idesc_qk,
                               const Bars& bars, const WaitCtl& wc) {
@@ -714,6 +733,10 @@ __device__ bool mma_solo_unit(bool leader, const Item& item, RingPos& rp, uint32
       const RingPos& vt = t ? v[1] : v[0];
       const RingPos& kt = t ? k[1] : k[0];
       if (!mbar_wait(bars.p_half(t, 0), p_phase[t], wc)) return false;
+      if constexpr (C::kCorr) {
+        if (!mbar_wait(bars.o_ready(t), o_rphase[t], wc)) return false;
+        o_rphase[t] ^= 1u;
+      }
       if (!mbar_wait(bars.full(vt.slot), vt.phase, wc)) return false;
       tc_fence_after();
       issue_pv_half<D, DT, 0>(leader, tO[t], tS[t], v_lo0 + vt.slot * kTileW, j > 0 ? 1u : 0u);
@@ -762,6 +785,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
   RingPos rp;
   uint32_t it = 0;
   uint32_t p_phase[2] = {0u, 0u};
+  uint32_t o_rphase[2] = {0u, 0u};  // e4m3: o_ready phases
   bool ok = true;
   const int grid = gridDim.x, bid = blockIdx.x;
   UnitWalk<kMode> walk;
@@ -778,7 +802,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
     if constexpr (kMode == kModeDense) {
       if (item.solo) {
         const bool rf[2] = {rf0, rf1};
-        if (!mma_solo_unit<D, DT>(leader, item, rp, p_phase, q_lo[0], k_lo0, v_lo0, tS, tO, rf,
+        if (!mma_solo_unit<D, DT>(leader, item, rp, p_phase, o_rphase, q_lo[0], k_lo0, v_lo0, tS, tO, rf,
                                   idesc_qk, bars, wc)) {
           ok = false;
           break;
@@ -834,6 +858,11 @@ __device__ void mma_role(const KernelParams& p, uint32_t tmem, uint32_t sQ, uint
         if (!((done >> t) & 1u) && !mbar_wait(bars.p_half(t, 0), p_phase[t], wc)) {
           ok = false;
           break;
+        }
+        // e4m3: the correction warps have rescaled O_t for this block.
+        if constexpr (C::kCorr) {
+          if (!mbar_wait(bars.o_ready(t), o_rphase[t], wc)) { ok = false; break; }
+          o_rphase[t] ^= 1u;
         }
         if (!v_ready) {
           if (!(done & 4u) && !mbar_wait(bars.full(slotV), phV, wc)) { ok = false; break; }
@@ -894,6 +923,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+__device__ __forceinline__ void st_shared_f1(uint32_t addr, float a) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
+}
+__device__ __forceinline__ float ld_shared_f1(uint32_t addr) {
+  float a;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(a) : "r"(addr) : "memory");
+  return a;
+}
+
 __device__ __forceinline__ void st_shared_f2(uint32_t addr, float a, float b) {
   asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
 }
@@ -909,7 +947,7 @@ __device__ __forceinline__ void ld_shared_f2(uint32_t addr, float& a, float& b) 
 template <int D, int DT, bool kMasked>
 __device__ __forceinline__ void softmax_block(float (&s)[128], int lim, int j, float sl2,
                                               float& m_run, float& l, uint32_t tS, uint32_t tO,
-                                              const Bars& bars, int t) {
+                                              uint32_t alpha_slot, const Bars& bars, int t) {
   using C = Cfg<D, DT>;
   // Masked columns become -inf: they drop out of the max and give p = 0.
   if constexpr (kMasked) {
@@ -947,8 +985,13 @@ __device__ __forceinline__ void softmax_block(float (&s)[128], int lim, int j, f
   const float m_sub = (m_run == -CUDART_INF_F) ? 0.0f : m_run;
   // O_t *= alpha for the rows whose max moved, before any PV of this block
   // accumulates into O (O is complete: the commit that signalled S_j
-  // covered the previous PV; this block's PV waits for P below).
-  if (__any_sync(0xffffffffu, resc)) {
+  // covered the previous PV; this block's PV waits for P below).  e4m3: the
+  // correction warps do it (correction_role) while this warp computes P; it
+  // hands them the row's factor, 1 when the max did not move.
+  if constexpr (C::kCorr) {
+    st_shared_f1(alpha_slot, alpha);
+    mbar_arrive(bars.alpha_ready(t));
+  } else if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t ov[32];
@@ -1062,6 +1105,9 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t tS = tmem + lane_off + C::kTmemS + t * kBN;
   const uint32_t tO = tmem + lane_off + C::kTmemO + t * 128;
+  // e4m3: this row's slot for the block's O-rescale factor.
+  const uint32_t alpha_slot =
+      sEpi + static_cast<uint32_t>(C::kAlphaOffset - C::kEpiOffset + (t * 128 + r) * 4);
   constexpr bool kVarSplit = kMode == kModePagedSplit;
   constexpr bool kSplit = kMode == kModeSplit;    // dense split: [n*B, H, S_q, D] partials
   constexpr bool split = kSplit || kVarSplit;     // fp32 partial O and lse
@@ -1169,9 +1215,9 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
       const bool masked = (col0 + kBN > k_len) || (p.causal && col0 + (kBN - 1) > tile_row0 + item.off);
       const int lim = static_cast<int>(max(min(col_end - col0, static_cast<int64_t>(kBN)), int64_t(0)));
       if (masked)
-        softmax_block<D, DT, true>(s, lim, j, sl2, m_run, l, tS, tO, bars, t);
+        softmax_block<D, DT, true>(s, lim, j, sl2, m_run, l, tS, tO, alpha_slot, bars, t);
       else
-        softmax_block<D, DT, false>(s, kBN, j, sl2, m_run, l, tS, tO, bars, t);
+        softmax_block<D, DT, false>(s, kBN, j, sl2, m_run, l, tS, tO, alpha_slot, bars, t);
     }
     if (!ok) break;
 
@@ -1336,10 +1382,61 @@ __device__ void softmax_role(const KernelParams& p, const CUtensorMap* tmO, cons
 }
 
 // ---------------------------------------------------------------------------
+// e4m3 correction warpgroup (warps 12-15, one TMEM lane quarter each): for
+// every block of every tile slot, in the order the issuing warp takes them,
+// O_t *= alpha (the row's factor the softmax handed over) when any row of
+// the warp's quarter moved its max, then O_t is released for the block's PV
+// product.  The softmax warps meanwhile compute P.
+// ---------------------------------------------------------------------------
+template <int D, int DT, int kMode>
+__device__ void correction_role(const KernelParams& p, uint32_t tmem, uint32_t sEpi, int warp,
+                                int lane, const Bars& bars, const WaitCtl& wc) {
+  using C = Cfg<D, DT>;
+  const int wq = warp & 3;
+  const int r = wq * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t sAlpha = sEpi + static_cast<uint32_t>(C::kAlphaOffset - C::kEpiOffset);
+  uint32_t a_phase[2] = {0u, 0u};
+  const int grid = gridDim.x, bid = blockIdx.x;
+  UnitWalk<kMode> walk;
+  bool ok = true;
+  for (int u; ok && walk.next(p, grid, bid, u);) {
+    const Item item = decode_item<kMode>(p, u);
+    const int nmax = max(item.n[0], item.n[1]);
+    for (int j = 0; j < nmax && ok; ++j) {
+      for (int t = 0; t < 2; ++t) {
+        if (j >= (t ? item.n[1] : item.n[0])) continue;
+        if (!mbar_wait(bars.alpha_ready(t), a_phase[t], wc)) { ok = false; break; }
+        a_phase[t] ^= 1u;
+        const float alpha = ld_shared_f1(sAlpha + static_cast<uint32_t>((t * 128 + r) * 4));
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+          tc_fence_after();
+          const uint32_t tO = tmem + lane_off + C::kTmemO + t * 128;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld_x32(tO + 32 * c, ov);
+            tmem_wait_ld();
+            reg_dep_x32(ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st_x32(tO + 32 * c, ov);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.o_ready(t));
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int D, int DT, int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D, DT>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                   const __grid_constant__ CUtensorMap tmOp, const __grid_constant__ KernelParams p) {
@@ -1372,6 +1469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bars.drain(), 1);
     mbar_init(bars.solo_ml(), 128);
     mbar_init(bars.solo_read(), 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars.alpha_ready(t), 128);
+      mbar_init(bars.o_ready(t), 4);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1403,6 +1504,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kProducerWarp) {
     reg_alloc_inc<C::kRegSoftmax>();
     softmax_role<D, DT, kMode>(p, &tmO, &tmOp, tmem, sEpi, warp, lane, bars, wc);
+  } else if (C::kCorr && warp >= kCorrWarp0) {
+    reg_alloc_dec<C::kRegCorr>();
+    correction_role<D, DT, kMode>(p, tmem, sEpi, warp, lane, bars, wc);
   } else {
     reg_alloc_dec<C::kRegControl>();
     if (warp == kProducerWarp) {
@@ -1444,7 +1548,7 @@ cudaError_t launch_fa_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUte
   pp.idesc_qk = p.neg_scale ? C::kIdescQKNeg : C::kIdescQK;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
