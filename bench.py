@@ -37,6 +37,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 
 
 FWD_SOURCES = ("fa_api.cu", "fa_kernel.cuh", "fa_ptx.cuh", "fa_tmem_io.cuh", "fa_inst_*.cu")
+BWD_SOURCES = ("fa_api.cu", "fa_bwd.cuh", "fa_ptx.cuh", "fa_tmem_io.cuh", "fa_bwd_inst_*.cu")
 
 
 def _code_only(text: str) -> str:
@@ -47,13 +48,14 @@ def _code_only(text: str) -> str:
     return " ".join(text.split())
 
 
-def kernel_source_sha() -> str:
-    """Hash of the forward kernel's code (kernel, PTX helpers, instantiations and the host
-    code that sets up its launch; comments and layout excluded): ties a recorded ncu capture
-    to the kernel it measured, and a comment edit does not detach it."""
+def kernel_source_sha(sources=FWD_SOURCES) -> str:
+    """Hash of a kernel's code (kernel, PTX helpers, instantiations and the host code that
+    sets up its launch; comments and layout excluded): ties a recorded ncu capture to the
+    kernel it measured, and a comment edit does not detach it.  The forward's files by
+    default; BWD_SOURCES for the backward's kernels."""
     h = hashlib.sha256()
     files = set()
-    for pat in FWD_SOURCES:
+    for pat in sources:
         files.update(glob.glob(os.path.join(ROOT, "tiled_attention_10_gb300", "csrc", pat)))
     for f in sorted(files):
         with open(f, encoding="utf-8") as fh:
@@ -84,15 +86,15 @@ def tensor_peak(peaks, dtype: str, sustained: bool) -> float:
     return base * (2.0 if dtype == "e4m3" else 1.0)
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"fa_fwd_{workload}.ncu.json")
+def recorded_traffic(workload: str, kernel: str = "fa_fwd", sources=FWD_SOURCES):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
+    taken on the current source of that kernel; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.ncu.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
-    if rec.get("kernel_sha") != kernel_source_sha():
+    if rec.get("kernel_sha") != kernel_source_sha(sources):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -740,6 +742,8 @@ def run_ours_bwd(args, w, world, rank, local):
                      **({"frac_of_burst": round(achieved / tensor_peak(peaks, w.dtype, False), 4)}
                         if sustained else {}),
                      "traffic": None,
+                     "traffic_by_kernel": {k: recorded_traffic(w.name, k, BWD_SOURCES)
+                                           for k in ("fa_bwd_dq", "fa_bwd_dkdv")},
                      "scope": "whole fa_bwd step (row statistics + dQ + dK/dV kernels, CUDA "
                               "events around each call)",
                      "executed_frac": round(executed / peak, 4),
