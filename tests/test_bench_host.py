@@ -1,5 +1,7 @@
 """Host-side logic of bench.py, on CPU: the clock summary, the sample FLOP
 count, and the N>1 plumbing (barrier + max over ranks) with two gloo ranks."""
+import glob
+import json
 import os
 import socket
 import subprocess
@@ -31,6 +33,22 @@ def test_peak_choice_follows_run_length_and_power_cap():
     assert not bench.use_sustained_peak(200.0, {})
     assert bench.use_sustained_peak(1500.0, {"reasons": []})
     assert bench.use_sustained_peak(200.0, {"reasons": ["sw_power_cap"]})
+
+
+def test_recorded_traffic_is_tied_to_each_kernels_sources():
+    # a committed ncu record counts only while the sources it was taken on are
+    # unchanged: the forward's records against the forward's files, the
+    # backward's against the backward's
+    fwd, bwd = bench.kernel_source_sha(), bench.kernel_source_sha(bench.BWD_SOURCES)
+    assert fwd != bwd and len(fwd) == len(bwd) == 16
+    for kernel, sources, sha in (("fa_fwd", bench.FWD_SOURCES, fwd),
+                                 ("fa_bwd_dkdv", bench.BWD_SOURCES, bwd)):
+        for path in glob.glob(os.path.join(ROOT, "profiles", f"{kernel}_*.ncu.json")):
+            rec = json.load(open(path))
+            workload = os.path.basename(path)[len(kernel) + 1:-len(".ncu.json")]
+            got = bench.recorded_traffic(workload, kernel, sources)
+            assert got == (rec["dram_bytes_per_launch"] if rec["kernel_sha"] == sha else None)
+    assert bench.recorded_traffic("no_such_workload") is None
 
 
 def test_sample_flops_matches_nominal_formula_on_full_problem():
