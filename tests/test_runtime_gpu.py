@@ -1,5 +1,7 @@
 """Runtime behaviour on the GPU: determinism, streams, the bounded-wait
 timeout path, and that a call with bad arguments launches nothing."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -153,6 +155,55 @@ def test_dependent_calls_back_to_back(split, cuda_lib):
         assert float(np.abs(o2.float().cpu().double().numpy() - O2).max()) <= 1.6e-2
         assert float(np.abs(l2.cpu().double().numpy() - L2).max()) <= 1e-3
         q.copy_(q_host.to("cuda"))   # restore Q for the next round
+
+
+@pytest.mark.gpu
+def test_e4m3_and_bf16_calls_back_to_back(cuda_lib):
+    """The e4m3 forward runs 512 threads (its O correction warpgroup), the
+    16-bit one 384; chained on one stream with no synchronisation in between:
+    a bf16 call reads the e4m3 call's O as its Q, then a second e4m3 call
+    overwrites that O while the bf16 call may still be running.  Bit for bit
+    against the same three calls synchronised one by one."""
+    S, H, D = 512, 8, 128
+    scale = 1.0 / math.sqrt(D)
+    xa = make_inputs(Workload("t", 1, H, S, S, D, "e4m3", "BNSD", True, seed=33), device="cuda")
+    xc = make_inputs(Workload("t", 1, H, S, S, D, "e4m3", "BNSD", False, seed=35), device="cuda")
+    xb = make_inputs(Workload("t", 1, H, S, S, D, "bf16", "BNSD", False, seed=34), device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    descale = lambda x: [torch.tensor([d], dtype=torch.float32, device="cuda") for d in x.descale]
+    da, dc = descale(xa), descale(xc)
+
+    def e4m3(x, d, o, lse, causal):
+        st = binding.fa_fwd(x.q.data_ptr(), x.k.data_ptr(), x.v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), 1, H, S, S, D, scale, "BNSD", causal, "e4m3",
+                            d[0].data_ptr(), d[1].data_ptr(), d[2].data_ptr(), stream)
+        assert st == 0, binding.FA_STATUS.get(st)
+
+    def bf16(q, o, lse):
+        st = binding.fa_fwd(q.data_ptr(), xb.k.data_ptr(), xb.v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), 1, H, S, S, D, scale, "BNSD", 0, "bf16", None, None,
+                            None, stream)
+        assert st == 0, binding.FA_STATUS.get(st)
+
+    def outputs():
+        return (torch.empty(1, H, S, D, dtype=torch.bfloat16, device="cuda"),
+                torch.empty(1, H, S, device="cuda"))
+
+    (o1, l1), (o2, l2), (r1, rl1), (r2, rl2), (r3, rl3) = (outputs() for _ in range(5))
+    e4m3(xa, da, r1, rl1, 1)
+    torch.cuda.synchronize()
+    bf16(r1, r2, rl2)
+    torch.cuda.synchronize()
+    e4m3(xc, dc, r3, rl3, 0)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        e4m3(xa, da, o1, l1, 1)
+        bf16(o1, o2, l2)
+        e4m3(xc, dc, o1, l1, 0)
+        torch.cuda.synchronize()
+        assert binding.fa_last_device_error(stream) == 0
+        assert torch.equal(o2.view(torch.int16), r2.view(torch.int16)) and torch.equal(l2, rl2)
+        assert torch.equal(o1.view(torch.int16), r3.view(torch.int16)) and torch.equal(l1, rl3)
 
 
 @pytest.mark.gpu
